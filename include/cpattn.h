@@ -1,0 +1,222 @@
+/*
+ * cpattn.h -- C ABI of the zigzag context-parallel causal attention library
+ * (libcpattn.so, sm_103a).
+ *
+ * The computation is the one described on the page "context-parallel-
+ * multimodal" (xuesongtap.github.io), called "CP-VLM page" below:
+ *
+ *   - §1.1: the text of a sequence is cut into 2P chunks and simulated
+ *     context-parallel rank r keeps the head-tail pair (r, 2P-r-1), gathered
+ *     with index_select on the sequence dimension;
+ *   - §1 and the page's Ring Attention reference: every rank's queries meet
+ *     every rank's keys in ring order, and the per-step partial results are
+ *     merged by log-sum-exp;
+ *   - §4.1: an image-token prefix is replicated, unsplit, to every rank and
+ *     every text query sees all of it;
+ *   - §4.2: every rank obtains its own gradient of the prefix and these are
+ *     summed (the AllReduce);
+ *   - §5.3: packed samples are described by cu_seqlens.
+ *
+ * All P ranks are partitions of one sequence held in one GPU's memory: the
+ * ring "send" is a read of another partition and the AllReduce is a
+ * fixed-order sum on the device.  There are no collectives.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Tensors are caller-owned device memory unless a parameter says "host".
+ *    The library never allocates device memory; scratch lives in a caller-
+ *    supplied workspace whose size the *_workspace_size functions return.
+ *    (It keeps a few page-locked host staging buffers of its own for the
+ *    work lists it uploads.)
+ *  - Every call is asynchronous on `stream` (a cudaStream_t passed as void*;
+ *    NULL = legacy default stream).  Host arrays are read before the call
+ *    returns.  Calls sharing one workspace must be ordered on one stream.
+ *  - Layouts: q, k, v, out, dout, dq, dk, dv are [T][H][d] row-major in
+ *    natural token order ("THD").  lse is [H][T] fp32, natural log of the
+ *    softmax normaliser after the scale:
+ *        lse[h][i] = log sum_{j visible} exp(scale * q_i . k_j).
+ *  - cu_seqlens is n_seqs+1 ascending int32 on the HOST; sample i occupies
+ *    tokens [cu[i], cu[i+1]) and is laid out [prefix (prefix_len tokens),
+ *    text].  Each text length must be divisible by 2P.  The mask is causal
+ *    within each sample over [prefix, text] and blocks across samples.
+ *  - Every device pointer must be 16-byte aligned (CP_ERR_ALIGNMENT).
+ *  - Errors: every call returns a cp_status_t; cp_last_error() gives a
+ *    thread-local message for the last failing call of that thread.  A device
+ *    wait that exceeds its bound (see cp_set_wait_limit) makes the kernel
+ *    record the fact in the workspace and return early; cp_workspace_status()
+ *    reports it as CP_ERR_TIMEOUT.
+ */
+#ifndef CPATTN_H_
+#define CPATTN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define CPATTN_VERSION 1
+
+typedef enum {
+  CP_OK = 0,
+  CP_ERR_INVALID_ARG = 1, /* null pointer, negative size, bad enum */
+  CP_ERR_SHAPE = 2,       /* text length % 2P != 0, d not in {64,128}, ... */
+  CP_ERR_DTYPE = 3,       /* dtype not supported by this entry point */
+  CP_ERR_ALIGNMENT = 4,   /* a device pointer is not 16-byte aligned */
+  CP_ERR_WORKSPACE = 5,   /* workspace missing or smaller than required */
+  CP_ERR_CUDA = 6,        /* a CUDA runtime call failed (message has details) */
+  CP_ERR_TIMEOUT = 7,     /* a bounded device-side wait gave up */
+  CP_ERR_UNSUPPORTED = 8  /* no kernel for this device / configuration */
+} cp_status_t;
+
+typedef enum { CP_F32 = 0, CP_BF16 = 1 } cp_dtype_t;
+
+/* Message for the last failing call made by this thread ("" if none). */
+const char* cp_last_error(void);
+/* Static name of a status code. */
+const char* cp_status_string(cp_status_t s);
+/* CPATTN_VERSION of the loaded library. */
+int cp_version(void);
+
+/*
+ * cp_zigzag_index -- the zigzag gather table and its inverse.
+ * CP-VLM page §1.1 (index = [cp_rank, 2*cp_size-cp_rank-1], index_select on
+ * the sequence dimension), applied to each sample's text (§4.1 step 3, §5.3).
+ *
+ *   fwd_idx[k] (k < P*R, R = sum_i text_len_i / P): natural token index of
+ *     permuted text row k.  Rows are rank-major; within a rank sample-major;
+ *     within a sample chunk r (c_i rows) then chunk 2P-r-1 (c_i rows), where
+ *     c_i = text_len_i / (2P).
+ *   inv_idx[m] (m < sum_i text_len_i): permuted row of the m-th text token in
+ *     natural order (prefix tokens are not counted).
+ *
+ * on_device = 0: fwd_idx / inv_idx are host arrays, filled before return
+ * (stream unused).  on_device = 1: they are device arrays; the tables are
+ * built on the host and copied asynchronously on `stream`.  (Inside
+ * cp_attn_fwd the same table is produced by a device kernel.)  Either pointer
+ * may be NULL to skip that table.
+ * Errors: CP_ERR_INVALID_ARG (n_seqs < 1, P < 1, prefix_len < 0, null
+ * cu_seqlens), CP_ERR_SHAPE (a text length < 0 or not divisible by 2P).
+ */
+cp_status_t cp_zigzag_index(const int32_t* cu_seqlens_h, int n_seqs, int prefix_len, int P,
+                            int32_t* fwd_idx, int32_t* inv_idx, int on_device, void* stream);
+
+/*
+ * cp_zigzag_gather / cp_zigzag_scatter -- the vectorised row permutation of
+ * CP-VLM page §1.1 (index_select) and its inverse.  Rows are `row_bytes`
+ * contiguous bytes (a multiple of 16); idx is a device int32 table of n_rows
+ * entries.  gather: dst[k] = src[idx[k]].  scatter: dst[idx[k]] = src[k].
+ * Bit-exact copies.  src/dst must not overlap.
+ * Errors: CP_ERR_INVALID_ARG, CP_ERR_ALIGNMENT (pointers or row_bytes).
+ */
+cp_status_t cp_zigzag_gather(const void* src, void* dst, size_t row_bytes, const int32_t* idx,
+                             int n_rows, void* stream);
+cp_status_t cp_zigzag_scatter(const void* src, void* dst, size_t row_bytes, const int32_t* idx,
+                              int n_rows, void* stream);
+
+/*
+ * cp_attn_fwd -- context-parallel causal attention forward.
+ * CP-VLM page §1.1 (zigzag split), §1 (Ring Attention), §4.1 (replicated
+ * prefix), §5.3 (cu_seqlens).
+ *
+ * The text rows of q, k, v are gathered into rank-local order (the split),
+ * then for ring step s = 0..P-1 one kernel computes, for every simulated rank
+ * r, the partial attention of its queries over the KV of rank (r-s) mod P
+ * (step 0: [replicated prefix, own chunks]) and merges it by log-sum-exp into
+ * an fp32 running result; the last contributing step writes out/lse in
+ * natural order.  Prefix query rows attend causally to their own prefix once.
+ *
+ *   q, k, v    [T][H][d], dtype dt (CP_BF16: tensor-core path, fp32
+ *              accumulation; CP_F32: fp32 CUDA-core path)
+ *   T          cu_seqlens_h[n_seqs]
+ *   d          64 or 128
+ *   out        [T][H][d], dtype dt (bf16 rounds to nearest even)
+ *   lse        [H][T] fp32
+ *   workspace  >= cp_attn_fwd_workspace_size(...) bytes, 256-byte aligned
+ * Errors: CP_ERR_INVALID_ARG, CP_ERR_SHAPE, CP_ERR_DTYPE, CP_ERR_ALIGNMENT,
+ * CP_ERR_WORKSPACE, CP_ERR_CUDA, CP_ERR_UNSUPPORTED (CP_BF16 on a device
+ * without tcgen05).  T == 0 is a no-op returning CP_OK.
+ */
+size_t cp_attn_fwd_workspace_size(cp_dtype_t dt, int T, int H, int d,
+                                  const int32_t* cu_seqlens_h, int n_seqs, int P,
+                                  int prefix_len);
+cp_status_t cp_attn_fwd(const void* q, const void* k, const void* v, cp_dtype_t dt, int T,
+                        int H, int d, const int32_t* cu_seqlens_h, int n_seqs, int P,
+                        int prefix_len, float softmax_scale, void* out, float* lse,
+                        void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * cp_lse_merge -- merge n_parts partial attention results over disjoint key
+ * sets by log-sum-exp (the Ring Attention combination the CP-VLM page relies
+ * on in §1 and §4.1 step 5):
+ *     lse = log sum_p exp(lse_p),   out = sum_p exp(lse_p - lse) * out_p.
+ * A part with lse = -inf contributes nothing; if every part is -inf the row
+ * gets lse = -inf and out = 0.  Parts are folded in index order.
+ *
+ *   part_out  [n_parts][rows][H][d] fp32       part_lse [n_parts][H][rows] fp32
+ *   out       [rows][H][d], dtype out_dt       lse      [H][rows] fp32
+ * Errors: CP_ERR_INVALID_ARG, CP_ERR_ALIGNMENT, CP_ERR_DTYPE, CP_ERR_CUDA.
+ */
+cp_status_t cp_lse_merge(int n_parts, const float* part_out, const float* part_lse, int rows,
+                         int H, int d, void* out, cp_dtype_t out_dt, float* lse, void* stream);
+
+/*
+ * cp_attn_bwd -- backward of cp_attn_fwd.  CP-VLM page §4.2.
+ *
+ * Uses the final lse of the forward: D_i = dO_i . o_i, then for every ring
+ * step the partial gradients of each rank's queries against the KV it met;
+ * text dK/dV are accumulated for the rank that owns the KV.  At step 0 each
+ * rank produces its own gradient of the replicated prefix K/V; these per-rank
+ * gradients and the prefix queries' own term are summed in fixed order
+ * (ranks 0..P-1, then the prefix-query term) -- the single-GPU stand-in for
+ * the page's AllReduce.
+ *
+ *   q, k, v, out, dout  [T][H][d], dtype dt;  lse [H][T] fp32 (from cp_attn_fwd)
+ *   dq, dk, dv          [T][H][d] fp32 outputs (overwritten)
+ *   prefix_grad_per_rank  NULL, or [2][P+1][n_seqs*prefix_len][H][d] fp32:
+ *                       receives the per-rank prefix dK (slot 0) and dV
+ *                       (slot 1) before the sum; index P = prefix-query term.
+ *   workspace           >= cp_attn_bwd_workspace_size(...) bytes
+ * Errors: as cp_attn_fwd.
+ */
+size_t cp_attn_bwd_workspace_size(cp_dtype_t dt, int T, int H, int d,
+                                  const int32_t* cu_seqlens_h, int n_seqs, int P,
+                                  int prefix_len);
+cp_status_t cp_attn_bwd(const void* q, const void* k, const void* v, const void* out,
+                        const float* lse, const void* dout, cp_dtype_t dt, int T, int H, int d,
+                        const int32_t* cu_seqlens_h, int n_seqs, int P, int prefix_len,
+                        float softmax_scale, float* dq, float* dk, float* dv,
+                        float* prefix_grad_per_rank, void* workspace, size_t ws_bytes,
+                        void* stream);
+
+/*
+ * cp_workspace_status -- synchronise `stream` and report whether a kernel of
+ * the last cp_attn_fwd / cp_attn_bwd call that used `workspace` gave up on a
+ * bounded device wait (CP_ERR_TIMEOUT) or CP_OK.
+ */
+cp_status_t cp_workspace_status(const void* workspace, void* stream);
+
+/*
+ * cp_plan_pairs -- host-only introspection of the ring-step work lists: for
+ * every step s < P, the number of visible (query, key) pairs the forward and
+ * the backward work lists cover (prefix-query pairs are part of step 0) and
+ * the number of work items.  Any output may be NULL.  Needs no GPU.
+ * Errors: CP_ERR_INVALID_ARG, CP_ERR_SHAPE.
+ */
+cp_status_t cp_plan_pairs(const int32_t* cu_seqlens_h, int n_seqs, int prefix_len, int P,
+                          int64_t* fwd_pairs, int64_t* bwd_pairs, int64_t* fwd_items,
+                          int64_t* bwd_items);
+
+/*
+ * cp_set_wait_limit -- bound, in polling rounds, for every device-side wait of
+ * the tensor-core kernels launched afterwards by any thread (<= 0 restores
+ * the default, about a second of waiting).  A test hook for the timeout path.
+ */
+void cp_set_wait_limit(long long rounds);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CPATTN_H_ */

@@ -25,3 +25,13 @@ def pytest_collection_modifyitems(config, items):
     for it in items:
         if "gpu" in it.keywords:
             it.add_marker(skip)
+
+
+@pytest.fixture(scope="session")
+def cplib():
+    """The built library (built in-tree on first use)."""
+    from vlm_zigzag_head_gb300 import _binding, build
+    import os as _os
+    if not _os.path.exists(_binding.lib_path()):
+        build.build()
+    return _binding.lib()

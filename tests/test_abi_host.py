@@ -1,0 +1,131 @@
+"""Host-side checks of the C ABI (no GPU): every declared symbol is exported,
+the host index builder is bit-exact against the oracle, the work lists cover
+exactly the pairs the oracle's masks allow, and bad arguments give the
+documented status codes."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+from vlm_zigzag_head_gb300 import _binding as B
+from vlm_zigzag_head_gb300 import cp_plan_pairs, cp_zigzag_index, workloads
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared_symbols():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", fn)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names |= set(re.findall(r"\b(cp_\w+)\s*\(", src))
+    return names
+
+
+def test_library_exports_every_declared_symbol(cplib):
+    names = _declared_symbols()
+    assert {"cp_attn_fwd", "cp_attn_bwd", "cp_lse_merge", "cp_zigzag_index"} <= names
+    for n in names:
+        assert hasattr(cplib, n), n
+    assert cplib.cp_version() == 1
+    assert set(B.SIGNATURES) >= names
+
+
+def _cu(prefix, texts):
+    cu = [0]
+    for L in texts:
+        cu.append(cu[-1] + prefix + L)
+    return cu
+
+
+CASES = [(2, 0, [256]), (1, 0, [16]), (3, 5, [12, 0, 24]), (4, 576, [1024, 2048, 512]),
+         (8, 3, [32, 16]), (8, 0, [131072]), (4, 2304, [16384, 16384])]
+
+
+@pytest.mark.parametrize("P,N,texts", CASES)
+def test_host_index_bit_exact_vs_oracle(cplib, P, N, texts):
+    cu = _cu(N, texts)
+    fwd, inv = cp_zigzag_index(cu, N, P)
+    ofwd, oinv = oracle.zigzag_index(cu, N, P)
+    assert np.array_equal(fwd.numpy().astype(np.int64), ofwd)
+    assert np.array_equal(inv.numpy().astype(np.int64), oinv)
+
+
+def test_host_index_on_named_workloads(cplib):
+    for name in workloads.WORKLOADS:
+        w = workloads.get(name)
+        cu = workloads.cu_seqlens(w)
+        fwd, inv = cp_zigzag_index(cu, w.prefix_len, w.P)
+        ofwd, oinv = oracle.zigzag_index(cu, w.prefix_len, w.P)
+        assert np.array_equal(fwd.numpy().astype(np.int64), ofwd), name
+        assert np.array_equal(inv.numpy().astype(np.int64), oinv), name
+
+
+@pytest.mark.parametrize("P,N,texts", [(2, 0, [256]), (1, 3, [8]), (3, 5, [12, 0, 24]),
+                                       (4, 130, [1024, 512]), (8, 3, [32, 16]),
+                                       (2, 200, [0, 384])])
+def test_work_lists_cover_exactly_the_visible_pairs(cplib, P, N, texts):
+    """Forward (query tiles x key runs) and backward (key tiles x query runs)
+    work lists cover, per ring step, exactly the pairs the oracle's masks
+    allow (prefix-query pairs in step 0)."""
+    cu = _cu(N, texts)
+    fwd_pairs, bwd_pairs, fwd_items, bwd_items = cp_plan_pairs(cu, N, P)
+    counts, self_pairs = oracle.cp_pair_counts(cu, N, P)
+    want = counts.sum(axis=0)
+    want[0] += self_pairs
+    assert fwd_pairs == want.tolist()
+    assert bwd_pairs == want.tolist()
+
+
+@pytest.mark.parametrize("name", ["text_llm", "vlm_prefix", "packed_vlm", "long"])
+def test_work_lists_match_closed_form_on_workloads(cplib, name):
+    w = workloads.get(name)
+    cu = workloads.cu_seqlens(w)
+    fwd_pairs, bwd_pairs, _, _ = cp_plan_pairs(cu, w.prefix_len, w.P)
+    P, N = w.P, w.prefix_len
+    want = [0] * P
+    for L in workloads.text_lengths(w):
+        c = L // (2 * P)
+        want[0] += P * (c * c + c * (c + 1) + 2 * c * N) + N * (N + 1) // 2
+        for s in range(1, P):
+            want[s] += P * 2 * c * c
+    assert fwd_pairs == want and bwd_pairs == want
+    total = sum((N + L) * (N + L + 1) // 2 for L in workloads.text_lengths(w))
+    assert sum(want) == total
+
+
+def test_bad_arguments_return_status(cplib):
+    L = cplib
+    cu = B.cu_array([0, 10])
+    assert L.cp_zigzag_index(cu, 1, 0, 2, None, None, 0, None) == 2        # 10 % 4 != 0
+    assert L.cp_zigzag_index(None, 1, 0, 2, None, None, 0, None) == 1
+    assert L.cp_zigzag_index(cu, 1, 0, 0, None, None, 0, None) == 1       # P < 1
+    assert L.cp_zigzag_index(B.cu_array([0, 3]), 1, 4, 1, None, None, 0, None) == 2  # prefix > len
+    assert L.cp_attn_fwd_workspace_size(1, 10, 1, 64, cu, 1, 2, 0) == 0
+    assert L.cp_attn_fwd_workspace_size(1, 8, 1, 64, B.cu_array([0, 8]), 1, 2, 0) > 0
+    # d not in {64,128}, wrong dtype, null tensors, misaligned pointers
+    cu8 = B.cu_array([0, 8])
+    fake = ctypes.c_void_p(1 << 20)
+    st = L.cp_attn_fwd(fake, fake, fake, 1, 8, 1, 96, cu8, 1, 2, 0, 1.0, fake, fake, fake, 1 << 20,
+                       None)
+    assert st == 2
+    st = L.cp_attn_fwd(fake, fake, fake, 7, 8, 1, 64, cu8, 1, 2, 0, 1.0, fake, fake, fake, 1 << 20,
+                       None)
+    assert st == 3
+    st = L.cp_attn_fwd(None, fake, fake, 1, 8, 1, 64, cu8, 1, 2, 0, 1.0, fake, fake, fake, 1 << 20,
+                       None)
+    assert st == 1
+    odd = ctypes.c_void_p((1 << 20) + 4)
+    st = L.cp_attn_fwd(odd, fake, fake, 1, 8, 1, 64, cu8, 1, 2, 0, 1.0, fake, fake, fake, 1 << 20,
+                       None)
+    assert st == 4
+    st = L.cp_attn_fwd(fake, fake, fake, 1, 9, 1, 64, cu8, 1, 2, 0, 1.0, fake, fake, fake, 1 << 20,
+                       None)
+    assert st == 2                                                         # T != cu[-1]
+    L.cp_zigzag_index(cu, 1, 0, 2, None, None, 0, None)
+    assert b"not divisible" in L.cp_last_error()
+    assert L.cp_status_string(7) == b"CP_ERR_TIMEOUT"

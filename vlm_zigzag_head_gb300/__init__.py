@@ -1,0 +1,243 @@
+"""Zigzag context-parallel causal attention on GB300 (sm_103a).
+
+Thin Python layer over the C ABI of ``libcpattn.so`` (``include/cpattn.h``):
+it checks tensors, owns the workspace buffer and passes device pointers and
+the current CUDA stream down.  Every step of the computation runs in the
+library's CUDA kernels; there is no fallback.
+
+Functions keep the names of the C entry points:
+
+* :func:`cp_zigzag_index`, :func:`cp_zigzag_gather`, :func:`cp_zigzag_scatter`
+* :func:`cp_attn_fwd`, :func:`cp_lse_merge`, :func:`cp_attn_bwd`
+* :func:`cp_workspace_status`, :func:`cp_set_wait_limit`, :func:`cp_plan_pairs`
+* :func:`attention_host` -- end-to-end call on host (pinned) tensors.
+"""
+from __future__ import annotations
+
+import ctypes
+from typing import Optional, Sequence
+
+import torch
+
+from . import _binding as _b
+from ._binding import CP_BF16, CP_F32, CpError  # noqa: F401
+
+__all__ = ["cp_zigzag_index", "cp_zigzag_gather", "cp_zigzag_scatter", "cp_attn_fwd",
+           "cp_lse_merge", "cp_attn_bwd", "cp_workspace_status", "cp_set_wait_limit",
+           "cp_plan_pairs", "Workspace", "attention_host", "CpError"]
+
+
+def _dt(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return CP_BF16
+    if t.dtype == torch.float32:
+        return CP_F32
+    raise CpError(3, "dtype %s not supported (bf16 or fp32)" % t.dtype)
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(device) -> ctypes.c_void_p:
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _need_cuda(*ts):
+    for t in ts:
+        if t is None:
+            continue
+        if not t.is_cuda:
+            raise CpError(1, "tensors must live on a CUDA device")
+        if not t.is_contiguous():
+            raise CpError(1, "tensors must be contiguous")
+
+
+class Workspace:
+    """A growable device byte buffer (256-byte aligned) reused across calls on
+    one stream."""
+
+    def __init__(self, device=None):
+        self.device = torch.device(device) if device is not None else None
+        self.buf = None
+
+    def get(self, nbytes: int, device) -> torch.Tensor:
+        if self.buf is None or self.buf.numel() < nbytes or self.buf.device != device:
+            self.buf = torch.empty(max(nbytes, 256) + 256, dtype=torch.uint8, device=device)
+        return self.buf
+
+    def ptr(self):
+        p = self.buf.data_ptr()
+        return (p + 255) // 256 * 256
+
+    def nbytes(self):
+        return self.buf.numel() - (self.ptr() - self.buf.data_ptr())
+
+
+_default_ws = {}
+
+
+def _ws(ws: Optional[Workspace], device, nbytes: int, key: str) -> Workspace:
+    if ws is None:
+        ws = _default_ws.setdefault((key, str(device)), Workspace(device))
+    ws.get(nbytes, device)
+    return ws
+
+
+# ---------------------------------------------------------------------------
+def cp_zigzag_index(cu_seqlens: Sequence[int], prefix_len: int, P: int, device=None):
+    """Zigzag gather table ``fwd_idx`` and inverse ``inv_idx`` (int32).  On the
+    host when ``device`` is None, else copied to that device on its current
+    stream."""
+    cu = _b.cu_array(cu_seqlens)
+    n = len(cu_seqlens) - 1
+    text = sum(int(cu_seqlens[i + 1]) - int(cu_seqlens[i]) - prefix_len for i in range(n))
+    text = max(text, 0)
+    if device is None:
+        fwd = torch.empty(text, dtype=torch.int32)
+        inv = torch.empty(text, dtype=torch.int32)
+        _b.check(_b.lib().cp_zigzag_index(cu, n, prefix_len, P, _ptr(fwd), _ptr(inv), 0, None))
+    else:
+        fwd = torch.empty(text, dtype=torch.int32, device=device)
+        inv = torch.empty(text, dtype=torch.int32, device=device)
+        _b.check(_b.lib().cp_zigzag_index(cu, n, prefix_len, P, _ptr(fwd), _ptr(inv), 1,
+                                          _stream(fwd.device)))
+    return fwd, inv
+
+
+def cp_zigzag_gather(src: torch.Tensor, idx: torch.Tensor, out: Optional[torch.Tensor] = None):
+    """``out[k] = src[idx[k]]`` along dim 0 (rows of ``src[0].nbytes`` bytes)."""
+    _need_cuda(src, idx, out)
+    if out is None:
+        out = torch.empty((idx.numel(),) + tuple(src.shape[1:]), dtype=src.dtype,
+                          device=src.device)
+    row = src[0].numel() * src.element_size() if src.dim() > 1 else src.element_size()
+    _b.check(_b.lib().cp_zigzag_gather(_ptr(src), _ptr(out), row, _ptr(idx), idx.numel(),
+                                       _stream(src.device)))
+    return out
+
+
+def cp_zigzag_scatter(src: torch.Tensor, idx: torch.Tensor, out: torch.Tensor):
+    """``out[idx[k]] = src[k]`` along dim 0."""
+    _need_cuda(src, idx, out)
+    row = src[0].numel() * src.element_size() if src.dim() > 1 else src.element_size()
+    _b.check(_b.lib().cp_zigzag_scatter(_ptr(src), _ptr(out), row, _ptr(idx), idx.numel(),
+                                        _stream(src.device)))
+    return out
+
+
+def cp_attn_fwd(q, k, v, cu_seqlens, P: int, prefix_len: int, softmax_scale: float,
+                out=None, lse=None, workspace: Optional[Workspace] = None):
+    """Context-parallel causal attention forward; returns ``(out, lse)`` with
+    out ``[T,H,d]`` (q's dtype) and lse ``[H,T]`` fp32 (natural log)."""
+    _need_cuda(q, k, v, out, lse)
+    T, H, d = q.shape
+    dt = _dt(q)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((H, T), dtype=torch.float32, device=q.device)
+    cu = _b.cu_array(cu_seqlens)
+    n = len(cu_seqlens) - 1
+    L = _b.lib()
+    nbytes = L.cp_attn_fwd_workspace_size(dt, T, H, d, cu, n, P, prefix_len)
+    if nbytes == 0:  # invalid arguments: let the library name the problem
+        _b.check(L.cp_attn_fwd(_ptr(q), _ptr(k), _ptr(v), dt, T, H, d, cu, n, P, prefix_len,
+                               float(softmax_scale), _ptr(out), _ptr(lse), None, 0,
+                               _stream(q.device)))
+    ws = _ws(workspace, q.device, nbytes, "fwd")
+    _b.check(L.cp_attn_fwd(_ptr(q), _ptr(k), _ptr(v), dt, T, H, d, cu, n, P, prefix_len,
+                           float(softmax_scale), _ptr(out), _ptr(lse), ctypes.c_void_p(ws.ptr()),
+                           ws.nbytes(), _stream(q.device)))
+    return out, lse
+
+
+def cp_lse_merge(part_out: torch.Tensor, part_lse: torch.Tensor, out_dtype=torch.float32):
+    """Merge ``part_out [n,rows,H,d]`` / ``part_lse [n,H,rows]`` (fp32) into
+    ``(out [rows,H,d], lse [H,rows])`` by log-sum-exp."""
+    _need_cuda(part_out, part_lse)
+    n, rows, H, d = part_out.shape
+    out = torch.empty((rows, H, d), dtype=out_dtype, device=part_out.device)
+    lse = torch.empty((H, rows), dtype=torch.float32, device=part_out.device)
+    _b.check(_b.lib().cp_lse_merge(n, _ptr(part_out), _ptr(part_lse), rows, H, d, _ptr(out),
+                                   _dt(out), _ptr(lse), _stream(part_out.device)))
+    return out, lse
+
+
+def cp_attn_bwd(q, k, v, out, lse, dout, cu_seqlens, P: int, prefix_len: int,
+                softmax_scale: float, per_rank_prefix: bool = False,
+                workspace: Optional[Workspace] = None, grads=None):
+    """Backward; returns ``(dq, dk, dv)`` fp32 ``[T,H,d]`` and, with
+    ``per_rank_prefix``, the per-rank prefix gradients
+    ``[2, P+1, n*prefix_len, H, d]`` (slot P: prefix queries' own term)."""
+    _need_cuda(q, k, v, out, lse, dout)
+    T, H, d = q.shape
+    dt = _dt(q)
+    if grads is None:
+        grads = tuple(torch.empty((T, H, d), dtype=torch.float32, device=q.device)
+                      for _ in range(3))
+    dq, dk, dv = grads
+    n = len(cu_seqlens) - 1
+    pgrad = None
+    if per_rank_prefix:
+        pgrad = torch.empty((2, P + 1, n * prefix_len, H, d), dtype=torch.float32,
+                            device=q.device)
+    cu = _b.cu_array(cu_seqlens)
+    L = _b.lib()
+    nbytes = L.cp_attn_bwd_workspace_size(dt, T, H, d, cu, n, P, prefix_len)
+    if nbytes == 0:  # invalid arguments: let the library name the problem
+        _b.check(L.cp_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout), dt,
+                               T, H, d, cu, n, P, prefix_len, float(softmax_scale), _ptr(dq),
+                               _ptr(dk), _ptr(dv), _ptr(pgrad), None, 0, _stream(q.device)))
+    ws = _ws(workspace, q.device, nbytes, "bwd")
+    _b.check(L.cp_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout), dt, T, H,
+                           d, cu, n, P, prefix_len, float(softmax_scale), _ptr(dq), _ptr(dk),
+                           _ptr(dv), _ptr(pgrad), ctypes.c_void_p(ws.ptr()), ws.nbytes(),
+                           _stream(q.device)))
+    if per_rank_prefix:
+        return dq, dk, dv, pgrad
+    return dq, dk, dv
+
+
+def cp_workspace_status(workspace: Workspace) -> int:
+    """Synchronise the current stream; 0 or the CP_ERR_TIMEOUT status."""
+    st = _b.lib().cp_workspace_status(ctypes.c_void_p(workspace.ptr()),
+                                      _stream(workspace.buf.device))
+    return st
+
+
+def default_workspace(kind: str, device) -> Workspace:
+    return _default_ws[(kind, str(torch.device(device)))]
+
+
+def cp_set_wait_limit(rounds: int):
+    _b.lib().cp_set_wait_limit(int(rounds))
+
+
+def cp_plan_pairs(cu_seqlens, prefix_len: int, P: int):
+    """Host-only: visible pairs and items per ring step of both work lists."""
+    arrs = [(ctypes.c_int64 * P)() for _ in range(4)]
+    cu = _b.cu_array(cu_seqlens)
+    _b.check(_b.lib().cp_plan_pairs(cu, len(cu_seqlens) - 1, prefix_len, P, *arrs))
+    return tuple([int(x) for x in a] for a in arrs)
+
+
+def attention_host(q, k, v, dout, cu_seqlens, P: int, prefix_len: int, softmax_scale: float,
+                   device="cuda", host_out=None):
+    """End-to-end call on host tensors (pinned for asynchronous copies): copy the
+    inputs to ``device``, run forward (and backward when ``dout`` is given),
+    copy results back.  Returns host tensors ``(out, lse[, dq, dk, dv])``."""
+    dev = torch.device(device)
+    qd, kd, vd = (x.to(dev, non_blocking=True) for x in (q, k, v))
+    out, lse = cp_attn_fwd(qd, kd, vd, cu_seqlens, P, prefix_len, softmax_scale)
+    res = [out, lse]
+    if dout is not None:
+        dod = dout.to(dev, non_blocking=True)
+        res += list(cp_attn_bwd(qd, kd, vd, out, lse, dod, cu_seqlens, P, prefix_len,
+                                softmax_scale))
+    if host_out is None:
+        host_out = [torch.empty(r.shape, dtype=r.dtype, pin_memory=True) for r in res]
+    for h, r in zip(host_out, res):
+        h.copy_(r, non_blocking=True)
+    torch.cuda.current_stream(dev).synchronize()
+    return tuple(host_out)

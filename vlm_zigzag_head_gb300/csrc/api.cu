@@ -1,0 +1,577 @@
+// C ABI of libcpattn: argument checks, work-list planning and upload,
+// workspace layout, and the launch sequence of every entry point.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <memory>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "../../include/cpattn.h"
+#include "kernels.h"
+#include "plan.h"
+#include "tc.h"
+
+using namespace cpattn;
+
+namespace {
+
+thread_local std::string g_err;
+std::atomic<long long> g_wait_limit{0};
+
+cp_status_t fail(cp_status_t s, const std::string& msg) {
+  g_err = msg;
+  return s;
+}
+
+cp_status_t cuda_fail(cudaError_t e, const char* what) {
+  return fail(CP_ERR_CUDA, std::string(what) + ": " + cudaGetErrorString(e));
+}
+
+#define CP_CUDA(call, what)                        \
+  do {                                             \
+    cudaError_t e_ = (call);                       \
+    if (e_ != cudaSuccess) return cuda_fail(e_, what); \
+  } while (0)
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// ---------------------------------------------------------------------------
+// page-locked staging ring: work lists are copied host -> device without the
+// implicit stream synchronisation of pageable copies.  A slot is reused only
+// after the event recorded behind its last copy has completed.
+// ---------------------------------------------------------------------------
+class Stager {
+ public:
+  cudaError_t upload(void* dst, const void* src, size_t bytes, cudaStream_t st) {
+    if (bytes == 0) return cudaSuccess;
+    std::lock_guard<std::mutex> lk(mu_);
+    Slot& s = slots_[next_];
+    next_ = (next_ + 1) % kSlots;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (s.ev && s.used) {
+      e = cudaEventSynchronize(s.ev);
+      if (e != cudaSuccess) return e;
+    }
+    if (s.ev && s.dev != dev) {
+      cudaEventDestroy(s.ev);
+      s.ev = nullptr;
+    }
+    if (!s.ev) {
+      e = cudaEventCreateWithFlags(&s.ev, cudaEventDisableTiming);
+      if (e != cudaSuccess) return e;
+      s.dev = dev;
+    }
+    if (s.cap < bytes) {
+      if (s.host) cudaFreeHost(s.host);
+      s.host = nullptr;
+      s.cap = 0;
+      size_t cap = align_up(bytes * 2, 1 << 16);
+      e = cudaHostAlloc(&s.host, cap, cudaHostAllocDefault);
+      if (e != cudaSuccess) return e;
+      s.cap = cap;
+    }
+    memcpy(s.host, src, bytes);
+    e = cudaMemcpyAsync(dst, s.host, bytes, cudaMemcpyHostToDevice, st);
+    if (e != cudaSuccess) return e;
+    e = cudaEventRecord(s.ev, st);
+    s.used = (e == cudaSuccess);
+    return e;
+  }
+
+ private:
+  static constexpr int kSlots = 16;
+  struct Slot {
+    void* host = nullptr;
+    size_t cap = 0;
+    cudaEvent_t ev = nullptr;
+    int dev = -1;
+    bool used = false;
+  };
+  std::mutex mu_;
+  Slot slots_[kSlots];
+  int next_ = 0;
+};
+
+Stager& stager() {
+  static Stager* s = new Stager();  // intentionally leaked: outlives static destructors
+  return *s;
+}
+
+// ---------------------------------------------------------------------------
+// plan cache (plans depend only on cu_seqlens, prefix_len and P)
+// ---------------------------------------------------------------------------
+struct PlanSet {
+  Problem pb;
+  FwdPlan fwd;       // text rows in rank-local order
+  FwdPlan fwd_nat;   // text rows in natural order (fp32 dQ pass)
+  BwdPlan bwd;
+  std::vector<int32_t> samples;  // [n][4]: t0, c, off, ord0 (index kernel)
+};
+
+struct PlanCache {
+  std::mutex mu;
+  std::vector<std::shared_ptr<PlanSet>> lru;
+};
+
+PlanCache& plan_cache() {
+  static PlanCache* c = new PlanCache();
+  return *c;
+}
+
+cp_status_t get_plans(const int32_t* cu, int n_seqs, int N, int P, int T, int H, int d,
+                      std::shared_ptr<PlanSet>* out) {
+  Problem pb;
+  std::string err = make_problem(cu, n_seqs, N, P, T, H, d, &pb);
+  if (!err.empty()) return fail(CP_ERR_SHAPE, err);
+  PlanCache& pc = plan_cache();
+  {
+    std::lock_guard<std::mutex> lk(pc.mu);
+    for (auto& p : pc.lru) {
+      if (p->pb.P == P && p->pb.N == N && p->pb.cu == pb.cu) {
+        *out = p;
+        return CP_OK;
+      }
+    }
+  }
+  auto ps = std::make_shared<PlanSet>();
+  ps->pb = pb;
+  plan_forward(pb, true, &ps->fwd);
+  plan_forward(pb, false, &ps->fwd_nat);
+  plan_backward(pb, &ps->bwd);
+  int64_t ord = 0;
+  for (int i = 0; i < n_seqs; ++i) {
+    ps->samples.push_back(pb.cu[i] + N);
+    ps->samples.push_back(pb.c[i]);
+    ps->samples.push_back(pb.off[i]);
+    ps->samples.push_back((int32_t)ord);
+    ord += 2LL * P * pb.c[i];
+  }
+  std::lock_guard<std::mutex> lk(pc.mu);
+  pc.lru.insert(pc.lru.begin(), ps);
+  if (pc.lru.size() > 8) pc.lru.pop_back();
+  *out = ps;
+  return CP_OK;
+}
+
+// ---------------------------------------------------------------------------
+// workspace layouts
+// ---------------------------------------------------------------------------
+struct FwdWs {
+  size_t status = 0, items = 0, samples = 0, idx = 0, qkv[3] = {0, 0, 0}, o_run = 0, lse_run = 0,
+         total = 0;
+};
+
+FwdWs fwd_layout(const PlanSet& ps, int H, int d, size_t elem) {
+  FwdWs w;
+  size_t o = 0;
+  w.status = o; o += kStatusBytes;
+  w.items = o; o = align_up(o + ps.fwd.items.size() * sizeof(FwdItem), 256);
+  w.samples = o; o = align_up(o + ps.samples.size() * sizeof(int32_t), 256);
+  w.idx = o; o = align_up(o + (size_t)ps.pb.text_rows * sizeof(int32_t), 256);
+  const size_t tb = (size_t)ps.pb.text_rows * H * d * elem;
+  for (int i = 0; i < 3; ++i) { w.qkv[i] = o; o = align_up(o + tb, 256); }
+  w.o_run = o; o = align_up(o + (size_t)ps.pb.text_rows * H * d * sizeof(float), 256);
+  w.lse_run = o; o = align_up(o + (size_t)ps.pb.text_rows * H * sizeof(float), 256);
+  w.total = o;
+  return w;
+}
+
+struct BwdWs {
+  size_t status = 0, items = 0, qitems = 0, cu = 0, D = 0, lse2 = 0, slots = 0, total = 0;
+};
+
+BwdWs bwd_layout(const PlanSet& ps, int H, int d, bool simt, bool own_slots) {
+  BwdWs w;
+  const Problem& pb = ps.pb;
+  size_t o = 0;
+  w.status = o; o += kStatusBytes;
+  w.items = o; o = align_up(o + ps.bwd.items.size() * sizeof(BwdItem), 256);
+  w.qitems = o;
+  if (simt) o = align_up(o + ps.fwd_nat.items.size() * sizeof(FwdItem), 256);
+  w.cu = o; o = align_up(o + pb.cu.size() * sizeof(int32_t), 256);
+  w.D = o; o = align_up(o + (size_t)pb.T * H * sizeof(float), 256);
+  w.lse2 = o; o = align_up(o + (size_t)pb.T * H * sizeof(float), 256);
+  w.slots = o;
+  if (own_slots)
+    o = align_up(o + 2ull * (pb.P + 1) * pb.n_seqs * pb.N * H * d * sizeof(float), 256);
+  w.total = o;
+  return w;
+}
+
+cp_status_t check_common(const void* const* ptrs, int n_ptrs, cp_dtype_t dt, int T, int H,
+                         int d, const int32_t* cu, int n_seqs, int P, int N, float scale) {
+  if (dt != CP_F32 && dt != CP_BF16) return fail(CP_ERR_DTYPE, "dtype must be CP_F32 or CP_BF16");
+  if (T < 0 || H < 1 || n_seqs < 1 || P < 1 || N < 0)
+    return fail(CP_ERR_INVALID_ARG, "T >= 0, H >= 1, n_seqs >= 1, P >= 1, prefix_len >= 0");
+  if (!cu) return fail(CP_ERR_INVALID_ARG, "cu_seqlens is NULL");
+  if (d != 64 && d != 128) return fail(CP_ERR_SHAPE, "head_dim must be 64 or 128");
+  if (!std::isfinite(scale)) return fail(CP_ERR_INVALID_ARG, "softmax_scale must be finite");
+  for (int i = 0; i < n_ptrs && T > 0; ++i) {
+    if (!ptrs[i]) return fail(CP_ERR_INVALID_ARG, "a tensor pointer is NULL");
+    if (!aligned16(ptrs[i])) return fail(CP_ERR_ALIGNMENT, "tensor pointers must be 16-byte aligned");
+  }
+  return CP_OK;
+}
+
+cp_status_t check_device_for_bf16() {
+  int dev = 0, major = 0, minor = 0;
+  CP_CUDA(cudaGetDevice(&dev), "cudaGetDevice");
+  CP_CUDA(cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev), "cc major");
+  CP_CUDA(cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev), "cc minor");
+  if (major != 10 || minor != 3)
+    return fail(CP_ERR_UNSUPPORTED, "the bf16 path is built for sm_103a (compute capability 10.3)");
+  return CP_OK;
+}
+
+bool use_tc_path() {
+  static int v = [] {
+    const char* e = getenv("CPATTN_BF16_SIMT");
+    return (e && e[0] == '1') ? 0 : 1;
+  }();
+  return v != 0;
+}
+
+long long wait_limit() {
+  long long w = g_wait_limit.load();
+  return w > 0 ? w : (1LL << 22);
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* cp_last_error(void) { return g_err.c_str(); }
+
+const char* cp_status_string(cp_status_t s) {
+  switch (s) {
+    case CP_OK: return "CP_OK";
+    case CP_ERR_INVALID_ARG: return "CP_ERR_INVALID_ARG";
+    case CP_ERR_SHAPE: return "CP_ERR_SHAPE";
+    case CP_ERR_DTYPE: return "CP_ERR_DTYPE";
+    case CP_ERR_ALIGNMENT: return "CP_ERR_ALIGNMENT";
+    case CP_ERR_WORKSPACE: return "CP_ERR_WORKSPACE";
+    case CP_ERR_CUDA: return "CP_ERR_CUDA";
+    case CP_ERR_TIMEOUT: return "CP_ERR_TIMEOUT";
+    case CP_ERR_UNSUPPORTED: return "CP_ERR_UNSUPPORTED";
+  }
+  return "CP_ERR_UNKNOWN";
+}
+
+int cp_version(void) { return CPATTN_VERSION; }
+
+void cp_set_wait_limit(long long rounds) { g_wait_limit.store(rounds > 0 ? rounds : 0); }
+
+cp_status_t cp_zigzag_index(const int32_t* cu, int n_seqs, int N, int P, int32_t* fwd_idx,
+                            int32_t* inv_idx, int on_device, void* stream) {
+  if (!cu || n_seqs < 1 || P < 1 || N < 0)
+    return fail(CP_ERR_INVALID_ARG, "cu_seqlens non-NULL, n_seqs >= 1, P >= 1, prefix_len >= 0");
+  if (on_device) {
+    std::shared_ptr<PlanSet> ps;
+    cp_status_t s = get_plans(cu, n_seqs, N, P, -1, 1, 64, &ps);
+    if (s != CP_OK) return s;
+    if ((fwd_idx && !aligned16(fwd_idx)) || (inv_idx && !aligned16(inv_idx)))
+      return fail(CP_ERR_ALIGNMENT, "index tables must be 16-byte aligned");
+    if (ps->pb.text_rows == 0) return CP_OK;
+    std::vector<int32_t> f(ps->pb.text_rows), v(ps->pb.text_rows);
+    zigzag_tables(ps->pb, f.data(), v.data());
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (fwd_idx) CP_CUDA(stager().upload(fwd_idx, f.data(), f.size() * 4, st), "upload fwd_idx");
+    if (inv_idx) CP_CUDA(stager().upload(inv_idx, v.data(), v.size() * 4, st), "upload inv_idx");
+    return CP_OK;
+  }
+  Problem pb;
+  std::string err = make_problem(cu, n_seqs, N, P, -1, 1, 64, &pb);
+  if (!err.empty()) return fail(CP_ERR_SHAPE, err);
+  zigzag_tables(pb, fwd_idx, inv_idx);
+  return CP_OK;
+}
+
+cp_status_t cp_zigzag_gather(const void* src, void* dst, size_t row_bytes, const int32_t* idx,
+                             int n_rows, void* stream) {
+  if (n_rows < 0) return fail(CP_ERR_INVALID_ARG, "n_rows < 0");
+  if (n_rows == 0) return CP_OK;
+  if (!src || !dst || !idx) return fail(CP_ERR_INVALID_ARG, "NULL pointer");
+  if (!aligned16(src) || !aligned16(dst) || (row_bytes % 16) != 0 || row_bytes == 0)
+    return fail(CP_ERR_ALIGNMENT, "pointers and row_bytes must be multiples of 16");
+  const void* s[1] = {src};
+  void* d[1] = {dst};
+  CP_CUDA(launch_gather_rows(s, d, 1, row_bytes, idx, n_rows, false,
+                             static_cast<cudaStream_t>(stream)),
+          "zigzag gather");
+  return CP_OK;
+}
+
+cp_status_t cp_zigzag_scatter(const void* src, void* dst, size_t row_bytes, const int32_t* idx,
+                              int n_rows, void* stream) {
+  if (n_rows < 0) return fail(CP_ERR_INVALID_ARG, "n_rows < 0");
+  if (n_rows == 0) return CP_OK;
+  if (!src || !dst || !idx) return fail(CP_ERR_INVALID_ARG, "NULL pointer");
+  if (!aligned16(src) || !aligned16(dst) || (row_bytes % 16) != 0 || row_bytes == 0)
+    return fail(CP_ERR_ALIGNMENT, "pointers and row_bytes must be multiples of 16");
+  const void* s[1] = {src};
+  void* d[1] = {dst};
+  CP_CUDA(launch_gather_rows(s, d, 1, row_bytes, idx, n_rows, true,
+                             static_cast<cudaStream_t>(stream)),
+          "zigzag scatter");
+  return CP_OK;
+}
+
+size_t cp_attn_fwd_workspace_size(cp_dtype_t dt, int T, int H, int d, const int32_t* cu,
+                                  int n_seqs, int P, int N) {
+  std::shared_ptr<PlanSet> ps;
+  if (!cu || H < 1 || (dt != CP_F32 && dt != CP_BF16)) return 0;
+  if (get_plans(cu, n_seqs, N, P, T, H, d, &ps) != CP_OK) return 0;
+  return fwd_layout(*ps, H, d, dt == CP_BF16 ? 2 : 4).total;
+}
+
+cp_status_t cp_attn_fwd(const void* q, const void* k, const void* v, cp_dtype_t dt, int T, int H,
+                        int d, const int32_t* cu, int n_seqs, int P, int N, float scale,
+                        void* out, float* lse, void* ws, size_t ws_bytes, void* stream) {
+  const void* ptrs[5] = {q, k, v, out, lse};
+  cp_status_t s = check_common(ptrs, 5, dt, T, H, d, cu, n_seqs, P, N, scale);
+  if (s != CP_OK) return s;
+  std::shared_ptr<PlanSet> ps;
+  s = get_plans(cu, n_seqs, N, P, T, H, d, &ps);
+  if (s != CP_OK) return s;
+  if (T == 0) return CP_OK;
+  const bool bf16 = dt == CP_BF16;
+  const bool tc = bf16 && use_tc_path();
+  if (tc && (s = check_device_for_bf16()) != CP_OK) return s;
+  const size_t elem = bf16 ? 2 : 4;
+  const FwdWs L = fwd_layout(*ps, H, d, elem);
+  if (!ws || ws_bytes < L.total)
+    return fail(CP_ERR_WORKSPACE, "workspace smaller than cp_attn_fwd_workspace_size()");
+  if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0)
+    return fail(CP_ERR_ALIGNMENT, "workspace must be 256-byte aligned");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  char* w = static_cast<char*>(ws);
+  const Problem& pb = ps->pb;
+  CP_CUDA(cudaMemsetAsync(w + L.status, 0, kStatusBytes, st), "clear status");
+  CP_CUDA(stager().upload(w + L.items, ps->fwd.items.data(),
+                          ps->fwd.items.size() * sizeof(FwdItem), st),
+          "upload work list");
+  CP_CUDA(stager().upload(w + L.samples, ps->samples.data(), ps->samples.size() * 4, st),
+          "upload sample table");
+  int32_t* idx = reinterpret_cast<int32_t*>(w + L.idx);
+  // get_batch_on_this_cp_rank: zigzag table, then index_select of q, k, v text rows
+  CP_CUDA(launch_zigzag_index(reinterpret_cast<const int32_t*>(w + L.samples), n_seqs, P, pb.R,
+                              idx, nullptr, st),
+          "zigzag index kernel");
+  const void* src[3] = {q, k, v};
+  void* dst[3] = {w + L.qkv[0], w + L.qkv[1], w + L.qkv[2]};
+  CP_CUDA(launch_gather_rows(src, dst, 3, (size_t)H * d * elem, idx, (int)pb.text_rows, false, st),
+          "zigzag gather");
+  const FwdItem* items = reinterpret_cast<const FwdItem*>(w + L.items);
+  float* o_run = reinterpret_cast<float*>(w + L.o_run);
+  float* lse_run = reinterpret_cast<float*>(w + L.lse_run);
+  if (tc) {
+    TcFwdArgs a;
+    const char* terr = nullptr;
+    const int64_t PR = pb.text_rows;
+    bool ok = make_tmap_thd(&a.tm_q_text, dst[0], PR, H, d, 128, &terr) &&
+              make_tmap_thd(&a.tm_k_text, dst[1], PR, H, d, 128, &terr) &&
+              make_tmap_thd(&a.tm_v_text, dst[2], PR, H, d, 128, &terr) &&
+              make_tmap_thd(&a.tm_q_nat, q, T, H, d, 128, &terr) &&
+              make_tmap_thd(&a.tm_k_nat, k, T, H, d, 128, &terr) &&
+              make_tmap_thd(&a.tm_v_nat, v, T, H, d, 128, &terr);
+    if (!ok) return fail(CP_ERR_CUDA, std::string("tensor map: ") + (terr ? terr : "?"));
+    a.H = H; a.d = d;
+    a.scale_log2 = scale * 1.4426950408889634f;
+    a.o_run = o_run; a.lse_run = lse_run; a.run_rows = PR;
+    a.out = out; a.lse = lse; a.T = T;
+    a.status = reinterpret_cast<int32_t*>(w + L.status);
+    a.wait_limit = wait_limit();
+    for (int step = 0; step < P; ++step) {
+      a.items = items + ps->fwd.step_begin[step];
+      a.n_items = ps->fwd.step_begin[step + 1] - ps->fwd.step_begin[step];
+      CP_CUDA(launch_tc_fwd(a, st), "tensor-core ring step");
+    }
+    return CP_OK;
+  }
+  SimtFwdArgs a;
+  a.q_text = dst[0]; a.k_text = dst[1]; a.v_text = dst[2];
+  a.q_nat = q; a.k_nat = k; a.v_nat = v;
+  a.H = H; a.d = d; a.scale = scale;
+  a.o_run = o_run; a.lse_run = lse_run; a.run_rows = pb.text_rows;
+  a.out = out; a.lse = lse; a.T = T;
+  for (int step = 0; step < P; ++step) {
+    a.items = items + ps->fwd.step_begin[step];
+    a.n_items = ps->fwd.step_begin[step + 1] - ps->fwd.step_begin[step];
+    CP_CUDA(launch_simt_fwd(a, bf16, st), "ring step");
+  }
+  return CP_OK;
+}
+
+cp_status_t cp_lse_merge(int n_parts, const float* part_out, const float* part_lse, int rows,
+                         int H, int d, void* out, cp_dtype_t out_dt, float* lse, void* stream) {
+  if (n_parts < 1 || rows < 0 || H < 1 || d < 1 || d > 128)
+    return fail(CP_ERR_INVALID_ARG, "n_parts >= 1, rows >= 0, H >= 1, 1 <= d <= 128");
+  if (out_dt != CP_F32 && out_dt != CP_BF16) return fail(CP_ERR_DTYPE, "out dtype");
+  if (rows == 0) return CP_OK;
+  const void* ptrs[4] = {part_out, part_lse, out, lse};
+  for (const void* p : ptrs) {
+    if (!p) return fail(CP_ERR_INVALID_ARG, "NULL pointer");
+    if (!aligned16(p)) return fail(CP_ERR_ALIGNMENT, "pointers must be 16-byte aligned");
+  }
+  CP_CUDA(launch_lse_merge(n_parts, part_out, part_lse, rows, H, d, out, out_dt == CP_BF16, lse,
+                           static_cast<cudaStream_t>(stream)),
+          "lse merge");
+  return CP_OK;
+}
+
+size_t cp_attn_bwd_workspace_size(cp_dtype_t dt, int T, int H, int d, const int32_t* cu,
+                                  int n_seqs, int P, int N) {
+  std::shared_ptr<PlanSet> ps;
+  if (!cu || H < 1 || (dt != CP_F32 && dt != CP_BF16)) return 0;
+  if (get_plans(cu, n_seqs, N, P, T, H, d, &ps) != CP_OK) return 0;
+  const bool simt = !(dt == CP_BF16 && use_tc_path());
+  return bwd_layout(*ps, H, d, simt, true).total;
+}
+
+cp_status_t cp_attn_bwd(const void* q, const void* k, const void* v, const void* out,
+                        const float* lse, const void* dout, cp_dtype_t dt, int T, int H, int d,
+                        const int32_t* cu, int n_seqs, int P, int N, float scale, float* dq,
+                        float* dk, float* dv, float* pgrad, void* ws, size_t ws_bytes,
+                        void* stream) {
+  const void* ptrs[9] = {q, k, v, out, lse, dout, dq, dk, dv};
+  cp_status_t s = check_common(ptrs, 9, dt, T, H, d, cu, n_seqs, P, N, scale);
+  if (s != CP_OK) return s;
+  if (pgrad && !aligned16(pgrad)) return fail(CP_ERR_ALIGNMENT, "prefix_grad_per_rank alignment");
+  std::shared_ptr<PlanSet> ps;
+  s = get_plans(cu, n_seqs, N, P, T, H, d, &ps);
+  if (s != CP_OK) return s;
+  if (T == 0) return CP_OK;
+  const bool bf16 = dt == CP_BF16;
+  const bool tc = bf16 && use_tc_path();
+  if (tc && (s = check_device_for_bf16()) != CP_OK) return s;
+  const BwdWs L = bwd_layout(*ps, H, d, !tc, pgrad == nullptr);
+  if (!ws || ws_bytes < L.total)
+    return fail(CP_ERR_WORKSPACE, "workspace smaller than cp_attn_bwd_workspace_size()");
+  if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0)
+    return fail(CP_ERR_ALIGNMENT, "workspace must be 256-byte aligned");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  char* w = static_cast<char*>(ws);
+  const Problem& pb = ps->pb;
+  const int64_t pre_rows = (int64_t)n_seqs * N;
+  float* slots = pgrad ? pgrad : reinterpret_cast<float*>(w + L.slots);
+  float* pre_k = slots;
+  float* pre_v = slots + (size_t)(P + 1) * pre_rows * H * d;
+  float* Dd = reinterpret_cast<float*>(w + L.D);
+  float* lse2 = reinterpret_cast<float*>(w + L.lse2);
+  CP_CUDA(cudaMemsetAsync(w + L.status, 0, kStatusBytes, st), "clear status");
+  CP_CUDA(stager().upload(w + L.items, ps->bwd.items.data(),
+                          ps->bwd.items.size() * sizeof(BwdItem), st),
+          "upload work list");
+  CP_CUDA(stager().upload(w + L.cu, pb.cu.data(), pb.cu.size() * 4, st), "upload cu_seqlens");
+  CP_CUDA(launch_bwd_preprocess(out, dout, bf16, lse, T, H, d, Dd, lse2, st), "bwd preprocess");
+  const BwdItem* items = reinterpret_cast<const BwdItem*>(w + L.items);
+  if (tc) {
+    CP_CUDA(cudaMemsetAsync(dq, 0, (size_t)T * H * d * sizeof(float), st), "clear dq");
+    TcBwdArgs a;
+    const char* terr = nullptr;
+    bool ok = make_tmap_thd(&a.tm_q, q, T, H, d, kBwdTileQ, &terr) &&
+              make_tmap_thd(&a.tm_k, k, T, H, d, kBwdTileK, &terr) &&
+              make_tmap_thd(&a.tm_v, v, T, H, d, kBwdTileK, &terr) &&
+              make_tmap_thd(&a.tm_do, dout, T, H, d, kBwdTileQ, &terr);
+    if (!ok) return fail(CP_ERR_CUDA, std::string("tensor map: ") + (terr ? terr : "?"));
+    a.H = H; a.d = d; a.scale = scale; a.scale_log2 = scale * 1.4426950408889634f;
+    a.D = Dd; a.lse2 = lse2; a.T = T;
+    a.dq = dq; a.dk = dk; a.dv = dv;
+    a.pre_k = pre_k; a.pre_v = pre_v; a.pre_rows = pre_rows;
+    a.status = reinterpret_cast<int32_t*>(w + L.status);
+    a.wait_limit = wait_limit();
+    for (int step = 0; step < P; ++step) {
+      a.items = items + ps->bwd.step_begin[step];
+      a.n_items = ps->bwd.step_begin[step + 1] - ps->bwd.step_begin[step];
+      CP_CUDA(launch_tc_bwd(a, st), "tensor-core backward ring step");
+    }
+  } else {
+    CP_CUDA(stager().upload(w + L.qitems, ps->fwd_nat.items.data(),
+                            ps->fwd_nat.items.size() * sizeof(FwdItem), st),
+            "upload dq work list");
+    const FwdItem* qitems = reinterpret_cast<const FwdItem*>(w + L.qitems);
+    SimtBwdArgs a;
+    a.q = q; a.k = k; a.v = v; a.dout = dout; a.D = Dd; a.lse2 = lse2;
+    a.H = H; a.d = d; a.scale = scale; a.T = T;
+    a.dq = dq; a.dk = dk; a.dv = dv; a.pre_k = pre_k; a.pre_v = pre_v; a.pre_rows = pre_rows;
+    for (int step = 0; step < P; ++step) {
+      a.q_items = qitems + ps->fwd_nat.step_begin[step];
+      a.n_q_items = ps->fwd_nat.step_begin[step + 1] - ps->fwd_nat.step_begin[step];
+      a.k_items = items + ps->bwd.step_begin[step];
+      a.n_k_items = ps->bwd.step_begin[step + 1] - ps->bwd.step_begin[step];
+      CP_CUDA(launch_simt_bwd_dq(a, bf16, st), "backward dq step");
+      CP_CUDA(launch_simt_bwd_dkdv(a, bf16, st), "backward dk/dv step");
+    }
+  }
+  if (N > 0) {
+    // the AllReduce of the replicated prefix gradient: fixed-order sum of slots
+    CP_CUDA(launch_prefix_reduce(pre_k, pre_v, P + 1, reinterpret_cast<const int32_t*>(w + L.cu),
+                                 n_seqs, N, H, d, dk, dv, st),
+            "prefix gradient sum");
+  }
+  return CP_OK;
+}
+
+cp_status_t cp_workspace_status(const void* ws, void* stream) {
+  if (!ws) return fail(CP_ERR_INVALID_ARG, "workspace is NULL");
+  CP_CUDA(cudaStreamSynchronize(static_cast<cudaStream_t>(stream)), "stream sync");
+  DevStatus h{};
+  CP_CUDA(cudaMemcpy(&h, ws, sizeof(int32_t) * 2, cudaMemcpyDeviceToHost), "read status");
+  if (h.timeout) {
+    char buf[96];
+    snprintf(buf, sizeof buf, "a device wait gave up (site %d)", h.where);
+    return fail(CP_ERR_TIMEOUT, buf);
+  }
+  return CP_OK;
+}
+
+cp_status_t cp_plan_pairs(const int32_t* cu, int n_seqs, int N, int P, int64_t* fwd_pairs,
+                          int64_t* bwd_pairs, int64_t* fwd_items, int64_t* bwd_items) {
+  if (!cu || n_seqs < 1 || P < 1 || N < 0) return fail(CP_ERR_INVALID_ARG, "bad arguments");
+  Problem pb;
+  std::string err = make_problem(cu, n_seqs, N, P, -1, 1, 64, &pb);
+  if (!err.empty()) return fail(CP_ERR_SHAPE, err);
+  FwdPlan f;
+  BwdPlan b;
+  plan_forward(pb, true, &f);
+  plan_backward(pb, &b);
+  for (int s = 0; s < P; ++s) {
+    int64_t fp = 0, bp = 0;
+    for (int x = f.step_begin[s]; x < f.step_begin[s + 1]; ++x) {
+      const FwdItem& it = f.items[x];
+      for (int t = 0; t < it.q_len; ++t)
+        for (int g = 0; g < it.nseg; ++g) {
+          const Seg& sg = it.seg[g];
+          int64_t vis = sg.causal ? std::min<int64_t>(sg.len, std::max<int64_t>(0, t + sg.delta + 1))
+                                  : sg.len;
+          fp += vis;
+        }
+    }
+    for (int x = b.step_begin[s]; x < b.step_begin[s + 1]; ++x) {
+      const BwdItem& it = b.items[x];
+      for (int u = 0; u < it.k_len; ++u)
+        for (int g = 0; g < it.nseg; ++g) {
+          const Seg& sg = it.seg[g];
+          int64_t vis = sg.causal ? std::max<int64_t>(0, sg.len - std::max<int64_t>(0, u - sg.delta))
+                                  : sg.len;
+          bp += vis;
+        }
+    }
+    if (fwd_pairs) fwd_pairs[s] = fp;
+    if (bwd_pairs) bwd_pairs[s] = bp;
+    if (fwd_items) fwd_items[s] = f.step_begin[s + 1] - f.step_begin[s];
+    if (bwd_items) bwd_items[s] = b.step_begin[s + 1] - b.step_begin[s];
+  }
+  return CP_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,262 @@
+// HBM-bound kernels of the path: zigzag gather/scatter and index tables,
+// standalone log-sum-exp merge, backward preprocess, prefix-gradient sum.
+#include <cuda_bf16.h>
+
+#include "kernels.h"
+
+namespace cpattn {
+
+namespace {
+
+constexpr int kThreads = 256;
+
+__device__ __forceinline__ uint4 ld_stream(const uint4* p) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+  return r;
+}
+
+struct RowPtrs {
+  const uint4* s0; const uint4* s1; const uint4* s2; const uint4* s3;
+  uint4* d0; uint4* d1; uint4* d2; uint4* d3;
+};
+
+// One warp moves one row of one tensor; 16-byte vectors, coalesced per row.
+// gather: dst[k] = src[idx[k]];  scatter: dst[idx[k]] = src[k].
+__global__ void __launch_bounds__(kThreads) gather_rows_kernel(RowPtrs p, int n_tensors,
+                                                               int vec_per_row,
+                                                               const int32_t* __restrict__ idx,
+                                                               int n_rows, int scatter) {
+  const int lane = threadIdx.x & 31;
+  const long long warps = (long long)gridDim.x * (kThreads / 32);
+  const long long total = (long long)n_rows * n_tensors;
+  for (long long w = (long long)blockIdx.x * (kThreads / 32) + threadIdx.x / 32; w < total;
+       w += warps) {
+    const int tsel = (int)(w % n_tensors);
+    const long long k = w / n_tensors;
+    const long long ik = idx[k];
+    const long long srow = scatter ? k : ik;
+    const long long drow = scatter ? ik : k;
+    const uint4* s = tsel == 0 ? p.s0 : tsel == 1 ? p.s1 : tsel == 2 ? p.s2 : p.s3;
+    uint4* d = tsel == 0 ? p.d0 : tsel == 1 ? p.d1 : tsel == 2 ? p.d2 : p.d3;
+    s += srow * vec_per_row;
+    d += drow * vec_per_row;
+    int e = lane;
+    for (; e + 96 < vec_per_row; e += 128) {
+      uint4 a = ld_stream(s + e), b = ld_stream(s + e + 32), c = ld_stream(s + e + 64),
+            f = ld_stream(s + e + 96);
+      d[e] = a;
+      d[e + 32] = b;
+      d[e + 64] = c;
+      d[e + 96] = f;
+    }
+    for (; e < vec_per_row; e += 32) d[e] = ld_stream(s + e);
+  }
+}
+
+// Thread per permuted text row k: rank r = k / R; its sample by binary search
+// over the rank-local offsets; then chunk r or 2P-1-r (page §1.1 pairing).
+__global__ void zigzag_index_kernel(const int32_t* __restrict__ smp, int n_seqs, int P,
+                                    long long R, int32_t* fwd_idx, int32_t* inv_idx) {
+  const long long n = R * P;
+  for (long long k = (long long)blockIdx.x * blockDim.x + threadIdx.x; k < n;
+       k += (long long)gridDim.x * blockDim.x) {
+    const int r = (int)(k / R);
+    const long long loc = k - (long long)r * R;
+    int lo = 0, hi = n_seqs - 1;
+    while (lo < hi) {  // last sample whose range [off, off + 2c) contains loc
+      const int mid = (lo + hi + 1) >> 1;
+      if (smp[mid * 4 + 2] <= loc) lo = mid; else hi = mid - 1;
+    }
+    while (lo > 0 && smp[lo * 4 + 1] == 0) --lo;  // skip text-less samples
+    const long long t0 = smp[lo * 4 + 0], c = smp[lo * 4 + 1], off = smp[lo * 4 + 2],
+                    ord0 = smp[lo * 4 + 3];
+    const long long within = loc - off;
+    const int slot = (int)(within / c);
+    const long long t = within - slot * c;
+    const long long ch = slot == 0 ? r : 2 * P - 1 - r;
+    if (fwd_idx) fwd_idx[k] = (int32_t)(t0 + ch * c + t);
+    if (inv_idx) inv_idx[ord0 + ch * c + t] = (int32_t)k;
+  }
+}
+
+// One warp per (row, head): fold the parts in index order,
+// (o, l) (+) (o_p, l_p) with -inf parts contributing nothing.
+__global__ void __launch_bounds__(kThreads) lse_merge_kernel(int n_parts,
+                                                             const float* __restrict__ po,
+                                                             const float* __restrict__ pl,
+                                                             int rows, int H, int d, void* out,
+                                                             int out_bf16, float* lse) {
+  const int lane = threadIdx.x & 31;
+  const long long pairs = (long long)rows * H;
+  const long long stride_part_o = (long long)rows * H * d;
+  const long long stride_part_l = (long long)rows * H;
+  for (long long w = (long long)blockIdx.x * (kThreads / 32) + threadIdx.x / 32; w < pairs;
+       w += (long long)gridDim.x * (kThreads / 32)) {
+    const int h = (int)(w / rows);
+    const long long row = w - (long long)h * rows;
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    float l_run = -INFINITY;
+    for (int p = 0; p < n_parts; ++p) {
+      const float lp = pl[p * stride_part_l + (long long)h * rows + row];
+      const float m = fmaxf(l_run, lp);
+      if (m == -INFINITY) continue;
+      const float wa = expf(l_run - m), wb = expf(lp - m);
+      const float tot = wa + wb;
+      const float ca = wa / tot, cb = wb / tot;
+      const float* src = po + p * stride_part_o + (row * H + h) * (long long)d;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int e = lane + 32 * i;
+        if (e < d) acc[i] = ca * acc[i] + cb * src[e];
+      }
+      l_run = m + logf(tot);
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int e = lane + 32 * i;
+      if (e >= d) continue;
+      const long long o = (row * H + h) * (long long)d + e;
+      if (out_bf16) reinterpret_cast<__nv_bfloat16*>(out)[o] = __float2bfloat16_rn(acc[i]);
+      else reinterpret_cast<float*>(out)[o] = acc[i];
+    }
+    if (lane == 0) lse[(long long)h * rows + row] = l_run;
+  }
+}
+
+template <typename T>
+__device__ __forceinline__ float to_f(T x);
+template <>
+__device__ __forceinline__ float to_f<float>(float x) { return x; }
+template <>
+__device__ __forceinline__ float to_f<__nv_bfloat16>(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+// One warp per (head, token): D = dO . O in fp32, plus the log2-domain lse.
+template <typename T>
+__global__ void __launch_bounds__(kThreads) bwd_pre_kernel(const T* __restrict__ o,
+                                                           const T* __restrict__ dout,
+                                                           const float* __restrict__ lse, int Tn,
+                                                           int H, int d, float* D, float* lse2) {
+  const int lane = threadIdx.x & 31;
+  const long long pairs = (long long)Tn * H;
+  for (long long w = (long long)blockIdx.x * (kThreads / 32) + threadIdx.x / 32; w < pairs;
+       w += (long long)gridDim.x * (kThreads / 32)) {
+    const int h = (int)(w / Tn);
+    const long long t = w - (long long)h * Tn;
+    const long long base = (t * H + h) * (long long)d;
+    float acc = 0.f;
+    for (int e = lane; e < d; e += 32) acc += to_f(o[base + e]) * to_f(dout[base + e]);
+#pragma unroll
+    for (int sh = 16; sh > 0; sh >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, sh);
+    if (lane == 0) {
+      D[(long long)h * Tn + t] = acc;
+      lse2[(long long)h * Tn + t] = lse[(long long)h * Tn + t] * 1.4426950408889634f;
+    }
+  }
+}
+
+// Thread per float4 of the [n*N][H][d] prefix block: fixed-order sum over
+// slots 0..n_slots-1 (ranks, then the prefix queries' own term).
+__global__ void __launch_bounds__(kThreads) prefix_reduce_kernel(
+    const float4* __restrict__ sk, const float4* __restrict__ sv, int n_slots,
+    const int32_t* __restrict__ cu, int N, int H, int d, long long pre_rows, float4* dk,
+    float4* dv) {
+  const long long v_per_row = (long long)H * d / 4;
+  const long long total = pre_rows * v_per_row;
+  for (long long x = (long long)blockIdx.x * blockDim.x + threadIdx.x; x < total;
+       x += (long long)gridDim.x * blockDim.x) {
+    const long long prow = x / v_per_row;
+    const long long e = x - prow * v_per_row;
+    const int i = (int)(prow / N);
+    const long long u = prow - (long long)i * N;
+    float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
+    for (int s = 0; s < n_slots; ++s) {
+      const float4 ka = sk[(long long)s * total + x];
+      const float4 va = sv[(long long)s * total + x];
+      a.x += ka.x; a.y += ka.y; a.z += ka.z; a.w += ka.w;
+      b.x += va.x; b.y += va.y; b.z += va.z; b.w += va.w;
+    }
+    const long long nat = ((long long)cu[i] + u) * v_per_row + e;
+    dk[nat] = a;
+    dv[nat] = b;
+  }
+}
+
+int grid_for(long long work, int per_block) {
+  int dev = 0, sms = 148;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  long long want = (work + per_block - 1) / per_block;
+  long long cap = (long long)sms * 8;
+  if (want < 1) want = 1;
+  return (int)(want < cap ? want : cap);
+}
+
+}  // namespace
+
+cudaError_t launch_gather_rows(const void* const* src, void* const* dst, int n_tensors,
+                               size_t row_bytes, const int32_t* idx, int n_rows, bool scatter,
+                               cudaStream_t st) {
+  if (n_rows <= 0 || n_tensors <= 0) return cudaSuccess;
+  RowPtrs p{};
+  const uint4** s[4] = {&p.s0, &p.s1, &p.s2, &p.s3};
+  uint4** d[4] = {&p.d0, &p.d1, &p.d2, &p.d3};
+  for (int i = 0; i < n_tensors && i < 4; ++i) {
+    *s[i] = static_cast<const uint4*>(src[i]);
+    *d[i] = static_cast<uint4*>(dst[i]);
+  }
+  const long long warps = (long long)n_rows * n_tensors;
+  gather_rows_kernel<<<grid_for(warps, kThreads / 32), kThreads, 0, st>>>(
+      p, n_tensors, (int)(row_bytes / 16), idx, n_rows, scatter ? 1 : 0);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_zigzag_index(const int32_t* smp, int n_seqs, int P, int64_t R,
+                                int32_t* fwd_idx, int32_t* inv_idx, cudaStream_t st) {
+  const long long n = (long long)R * P;
+  if (n == 0) return cudaSuccess;
+  zigzag_index_kernel<<<grid_for(n, kThreads), kThreads, 0, st>>>(smp, n_seqs, P, R, fwd_idx,
+                                                                   inv_idx);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_lse_merge(int n_parts, const float* po, const float* pl, int rows, int H,
+                             int d, void* out, bool out_bf16, float* lse, cudaStream_t st) {
+  const long long pairs = (long long)rows * H;
+  if (pairs == 0) return cudaSuccess;
+  lse_merge_kernel<<<grid_for(pairs, kThreads / 32), kThreads, 0, st>>>(
+      n_parts, po, pl, rows, H, d, out, out_bf16 ? 1 : 0, lse);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_preprocess(const void* out, const void* dout, bool bf16, const float* lse,
+                                  int T, int H, int d, float* D, float* lse2, cudaStream_t st) {
+  const long long pairs = (long long)T * H;
+  if (pairs == 0) return cudaSuccess;
+  const int g = grid_for(pairs, kThreads / 32);
+  if (bf16)
+    bwd_pre_kernel<__nv_bfloat16><<<g, kThreads, 0, st>>>(
+        static_cast<const __nv_bfloat16*>(out), static_cast<const __nv_bfloat16*>(dout), lse, T,
+        H, d, D, lse2);
+  else
+    bwd_pre_kernel<float><<<g, kThreads, 0, st>>>(static_cast<const float*>(out),
+                                                  static_cast<const float*>(dout), lse, T, H, d,
+                                                  D, lse2);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_prefix_reduce(const float* sk, const float* sv, int n_slots, const int32_t* cu,
+                                 int n_seqs, int N, int H, int d, float* dk, float* dv,
+                                 cudaStream_t st) {
+  const long long pre_rows = (long long)n_seqs * N;
+  const long long total = pre_rows * H * d / 4;
+  if (total == 0) return cudaSuccess;
+  prefix_reduce_kernel<<<grid_for(total, kThreads), kThreads, 0, st>>>(
+      reinterpret_cast<const float4*>(sk), reinterpret_cast<const float4*>(sv), n_slots, cu, N, H,
+      d, pre_rows, reinterpret_cast<float4*>(dk), reinterpret_cast<float4*>(dv));
+  return cudaGetLastError();
+}
+
+}  // namespace cpattn

@@ -1,0 +1,91 @@
+// Work lists of the ring steps (host planner <-> kernels).
+//
+// The zigzag split (page "context-parallel-multimodal", §1.1) gives simulated
+// rank r the text chunks r and 2P-r-1 of every sample (§5.3: per sample).  At
+// ring step s rank r meets the KV of rank j = (r - s) mod P; at step 0 its
+// local KV is [replicated image prefix, own chunks] (§4.1 step 4).  Whether a
+// query chunk cq sees a key chunk ck follows from the global causal mask:
+// ck < cq -> every pair visible, ck == cq -> causal within the chunk,
+// ck > cq -> nothing.  The planner turns this into per-tile work items; the
+// kernels only walk runs of rows with an optional causal rule.
+#pragma once
+#include <stdint.h>
+
+#include <string>
+#include <vector>
+
+namespace cpattn {
+
+constexpr int kFwdTileQ = 128;  // query rows of one forward work item
+constexpr int kFwdTileK = 128;  // keys per forward KV tile
+constexpr int kBwdTileK = 128;  // keys of one backward work item
+constexpr int kBwdTileQ = 64;   // query rows per backward inner tile
+constexpr int kMaxSeg = 3;
+
+enum : int32_t { SRC_TEXT = 0, SRC_NAT = 1 };        // rank-local text buffer / natural order
+enum : int32_t { F_FIRST = 1, F_FINAL = 2 };         // forward merge epilogue modes
+enum : int32_t { DK_TEXT = 0, DK_PREFIX_SLOT = 1 };  // backward dK/dV destination
+
+// A run of `len` consecutive rows starting at `row0` of tensor `src`.
+// causal != 0: key u of the key run is visible to query t of the query run
+// iff u <= t + delta (positions inside the same chunk / prefix).
+struct Seg {
+  int32_t row0, len, src, causal, delta, pad0, pad1, pad2;
+};
+
+// Forward: one query tile (<= kFwdTileQ rows) against up to kMaxSeg key runs.
+struct FwdItem {
+  int32_t q_row0, q_len, q_src, nseg;
+  int32_t run_row0;  // row of the fp32 running result (rank-local order), -1: none
+  int32_t out_row0;  // natural row of the first query (final write)
+  int32_t flags;     // F_FIRST | F_FINAL
+  int32_t n_tiles;   // KV tiles visited (cost)
+  Seg seg[kMaxSeg];
+};
+
+// Backward: one key tile (<= kBwdTileK rows, natural order) against up to
+// kMaxSeg query runs (natural order).
+struct BwdItem {
+  int32_t k_row0, k_len, nseg, n_tiles;
+  int32_t dk_mode;  // DK_TEXT: dk/dv natural rows k_row0..; DK_PREFIX_SLOT: slot buffer
+  int32_t dk_row0;  // row inside the prefix slot buffer (DK_PREFIX_SLOT)
+  int32_t slot;     // prefix slot: rank 0..P-1, or P for the prefix queries' own term
+  int32_t flags;    // F_FIRST: overwrite the destination, else accumulate
+  Seg seg[kMaxSeg];
+};
+
+static_assert(sizeof(Seg) == 32, "Seg layout");
+static_assert(sizeof(FwdItem) == 128, "FwdItem layout");
+static_assert(sizeof(BwdItem) == 128, "BwdItem layout");
+
+struct Problem {
+  int T = 0, H = 0, d = 0, P = 0, N = 0, n_seqs = 0;
+  std::vector<int32_t> cu;     // n_seqs + 1
+  std::vector<int32_t> c;      // chunk length per sample
+  std::vector<int32_t> off;    // rank-local offset of each sample (sum of 2c before it)
+  int64_t R = 0;               // rank-local text rows per rank
+  int64_t text_rows = 0;       // P * R
+};
+
+// Validates shapes; returns "" on success or a message.
+std::string make_problem(const int32_t* cu_seqlens, int n_seqs, int prefix_len, int P, int T,
+                         int H, int d, Problem* out);
+
+// Zigzag tables (natural index of permuted row; permuted row of text ordinal).
+void zigzag_tables(const Problem& pb, int32_t* fwd_idx, int32_t* inv_idx);
+
+struct FwdPlan {
+  std::vector<FwdItem> items;
+  std::vector<int32_t> step_begin;  // P + 1 offsets into items
+};
+struct BwdPlan {
+  std::vector<BwdItem> items;
+  std::vector<int32_t> step_begin;
+};
+
+// text_perm = true: text rows address the rank-local (gathered) buffer;
+// false: they address natural order (used by the fp32 dQ pass).
+void plan_forward(const Problem& pb, bool text_perm, FwdPlan* plan);
+void plan_backward(const Problem& pb, BwdPlan* plan);
+
+}  // namespace cpattn

@@ -1,0 +1,42 @@
+// Tensor-core (tcgen05 / TMEM / TMA) attention kernels for sm_103a.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "plan.h"
+
+namespace cpattn {
+
+// 3-D tensor map over a bf16 [rows][H][d] tensor, box {64, 1, rows_per_box},
+// 128-byte swizzle.  Returns false (and a message) if encoding fails.
+bool make_tmap_thd(CUtensorMap* map, const void* base, int64_t rows, int H, int d,
+                   int rows_per_box, const char** err);
+
+struct TcFwdArgs {
+  CUtensorMap tm_q_text, tm_k_text, tm_v_text;  // rank-local (gathered) text rows
+  CUtensorMap tm_q_nat, tm_k_nat, tm_v_nat;     // natural order (prefix rows)
+  const FwdItem* items;
+  int n_items, H, d;
+  float scale_log2;           // softmax scale * log2(e)
+  float* o_run; float* lse_run; int64_t run_rows;
+  void* out; float* lse; int64_t T;
+  int32_t* status;            // DevStatus of the workspace
+  long long wait_limit;
+};
+cudaError_t launch_tc_fwd(const TcFwdArgs& a, cudaStream_t st);
+
+struct TcBwdArgs {
+  CUtensorMap tm_q, tm_k, tm_v, tm_do;  // natural order
+  const BwdItem* items;
+  int n_items, H, d;
+  float scale, scale_log2;
+  const float* D; const float* lse2; int64_t T;  // [H][T]
+  float* dq; float* dk; float* dv;
+  float* pre_k; float* pre_v; int64_t pre_rows;
+  int32_t* status;
+  long long wait_limit;
+};
+cudaError_t launch_tc_bwd(const TcBwdArgs& a, cudaStream_t st);
+
+}  // namespace cpattn
