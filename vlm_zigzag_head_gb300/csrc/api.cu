@@ -130,7 +130,7 @@ PlanCache& plan_cache() {
 cp_status_t get_plans(const int32_t* cu, int n_seqs, int N, int P, int T, int H, int d,
                       std::shared_ptr<PlanSet>* out) {
   Problem pb;
-  std::string err = make_problem(cu, n_seqs, N, P, T, H, d, &pb);
+  std::string err = make_problem(cu, n_seqs, N, P, T, &pb);
   if (!err.empty()) return fail(CP_ERR_SHAPE, err);
   PlanCache& pc = plan_cache();
   {
@@ -289,7 +289,7 @@ cp_status_t cp_zigzag_index(const int32_t* cu, int n_seqs, int N, int P, int32_t
     return CP_OK;
   }
   Problem pb;
-  std::string err = make_problem(cu, n_seqs, N, P, -1, 1, 64, &pb);
+  std::string err = make_problem(cu, n_seqs, N, P, -1, &pb);
   if (!err.empty()) return fail(CP_ERR_SHAPE, err);
   zigzag_tables(pb, fwd_idx, inv_idx);
   return CP_OK;
@@ -433,7 +433,7 @@ size_t cp_attn_bwd_workspace_size(cp_dtype_t dt, int T, int H, int d, const int3
   std::shared_ptr<PlanSet> ps;
   if (!cu || H < 1 || (dt != CP_F32 && dt != CP_BF16)) return 0;
   if (get_plans(cu, n_seqs, N, P, T, H, d, &ps) != CP_OK) return 0;
-  const bool simt = !(dt == CP_BF16 && use_tc_path());
+  const bool simt = !(dt == CP_BF16 && use_tc_path() && d == 128);
   return bwd_layout(*ps, H, d, simt, true).total;
 }
 
@@ -451,7 +451,8 @@ cp_status_t cp_attn_bwd(const void* q, const void* k, const void* v, const void*
   if (s != CP_OK) return s;
   if (T == 0) return CP_OK;
   const bool bf16 = dt == CP_BF16;
-  const bool tc = bf16 && use_tc_path();
+  // the tensor-core backward is built for head_dim 128; head_dim 64 runs on CUDA cores
+  const bool tc = bf16 && use_tc_path() && d == 128;
   if (tc && (s = check_device_for_bf16()) != CP_OK) return s;
   const BwdWs L = bwd_layout(*ps, H, d, !tc, pgrad == nullptr);
   if (!ws || ws_bytes < L.total)
@@ -538,7 +539,7 @@ cp_status_t cp_plan_pairs(const int32_t* cu, int n_seqs, int N, int P, int64_t* 
                           int64_t* bwd_pairs, int64_t* fwd_items, int64_t* bwd_items) {
   if (!cu || n_seqs < 1 || P < 1 || N < 0) return fail(CP_ERR_INVALID_ARG, "bad arguments");
   Problem pb;
-  std::string err = make_problem(cu, n_seqs, N, P, -1, 1, 64, &pb);
+  std::string err = make_problem(cu, n_seqs, N, P, -1, &pb);
   if (!err.empty()) return fail(CP_ERR_SHAPE, err);
   FwdPlan f;
   BwdPlan b;

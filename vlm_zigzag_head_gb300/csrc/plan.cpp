@@ -49,8 +49,8 @@ int64_t bwd_visible(const Seg& s) {
 
 }  // namespace
 
-std::string make_problem(const int32_t* cu, int n_seqs, int prefix_len, int P, int T, int H,
-                         int d, Problem* out) {
+std::string make_problem(const int32_t* cu, int n_seqs, int prefix_len, int P, int T,
+                         Problem* out) {
   char buf[256];
   if (!cu) return "cu_seqlens is NULL";
   if (n_seqs < 1) return "n_seqs must be >= 1";
@@ -58,9 +58,7 @@ std::string make_problem(const int32_t* cu, int n_seqs, int prefix_len, int P, i
   if (prefix_len < 0) return "prefix_len must be >= 0";
   if (cu[0] != 0) return "cu_seqlens[0] must be 0";
   Problem pb;
-  pb.T = T;
-  pb.H = H;
-  pb.d = d;
+  pb.T = cu[n_seqs];  // plans are cached per cu_seqlens: never the caller's T
   pb.P = P;
   pb.N = prefix_len;
   pb.n_seqs = n_seqs;

@@ -59,7 +59,7 @@ static_assert(sizeof(FwdItem) == 128, "FwdItem layout");
 static_assert(sizeof(BwdItem) == 128, "BwdItem layout");
 
 struct Problem {
-  int T = 0, H = 0, d = 0, P = 0, N = 0, n_seqs = 0;
+  int T = 0, P = 0, N = 0, n_seqs = 0;   // T = cu[n_seqs]
   std::vector<int32_t> cu;     // n_seqs + 1
   std::vector<int32_t> c;      // chunk length per sample
   std::vector<int32_t> off;    // rank-local offset of each sample (sum of 2c before it)
@@ -67,9 +67,10 @@ struct Problem {
   int64_t text_rows = 0;       // P * R
 };
 
-// Validates shapes; returns "" on success or a message.
+// Validates shapes (T < 0: do not check cu_seqlens[n] against T); returns ""
+// on success or a message.
 std::string make_problem(const int32_t* cu_seqlens, int n_seqs, int prefix_len, int P, int T,
-                         int H, int d, Problem* out);
+                         Problem* out);
 
 // Zigzag tables (natural index of permuted row; permuted row of text ordinal).
 void zigzag_tables(const Problem& pb, int32_t* fwd_idx, int32_t* inv_idx);

@@ -1,0 +1,455 @@
+// Ring-step attention backward on 5th-generation tensor cores (sm_103a).
+//
+// One CTA owns one key tile (128 keys, one head) of a ring step and walks the
+// query runs that met those keys at that step (page
+// "context-parallel-multimodal" §4.2: each rank differentiates its queries
+// against the KV it saw; the KV owner receives dK/dV; the replicated prefix
+// gets one gradient per rank).  Per 64-row query tile, with the final lse:
+//
+//   S^T  = K Q^T            dP^T = V dO^T                      (TMEM)
+//   P^T  = exp2(S^T * scale*log2e - lse2),  dS^T = P^T (dP^T - D)   (registers)
+//   dV  += P^T dO           dK  += dS^T Q                      (TMEM, whole item)
+//   dQ^T = K^T dS^T  -> fp32 atomic adds into dQ (scaled)
+//
+// Warp roles (384 threads):
+//   warp 0       TMA producer (K, V once; Q, dO, lse2, D per query tile)
+//   warp 1       TMEM allocation; lane 0 issues every tcgen05.mma
+//   warps 2, 3   idle
+//   warps 4..7   P / dS computation, then the dK / dV epilogue; thread = key row
+//   warps 8..11  dQ drain; thread = head-dim index (TMEM lane of dQ^T)
+//
+// TMEM columns: S^T [0,64), dP^T [64,128), dQ^T ping-pong [128,192) and
+// [192,256), dK [256,384), dV [384,512).
+#include <cuda_bf16.h>
+
+#include "kernels.h"
+#include "ptx.cuh"
+#include "tc.h"
+
+namespace cpattn {
+
+namespace {
+
+using namespace ptx;
+
+constexpr int kThreads = 384;
+constexpr int kD = 128;            // head dim of this kernel
+constexpr int kBK = kBwdTileK;     // 128 keys
+constexpr int kBQ = kBwdTileQ;     // 64 queries per inner tile
+constexpr int kStages = 2;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColS = 0, kColDP = 64, kColDQ0 = 128, kColDQ1 = 192, kColDK = 256,
+                   kColDV = 384;
+constexpr long long kDrainLimit = 1LL << 24;
+
+struct L {
+  static constexpr int kKVBox = 128 * 128;   // 128 rows x 128 bytes
+  static constexpr int kQBox = kBQ * 128;    // 64 rows x 128 bytes
+  static constexpr int kK = 0;
+  static constexpr int kV = kK + 2 * kKVBox;
+  static constexpr int kQ = kV + 2 * kKVBox;              // [stage][2 boxes]
+  static constexpr int kDO = kQ + kStages * 2 * kQBox;
+  static constexpr int kP = kDO + kStages * 2 * kQBox;     // [buf] 128 x 64 bf16
+  static constexpr int kDS = kP + 2 * kKVBox;
+  static constexpr int kLse = kDS + 2 * kKVBox;           // [stage][64] lse2, [stage][64] D
+  static constexpr int kBars = kLse + kStages * 2 * kBQ * 4;
+  static constexpr int kBytes = kBars + 512;
+  static constexpr int kAlloc = kBytes + 1024;
+};
+
+struct Bars {
+  uint64_t kv_full;
+  uint64_t qdo_full[kStages], qdo_empty[kStages];
+  uint64_t sdp_full, sdp_empty;
+  uint64_t ps_full[2], ps_empty[2];
+  uint64_t dq_full[2], dq_empty[2];
+  uint64_t dkv_done;
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort;
+};
+
+__device__ __forceinline__ int run_qtiles(const Seg& s) {
+  const int start = s.causal && s.delta < 0 ? -s.delta : 0;
+  const int n = s.len - start;
+  return n > 0 ? (n + kBQ - 1) / kBQ : 0;
+}
+__device__ __forceinline__ int run_qstart(const Seg& s) {
+  return s.causal && s.delta < 0 ? -s.delta : 0;
+}
+
+__device__ __forceinline__ void record_timeout(int32_t* status, volatile int* abort, int site) {
+  if (atomicCAS(&status[0], 0, 1) == 0) status[1] = site;
+  *abort = 1;
+}
+
+__global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_constant__ TcBwdArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  Bars* bars = reinterpret_cast<Bars*>(smem + L::kBars);
+  float* lse_s = reinterpret_cast<float*>(smem + L::kLse);  // [stage][2][64]
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int item_idx = blockIdx.x % a.n_items;
+  const int h = blockIdx.x / a.n_items;
+  const BwdItem& it = a.items[item_idx];
+  volatile int* abort = &bars->abort;
+  const long long lim = a.wait_limit;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bars->kv_full, 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&bars->qdo_full[s], 1);
+      mbar_init(&bars->qdo_empty[s], 1);
+    }
+    mbar_init(&bars->sdp_full, 1);
+    mbar_init(&bars->sdp_empty, 4);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&bars->ps_full[b], 4);
+      mbar_init(&bars->ps_empty[b], 1);
+      mbar_init(&bars->dq_full[b], 1);
+      mbar_init(&bars->dq_empty[b], 4);
+    }
+    mbar_init(&bars->dkv_done, 1);
+    mbar_init(&bars->drain, 1);
+    bars->abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&bars->tmem_base, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+
+  const int nseg = it.nseg;
+  int n_qt = 0;
+  for (int s = 0; s < nseg; ++s) n_qt += run_qtiles(it.seg[s]);
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    int issued = 0;
+    bool kv_issued = false;
+    if (n_qt > 0) {
+      if (lane == 0) {
+        mbar_expect_tx(&bars->kv_full, 4 * L::kKVBox);
+        for (int b = 0; b < 2; ++b) {
+          tma_load_3d(&a.tm_k, &bars->kv_full, smem + L::kK + b * L::kKVBox, b * 64, h, it.k_row0);
+          tma_load_3d(&a.tm_v, &bars->kv_full, smem + L::kV + b * L::kKVBox, b * 64, h, it.k_row0);
+        }
+      }
+      kv_issued = true;
+    }
+    // decisions are taken by lane 0 and broadcast: the warp never diverges
+    // around the __syncwarp below
+    int j = 0;
+    bool go = true;
+    for (int s = 0; go && s < nseg; ++s) {
+      const Seg sg = it.seg[s];
+      const int q0 = run_qstart(sg), nt = run_qtiles(sg);
+      for (int t = 0; t < nt; ++t, ++j) {
+        const int st = j % kStages;
+        int w_ok = 1;
+        if (lane == 0) {
+          w_ok = !*abort && (j < kStages ||
+                             mbar_wait(&bars->qdo_empty[st], ((j / kStages) - 1) & 1, lim, abort));
+          if (!w_ok) record_timeout(a.status, abort, 11);
+        }
+        go = __shfl_sync(0xffffffffu, w_ok, 0) != 0;
+        if (!go) break;
+        // lse2 / D of the tile's 64 queries; rows past the run get lse2 = +inf (P = 0)
+        const int row0 = q0 + t * kBQ;
+        float* ls = lse_s + st * 2 * kBQ;
+#pragma unroll
+        for (int x = lane; x < kBQ; x += 32) {
+          const bool in = row0 + x < sg.len;
+          const long long g = (long long)h * a.T + sg.row0 + row0 + x;
+          ls[x] = in ? a.lse2[g] : INFINITY;
+          ls[kBQ + x] = in ? a.D[g] : 0.f;
+        }
+        __syncwarp();
+        if (lane == 0) {
+          mbar_expect_tx(&bars->qdo_full[st], 4 * L::kQBox);
+          for (int b = 0; b < 2; ++b) {
+            tma_load_3d(&a.tm_q, &bars->qdo_full[st], smem + L::kQ + (st * 2 + b) * L::kQBox,
+                        b * 64, h, sg.row0 + row0);
+            tma_load_3d(&a.tm_do, &bars->qdo_full[st], smem + L::kDO + (st * 2 + b) * L::kQBox,
+                        b * 64, h, sg.row0 + row0);
+          }
+        }
+        issued = j + 1;
+      }
+    }
+    // every load issued here must have landed before the CTA exits (normally
+    // the consumers already waited for them and these waits return at once)
+    if (lane == 0) {
+      int zero = 0;
+      if (kv_issued) mbar_wait(&bars->kv_full, 0, kDrainLimit, &zero);
+      for (int x = issued - kStages; x < issued; ++x) {
+        if (x < 0) continue;
+        mbar_wait(&bars->qdo_full[x % kStages], (x / kStages) & 1, kDrainLimit, &zero);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc_sdp = idesc_bf16(kBK, kBQ, 0, 0);   // K-major A and B
+      constexpr uint32_t idesc_kv = idesc_bf16(kBK, kD, 0, 1);     // B (Q, dO) MN-major
+      constexpr uint32_t idesc_dq = idesc_bf16(kD, kBQ, 1, 1);     // A (K^T), B (dS^T) MN-major
+      const uint32_t k_addr = smem_u32(smem + L::kK), v_addr = smem_u32(smem + L::kV);
+      bool ok = n_qt == 0 || mbar_wait(&bars->kv_full, 0, lim, abort);
+      auto issue_grads = [&](int i) -> bool {
+        const int st = i % kStages, b = i & 1;
+        if (!mbar_wait(&bars->ps_full[b], (i >> 1) & 1, lim, abort)) return false;
+        if (i >= 2 && !mbar_wait(&bars->dq_empty[b], ((i >> 1) - 1) & 1, lim, abort)) return false;
+        tc_fence_after();
+        const uint32_t p_addr = smem_u32(smem + L::kP + b * L::kKVBox);
+        const uint32_t ds_addr = smem_u32(smem + L::kDS + b * L::kKVBox);
+        const uint32_t q_addr = smem_u32(smem + L::kQ + st * 2 * L::kQBox);
+        const uint32_t do_addr = smem_u32(smem + L::kDO + st * 2 * L::kQBox);
+#pragma unroll
+        for (int kk = 0; kk < kBQ / 16; ++kk) {     // over queries
+          const uint64_t pa = sdesc_sw128(p_addr + kk * 32, 16, 1024);
+          const uint64_t da = sdesc_sw128(ds_addr + kk * 32, 16, 1024);
+          const uint64_t ob = sdesc_sw128(do_addr + kk * 16 * 128, L::kQBox, 1024);
+          const uint64_t qb = sdesc_sw128(q_addr + kk * 16 * 128, L::kQBox, 1024);
+          const uint32_t acc = (i > 0 || kk > 0) ? 1u : 0u;
+          mma_bf16(tmem + kColDV, pa, ob, idesc_kv, acc);
+          mma_bf16(tmem + kColDK, da, qb, idesc_kv, acc);
+        }
+#pragma unroll
+        for (int kk = 0; kk < kBK / 16; ++kk) {     // over keys
+          const uint64_t ka = sdesc_sw128(k_addr + kk * 16 * 128, L::kKVBox, 1024);
+          const uint64_t sb = sdesc_sw128(ds_addr + kk * 16 * 128, 16, 1024);
+          mma_bf16(tmem + (b ? kColDQ1 : kColDQ0), ka, sb, idesc_dq, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(&bars->qdo_empty[st]);
+        mma_commit(&bars->ps_empty[b]);
+        mma_commit(&bars->dq_full[b]);
+        return true;
+      };
+      for (int i = 0; ok && i < n_qt; ++i) {
+        const int st = i % kStages;
+        if (!mbar_wait(&bars->qdo_full[st], (i / kStages) & 1, lim, abort) ||
+            (i >= 1 && !mbar_wait(&bars->sdp_empty, (i - 1) & 1, lim, abort))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t q_addr = smem_u32(smem + L::kQ + st * 2 * L::kQBox);
+        const uint32_t do_addr = smem_u32(smem + L::kDO + st * 2 * L::kQBox);
+#pragma unroll
+        for (int kk = 0; kk < kD / 16; ++kk) {      // over head dim
+          const uint32_t ko = (kk / 4) * L::kKVBox + (kk % 4) * 32;
+          const uint32_t qo = (kk / 4) * L::kQBox + (kk % 4) * 32;
+          mma_bf16(tmem + kColS, sdesc_sw128(k_addr + ko, 16, 1024),
+                   sdesc_sw128(q_addr + qo, 16, 1024), idesc_sdp, kk > 0 ? 1u : 0u);
+          mma_bf16(tmem + kColDP, sdesc_sw128(v_addr + ko, 16, 1024),
+                   sdesc_sw128(do_addr + qo, 16, 1024), idesc_sdp, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(&bars->sdp_full);
+        if (i >= 1 && !issue_grads(i - 1)) {
+          ok = false;
+          break;
+        }
+      }
+      if (ok && n_qt > 0 && !issue_grads(n_qt - 1)) ok = false;
+      if (ok && n_qt > 0) mma_commit(&bars->dkv_done);
+      if (!ok) {
+        record_timeout(a.status, abort, 12);
+        mma_commit(&bars->drain);
+        int zero = 0;
+        mbar_wait(&bars->drain, 0, kDrainLimit, &zero);
+      }
+    }
+  } else if (warp >= 4 && warp < 8) {
+    // ------------------------------------------------------------ P / dS
+    const int u = threadIdx.x - 128;             // key row == TMEM lane
+    const uint32_t lane_off = (uint32_t)((warp - 4) * 32) << 16;
+    const float sl2 = a.scale_log2;
+    const bool key_ok = u < it.k_len;
+    bool ok = true;
+    int i = 0;
+    for (int s = 0; ok && s < nseg; ++s) {
+      const Seg sg = it.seg[s];
+      const int q0 = run_qstart(sg), nt = run_qtiles(sg);
+      for (int t = 0; t < nt; ++t, ++i) {
+        const int st = i % kStages, b = i & 1;
+        if (!mbar_wait(&bars->sdp_full, i & 1, lim, abort) ||
+            !mbar_wait(&bars->qdo_full[st], (i / kStages) & 1, lim, abort)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        float sv[kBQ], dp[kBQ];
+        {
+          uint32_t r[32];
+#pragma unroll
+          for (int c = 0; c < kBQ / 32; ++c) {
+            tmem_ld32(tmem + lane_off + kColS + c * 32, r);
+            tmem_ld_wait();
+            reg_fence32(r);
+#pragma unroll
+            for (int x = 0; x < 32; ++x) sv[c * 32 + x] = __uint_as_float(r[x]);
+            tmem_ld32(tmem + lane_off + kColDP + c * 32, r);
+            tmem_ld_wait();
+            reg_fence32(r);
+#pragma unroll
+            for (int x = 0; x < 32; ++x) dp[c * 32 + x] = __uint_as_float(r[x]);
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->sdp_empty);
+        const float* ls = lse_s + st * 2 * kBQ;
+        const int row0 = q0 + t * kBQ;            // query index inside the run
+        // causal: key u visible to query row0 + x iff u <= row0 + x + delta
+        const int first_vis = u - sg.delta - row0;  // smallest visible x
+#pragma unroll
+        for (int x = 0; x < kBQ; ++x) {
+          float p = ex2(sv[x] * sl2 - ls[x]);
+          if (!key_ok || (sg.causal && x < first_vis)) p = 0.f;
+          sv[x] = p;
+          dp[x] = p * (dp[x] - ls[kBQ + x]);
+        }
+        if (i >= 2 && !mbar_wait(&bars->ps_empty[b], ((i >> 1) - 1) & 1, lim, abort)) {
+          ok = false;
+          break;
+        }
+        uint8_t* prow = smem + L::kP + b * L::kKVBox + u * 128;
+        uint8_t* srow = smem + L::kDS + b * L::kKVBox + u * 128;
+#pragma unroll
+        for (int c = 0; c < kBQ / 8; ++c) {
+          uint4 pv, dv;
+          pv.x = pack_bf16x2(sv[c * 8 + 0], sv[c * 8 + 1]);
+          pv.y = pack_bf16x2(sv[c * 8 + 2], sv[c * 8 + 3]);
+          pv.z = pack_bf16x2(sv[c * 8 + 4], sv[c * 8 + 5]);
+          pv.w = pack_bf16x2(sv[c * 8 + 6], sv[c * 8 + 7]);
+          dv.x = pack_bf16x2(dp[c * 8 + 0], dp[c * 8 + 1]);
+          dv.y = pack_bf16x2(dp[c * 8 + 2], dp[c * 8 + 3]);
+          dv.z = pack_bf16x2(dp[c * 8 + 4], dp[c * 8 + 5]);
+          dv.w = pack_bf16x2(dp[c * 8 + 6], dp[c * 8 + 7]);
+          const int sw = (c ^ (u & 7)) << 4;
+          *reinterpret_cast<uint4*>(prow + sw) = pv;
+          *reinterpret_cast<uint4*>(srow + sw) = dv;
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->ps_full[b]);
+      }
+    }
+    // ------------------------------------------------------------ dK / dV epilogue
+    if (ok && n_qt > 0 && !mbar_wait(&bars->dkv_done, 0, lim, abort)) ok = false;
+    if (!ok) {
+      record_timeout(a.status, abort, 13);
+    } else {
+      tc_fence_after();
+      float* pk;
+      float* pv;
+      if (it.dk_mode == DK_TEXT) {
+        pk = a.dk + ((long long)(it.k_row0 + u) * a.H + h) * kD;
+        pv = a.dv + ((long long)(it.k_row0 + u) * a.H + h) * kD;
+      } else {
+        const long long row = (long long)it.slot * a.pre_rows + it.dk_row0 + u;
+        pk = a.pre_k + (row * a.H + h) * kD;
+        pv = a.pre_v + (row * a.H + h) * kD;
+      }
+      const bool first = (it.flags & F_FIRST) != 0;
+#pragma unroll 1
+      for (int which = 0; which < 2; ++which) {
+        float* dst = which == 0 ? pk : pv;
+        const float mul = which == 0 ? a.scale : 1.f;
+        const uint32_t col = which == 0 ? kColDK : kColDV;
+#pragma unroll 1
+        for (int c = 0; c < kD / 32; ++c) {
+          uint32_t r[32];
+          if (n_qt > 0) {
+            tmem_ld32(tmem + lane_off + col + c * 32, r);
+            tmem_ld_wait();
+            reg_fence32(r);
+          } else {
+#pragma unroll
+            for (int x = 0; x < 32; ++x) r[x] = 0u;
+          }
+          if (!key_ok) continue;
+#pragma unroll
+          for (int x = 0; x < 32; x += 4) {
+            float4 v = make_float4(__uint_as_float(r[x]) * mul, __uint_as_float(r[x + 1]) * mul,
+                                   __uint_as_float(r[x + 2]) * mul,
+                                   __uint_as_float(r[x + 3]) * mul);
+            float4* d4 = reinterpret_cast<float4*>(dst + c * 32 + x);
+            if (!first) {
+              const float4 o = *d4;
+              v.x += o.x; v.y += o.y; v.z += o.z; v.w += o.w;
+            }
+            *d4 = v;
+          }
+        }
+      }
+    }
+  } else if (warp >= 8) {
+    // ------------------------------------------------------------ dQ drain
+    const int dd = threadIdx.x - 256;            // head-dim index == TMEM lane of dQ^T
+    const uint32_t lane_off = (uint32_t)((warp - 8) * 32) << 16;
+    bool ok = true;
+    int i = 0;
+    for (int s = 0; ok && s < nseg; ++s) {
+      const Seg sg = it.seg[s];
+      const int q0 = run_qstart(sg), nt = run_qtiles(sg);
+      for (int t = 0; t < nt; ++t, ++i) {
+        const int b = i & 1;
+        if (!mbar_wait(&bars->dq_full[b], (i >> 1) & 1, lim, abort)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        float v[kBQ];
+        {
+          uint32_t r[32];
+#pragma unroll
+          for (int c = 0; c < kBQ / 32; ++c) {
+            tmem_ld32(tmem + lane_off + (b ? kColDQ1 : kColDQ0) + c * 32, r);
+            tmem_ld_wait();
+            reg_fence32(r);
+#pragma unroll
+            for (int x = 0; x < 32; ++x) v[c * 32 + x] = __uint_as_float(r[x]);
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->dq_empty[b]);
+        const int row0 = q0 + t * kBQ;
+        const int nrow = min(kBQ, sg.len - row0);
+        float* base = a.dq + ((long long)(sg.row0 + row0) * a.H + h) * kD + dd;
+        const long long stride = (long long)a.H * kD;
+        for (int x = 0; x < nrow; ++x) atomicAdd(base + x * stride, v[x] * a.scale);
+      }
+    }
+    if (!ok) record_timeout(a.status, abort, 14);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_tc_bwd(const TcBwdArgs& a, cudaStream_t st) {
+  if (a.n_items == 0) return cudaSuccess;
+  if (a.d != kD) return cudaErrorNotSupported;
+  cudaError_t e = cudaFuncSetAttribute(tc_bwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       L::kAlloc);
+  if (e != cudaSuccess) return e;
+  const long long blocks = (long long)a.n_items * a.H;
+  if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  tc_bwd_kernel<<<(unsigned)blocks, kThreads, L::kAlloc, st>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace cpattn
