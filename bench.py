@@ -1,0 +1,356 @@
+"""Throughput of zigzag context-parallel causal attention (forward + backward).
+
+One step = one pass of the whole hot path over one batch of synthetic input:
+cp_attn_fwd (zigzag gather, P ring-step kernels with the fused log-sum-exp
+merge) followed by cp_attn_bwd (preprocess, P ring-step kernels, prefix
+gradient sum).  Default workload: "long" -- 131072 text tokens, P = 8
+simulated ranks, 32 heads, head_dim 128, bf16; inputs are ~1 GiB per tensor,
+far larger than L2, so no flush is needed between steps.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+    python bench.py --impl reference ...   # the CPU oracle on the host cores
+
+Prints one JSON line (rank 0).  With N > 1 (torchrun) every rank runs an
+independent replica (the path does not shard across GPUs); value is the sum
+of all ranks' work over the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from vlm_zigzag_head_gb300 import workloads as W  # noqa: E402
+
+METRIC = "CP causal attention TFLOP/s fwd & fwd+bwd, % of GB300 BF16 tensor peak"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def causal_pairs(w) -> int:
+    """Visible (query, key) pairs per head: per sample n(n+1)/2 over [prefix, text]."""
+    return sum((w.prefix_len + L) * (w.prefix_len + L + 1) // 2 for L in W.text_lengths(w))
+
+
+def fwd_flops(w) -> float:
+    """Algorithmic forward FLOPs: 4 d per visible pair and head (QK^T + PV)."""
+    return 4.0 * w.d * w.H * causal_pairs(w)
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join("/tmp", "cpattn_clocks_%d_%d.csv" % (os.getpid(), index))
+
+    def __enter__(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.Q,
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    mx.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle leg
+# ---------------------------------------------------------------------------
+def oracle_sample(w, n_queries: int = 8192):
+    """A bounded, exact piece of the workload for the CPU oracle: the first
+    n_queries text tokens of sample 0, head 0 (causal: they see only keys
+    before them), forward and backward.  Returns (seconds, algorithmic FLOPs,
+    description)."""
+    import numpy as np  # noqa: F401
+    import oracle
+    x = W.make_inputs(w)
+    a = 0
+    n = min(n_queries, x.cu_seqlens[1])
+    q, k, v, do = (t[a:a + n, :1] for t in (x.q, x.k, x.v, x.dout))
+    cu = [0, n]
+    t0 = time.perf_counter()
+    oracle.causal_attention_fwd(q, k, v, cu, x.scale)
+    oracle.causal_attention_bwd(q, k, v, do, cu, x.scale)
+    dt = time.perf_counter() - t0
+    flops = 3.5 * 4.0 * w.d * (n * (n + 1) // 2)
+    desc = ("first %d tokens of sample 0, head 0 of the '%s' workload (causal: a complete "
+            "slice of its work), oracle forward + backward in fp64" % (n, w.name))
+    return dt, flops, desc
+
+
+def run_reference(args, w, rank, world):
+    if rank != 0:
+        return 0
+    cores = os.cpu_count()
+    times, flops = [], 0.0
+    desc = ""
+    n_q = args.oracle_queries
+    for _ in range(args.warmup if args.warmup < 1 else 1):
+        oracle_sample(w, n_q // 2)
+    for _ in range(args.steps):
+        dt, flops, desc = oracle_sample(w, n_q)
+        times.append(dt)
+    t = sum(times) / len(times)
+    val = flops / t / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": val, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": w.name, "sample": desc},
+        "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------------
+# CUDA leg
+# ---------------------------------------------------------------------------
+def run_cuda(args, w, rank, world, dist):
+    import vlm_zigzag_head_gb300 as cp
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    x = W.make_inputs(w)
+    stream = torch.cuda.current_stream(dev)
+    qd, kd, vd, dod = (t.to(dev) for t in (x.q, x.k, x.v, x.dout))
+    cu, P, N, scale = x.cu_seqlens, w.P, w.prefix_len, x.scale
+    T, H, d = qd.shape
+    out = torch.empty_like(qd)
+    out_lo = torch.empty_like(qd)
+    lse = torch.empty((H, T), dtype=torch.float32, device=dev)
+    grads = tuple(torch.empty((T, H, d), dtype=torch.float32, device=dev) for _ in range(3))
+    ws_f, ws_b = cp.Workspace(dev), cp.Workspace(dev)
+
+    def step():
+        cp.cp_attn_fwd(qd, kd, vd, cu, P, N, scale, out=out, lse=lse, workspace=ws_f,
+                       residual=True, out_lo=out_lo)
+        cp.cp_attn_bwd(qd, kd, vd, out, lse, dod, cu, P, N, scale, workspace=ws_b, grads=grads,
+                       out_lo=out_lo)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    if cp.cp_workspace_status(ws_f) or cp.cp_workspace_status(ws_b):
+        raise RuntimeError("a device wait timed out during warm-up")
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    f_flops = fwd_flops(w)
+    total = 3.5 * f_flops
+    # ---- timed region: K steps, CUDA events on the launching stream
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(dev.index) as clk:
+        barrier()
+        cp.cp_profile_begin()
+        e0.record(stream)
+        for _ in range(args.steps):
+            step()
+        e1.record(stream)
+        barrier()
+        prof = cp.cp_profile_end()
+    ms = e0.elapsed_time(e1)
+    if dist is not None:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    if cp.cp_workspace_status(ws_f) or cp.cp_workspace_status(ws_b):
+        raise RuntimeError("a device wait timed out in the timed region")
+    ms_step = ms / args.steps
+    value = world * total * args.steps / (ms / 1e3) / 1e12
+    peaks, peak_src = load_peaks()
+    peak_sus = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+
+    # fwd-only and bwd-only timing (same workload, separate short loops)
+    def timed(fn, n):
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(dev)
+        a0.record(stream)
+        for _ in range(n):
+            fn()
+        a1.record(stream)
+        torch.cuda.synchronize(dev)
+        return a0.elapsed_time(a1) / n
+
+    n_sub = max(1, min(args.steps, 3))
+    fwd_ms = timed(lambda: cp.cp_attn_fwd(qd, kd, vd, cu, P, N, scale, out=out, lse=lse,
+                                          workspace=ws_f, residual=True, out_lo=out_lo), n_sub)
+    bwd_ms = timed(lambda: cp.cp_attn_bwd(qd, kd, vd, out, lse, dod, cu, P, N, scale,
+                                          workspace=ws_b, grads=grads, out_lo=out_lo), n_sub)
+
+    # dominant kernel: the tensor-core backward ring step (algorithmic FLOPs:
+    # 10 d per visible pair and head, summed over the P step launches)
+    bwd_ms_k, bwd_launches = prof["tc_bwd_step"]
+    fwd_ms_k, fwd_launches = prof["tc_fwd_step"]
+    bwd_launch_flops = 2.5 * f_flops / P
+    fwd_launch_flops = f_flops / P
+    roof = None
+    if bwd_launches:
+        avg = bwd_ms_k / bwd_launches
+        ach = bwd_launch_flops / (avg / 1e3) / 1e12
+        roof = {"kernel": "tc_bwd_kernel (backward ring step)", "bound": "tensor",
+                "achieved": ach, "peak": peak_sus, "unit": "TFLOP/s", "frac": ach / peak_sus,
+                "peak_source": "%s bf16_tflops_sustained" % peak_src,
+                "traffic": args.traffic, "launch_ms": avg,
+                "flops_per_launch": bwd_launch_flops}
+    kernels = {}
+    for k, (kms, n) in prof.items():
+        if n:
+            kernels[k] = {"launches": n, "ms_total": kms, "share": kms / max(ms, 1e-9)}
+    if fwd_launches:
+        avg = fwd_ms_k / fwd_launches
+        kernels["tc_fwd_step"]["achieved_tflops"] = fwd_launch_flops / (avg / 1e3) / 1e12
+    gpu_launches = sum(n for _, n in prof.values())
+
+    # ---- end to end through the public API with host buffers
+    e2e = None
+    if not args.no_e2e:
+        hq, hk, hv, hdo = (t.pin_memory() for t in (x.q, x.k, x.v, x.dout))
+        host_out = None
+        res = cp.attention_host(hq, hk, hv, hdo, cu, P, N, scale, device=dev)
+        host_out = list(res)
+        n_e2e = max(1, min(args.steps, 3))
+        barrier()
+        t0 = time.perf_counter()
+        for _ in range(n_e2e):
+            cp.attention_host(hq, hk, hv, hdo, cu, P, N, scale, device=dev, host_out=host_out)
+        barrier()
+        e2e_s = (time.perf_counter() - t0) / n_e2e
+        h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hdo))
+        d2h = sum(t.numel() * t.element_size() for t in host_out)
+        e2e = {"value": world * total / e2e_s / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "ms_per_step": e2e_s * 1e3}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": w.name, "text_len": W.text_lengths(w), "prefix_len": N,
+                       "P": P, "heads": H, "head_dim": d, "n_seqs": w.n_seqs,
+                       "parallelism": "replicas" if world > 1 else "single",
+                       "l2": "inputs larger than L2 (no flush)"},
+            "pct_of_bf16_peak": 100.0 * (value / world) / peak_sus,
+            "fwd_tflops": world * f_flops / (fwd_ms / 1e3) / 1e12, "fwd_ms": fwd_ms,
+            "bwd_tflops": world * 2.5 * f_flops / (bwd_ms / 1e3) / 1e12, "bwd_ms": bwd_ms,
+            "flops_per_step": total,
+            "roofline": roof,
+            "kernels": kernels,
+            "gpu_launches": gpu_launches,
+            "clocks": clk.summary(),
+            "e2e": e2e,
+        }
+        if not args.no_cpu_baseline and world == 1:
+            dt, fl, desc = oracle_sample(w, args.oracle_queries)
+            line["cpu_baseline"] = {"value": fl / dt / 1e12, "unit": "TFLOP/s",
+                                    "cores": os.cpu_count(), "kind": "oracle", "sample": desc,
+                                    "seconds": dt}
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="cuda", choices=["cuda", "reference"])
+    ap.add_argument("--workload", default="long", choices=sorted(W.WORKLOADS))
+    ap.add_argument("--oracle-queries", type=int, default=32768)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--traffic", type=float, default=None,
+                    help="DRAM bytes per launch of the dominant kernel from an ncu capture")
+    args = ap.parse_args()
+    w = W.get(args.workload)
+    if w.dtype != "bf16" or not w.backward:
+        raise SystemExit("bench workloads are the bf16 forward+backward ones")
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist_mod
+        backend = "nccl" if torch.cuda.is_available() and args.impl == "cuda" else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+        dist_mod.init_process_group(backend)
+        dist = dist_mod
+    try:
+        if args.impl == "reference":
+            return run_reference(args, w, rank, world)
+        return run_cuda(args, w, rank, world, dist)
+    finally:
+        if dist is not None:
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -133,6 +133,9 @@ cp_status_t cp_zigzag_scatter(const void* src, void* dst, size_t row_bytes, cons
  *   d          64 or 128
  *   out        [T][H][d], dtype dt (bf16 rounds to nearest even)
  *   lse        [H][T] fp32
+ *   out_lo     NULL, or (CP_BF16 only) [T][H][d] bf16: receives the rounding
+ *              remainder o - out of the fp32 result o, so that out + out_lo
+ *              carries o to about 16 bits.  Pass it to cp_attn_bwd.
  *   workspace  >= cp_attn_fwd_workspace_size(...) bytes, 256-byte aligned
  * Errors: CP_ERR_INVALID_ARG, CP_ERR_SHAPE, CP_ERR_DTYPE, CP_ERR_ALIGNMENT,
  * CP_ERR_WORKSPACE, CP_ERR_CUDA, CP_ERR_UNSUPPORTED (CP_BF16 on a device
@@ -144,7 +147,7 @@ size_t cp_attn_fwd_workspace_size(cp_dtype_t dt, int T, int H, int d,
 cp_status_t cp_attn_fwd(const void* q, const void* k, const void* v, cp_dtype_t dt, int T,
                         int H, int d, const int32_t* cu_seqlens_h, int n_seqs, int P,
                         int prefix_len, float softmax_scale, void* out, float* lse,
-                        void* workspace, size_t ws_bytes, void* stream);
+                        void* out_lo, void* workspace, size_t ws_bytes, void* stream);
 
 /*
  * cp_lse_merge -- merge n_parts partial attention results over disjoint key
@@ -173,6 +176,10 @@ cp_status_t cp_lse_merge(int n_parts, const float* part_out, const float* part_l
  * the page's AllReduce.
  *
  *   q, k, v, out, dout  [T][H][d], dtype dt;  lse [H][T] fp32 (from cp_attn_fwd)
+ *   out_lo              NULL, or the remainder written by cp_attn_fwd: then
+ *                       D_i = dO_i . (out_i + out_lo_i), which keeps the bf16
+ *                       rounding of the stored output out of dQ and dK (it
+ *                       matters when |dQ| is large, e.g. softmax scale 1)
  *   dq, dk, dv          [T][H][d] fp32 outputs (overwritten)
  *   prefix_grad_per_rank  NULL, or [2][P+1][n_seqs*prefix_len][H][d] fp32:
  *                       receives the per-rank prefix dK (slot 0) and dV
@@ -184,7 +191,8 @@ size_t cp_attn_bwd_workspace_size(cp_dtype_t dt, int T, int H, int d,
                                   const int32_t* cu_seqlens_h, int n_seqs, int P,
                                   int prefix_len);
 cp_status_t cp_attn_bwd(const void* q, const void* k, const void* v, const void* out,
-                        const float* lse, const void* dout, cp_dtype_t dt, int T, int H, int d,
+                        const void* out_lo, const float* lse, const void* dout, cp_dtype_t dt,
+                        int T, int H, int d,
                         const int32_t* cu_seqlens_h, int n_seqs, int P, int prefix_len,
                         float softmax_scale, float* dq, float* dk, float* dv,
                         float* prefix_grad_per_rank, void* workspace, size_t ws_bytes,
@@ -207,6 +215,20 @@ cp_status_t cp_workspace_status(const void* workspace, void* stream);
 cp_status_t cp_plan_pairs(const int32_t* cu_seqlens_h, int n_seqs, int prefix_len, int P,
                           int64_t* fwd_pairs, int64_t* bwd_pairs, int64_t* fwd_items,
                           int64_t* bwd_items);
+
+/*
+ * cp_profile_begin / cp_profile_end -- instrumentation: between the two calls
+ * the library records a pair of CUDA events on the launching stream around
+ * every kernel it launches (any thread).  cp_profile_end synchronises those
+ * events and returns, per kernel kind, the summed milliseconds and the launch
+ * count in ms[8] / launches[8] (either may be NULL):
+ *   0 zigzag index   1 zigzag gather   2 tensor-core forward ring step
+ *   3 backward preprocess   4 tensor-core backward ring step
+ *   5 prefix-gradient sum   6 CUDA-core forward step   7 CUDA-core backward step
+ * Errors: CP_ERR_CUDA.
+ */
+void cp_profile_begin(void);
+cp_status_t cp_profile_end(double* ms, int64_t* launches);
 
 /*
  * cp_set_wait_limit -- bound, in polling rounds, for every device-side wait of

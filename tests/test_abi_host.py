@@ -110,22 +110,16 @@ def test_bad_arguments_return_status(cplib):
     # d not in {64,128}, wrong dtype, null tensors, misaligned pointers
     cu8 = B.cu_array([0, 8])
     fake = ctypes.c_void_p(1 << 20)
-    st = L.cp_attn_fwd(fake, fake, fake, 1, 8, 1, 96, cu8, 1, 2, 0, 1.0, fake, fake, fake, 1 << 20,
-                       None)
-    assert st == 2
-    st = L.cp_attn_fwd(fake, fake, fake, 7, 8, 1, 64, cu8, 1, 2, 0, 1.0, fake, fake, fake, 1 << 20,
-                       None)
-    assert st == 3
-    st = L.cp_attn_fwd(None, fake, fake, 1, 8, 1, 64, cu8, 1, 2, 0, 1.0, fake, fake, fake, 1 << 20,
-                       None)
-    assert st == 1
+    def fwd(q, dt, T, d, lo=None):
+        return L.cp_attn_fwd(q, fake, fake, dt, T, 1, d, cu8, 1, 2, 0, 1.0, fake, fake, lo, fake,
+                             1 << 20, None)
+    assert fwd(fake, 1, 8, 96) == 2                                        # d not in {64, 128}
+    assert fwd(fake, 7, 8, 64) == 3                                        # dtype
+    assert fwd(None, 1, 8, 64) == 1                                        # null tensor
     odd = ctypes.c_void_p((1 << 20) + 4)
-    st = L.cp_attn_fwd(odd, fake, fake, 1, 8, 1, 64, cu8, 1, 2, 0, 1.0, fake, fake, fake, 1 << 20,
-                       None)
-    assert st == 4
-    st = L.cp_attn_fwd(fake, fake, fake, 1, 9, 1, 64, cu8, 1, 2, 0, 1.0, fake, fake, fake, 1 << 20,
-                       None)
-    assert st == 2                                                         # T != cu[-1]
+    assert fwd(odd, 1, 8, 64) == 4                                         # misaligned
+    assert fwd(fake, 1, 9, 64) == 2                                        # T != cu[-1]
+    assert fwd(fake, 0, 8, 64, lo=fake) == 3                               # out_lo with fp32
     L.cp_zigzag_index(cu, 1, 0, 2, None, None, 0, None)
     assert b"not divisible" in L.cp_last_error()
     assert L.cp_status_string(7) == b"CP_ERR_TIMEOUT"

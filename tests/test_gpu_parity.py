@@ -45,11 +45,13 @@ def _inputs(cu, H, d, dtype, seed, dout=True, q_mul=1.0):
 
 def _run(cp, q, k, v, do, cu, P, N, scale, per_rank=False):
     qd, kd, vd = (x.to(DEV) for x in (q, k, v))
-    out, lse = cp.cp_attn_fwd(qd, kd, vd, cu, P, N, scale)
+    keep = do is not None and q.dtype == torch.bfloat16
+    r = cp.cp_attn_fwd(qd, kd, vd, cu, P, N, scale, residual=keep)
+    out, lse = r[0], r[1]
     res = {"out": out, "lse": lse}
     if do is not None:
         g = cp.cp_attn_bwd(qd, kd, vd, out, lse, do.to(DEV), cu, P, N, scale,
-                           per_rank_prefix=per_rank)
+                           per_rank_prefix=per_rank, out_lo=r[2] if keep else None)
         res.update(dq=g[0], dk=g[1], dv=g[2])
         if per_rank:
             res["pgrad"] = g[3]
@@ -231,11 +233,15 @@ def test_bf16_long_workload_sampled(cp):
     k_t = torch.as_tensor(keys)
     assert_close("dk keys", got["dk"][k_t][:, heads], dk_ref, "bf16")
     assert_close("dv keys", got["dv"][k_t][:, heads], dv_ref, "bf16")
+    # The identities hold exactly; in finite precision the residual over all
+    # 131072 keys of a sum of independent per-key errors is ||e|| ~ sqrt(n)
+    # sigma_e against ||dK|| ~ sqrt(n) sigma_dK, i.e. the per-key relative
+    # error, which the bf16 bound caps at BF16_REL.
     sum_dv = got["dv"].double().sum(0)
     sum_do = x.dout.double().sum(0)
-    assert rel_l2(sum_dv, sum_do) < 1e-3
+    assert rel_l2(sum_dv, sum_do) < BF16_REL
     sum_dk = got["dk"].double().sum(0)
-    assert float(sum_dk.norm() / got["dk"].double().norm()) < 1e-3
+    assert float(sum_dk.norm() / got["dk"].double().norm()) < BF16_REL
 
 
 # ---------------------------------------------------------------------------
@@ -259,7 +265,7 @@ def test_device_error_paths(cp):
     st = B.lib().cp_attn_fwd(ctypes.c_void_p(qd.data_ptr()), ctypes.c_void_p(kd.data_ptr()),
                              ctypes.c_void_p(vd.data_ptr()), 1, 256, 1, 64, B.cu_array(cu), 1, 2,
                              0, 0.125, ctypes.c_void_p(out.data_ptr()),
-                             ctypes.c_void_p(lse.data_ptr()), ctypes.c_void_p(tiny_ws.ptr()),
+                             ctypes.c_void_p(lse.data_ptr()), None, ctypes.c_void_p(tiny_ws.ptr()),
                              tiny_ws.nbytes(), None)
     assert st == 5
     with pytest.raises(cp.CpError) as e:

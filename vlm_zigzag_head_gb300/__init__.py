@@ -24,7 +24,8 @@ from ._binding import CP_BF16, CP_F32, CpError  # noqa: F401
 
 __all__ = ["cp_zigzag_index", "cp_zigzag_gather", "cp_zigzag_scatter", "cp_attn_fwd",
            "cp_lse_merge", "cp_attn_bwd", "cp_workspace_status", "cp_set_wait_limit",
-           "cp_plan_pairs", "Workspace", "attention_host", "CpError"]
+           "cp_plan_pairs", "cp_profile_begin", "cp_profile_end", "Workspace",
+           "attention_host", "CpError"]
 
 
 def _dt(t: torch.Tensor) -> int:
@@ -127,28 +128,35 @@ def cp_zigzag_scatter(src: torch.Tensor, idx: torch.Tensor, out: torch.Tensor):
 
 
 def cp_attn_fwd(q, k, v, cu_seqlens, P: int, prefix_len: int, softmax_scale: float,
-                out=None, lse=None, workspace: Optional[Workspace] = None):
+                out=None, lse=None, workspace: Optional[Workspace] = None,
+                residual: bool = False, out_lo=None):
     """Context-parallel causal attention forward; returns ``(out, lse)`` with
-    out ``[T,H,d]`` (q's dtype) and lse ``[H,T]`` fp32 (natural log)."""
-    _need_cuda(q, k, v, out, lse)
+    out ``[T,H,d]`` (q's dtype) and lse ``[H,T]`` fp32 (natural log).  With
+    ``residual=True`` (bf16 only) it returns ``(out, lse, out_lo)``, where
+    out_lo holds the bf16 rounding remainder of out, for :func:`cp_attn_bwd`."""
+    _need_cuda(q, k, v, out, lse, out_lo)
     T, H, d = q.shape
     dt = _dt(q)
     if out is None:
         out = torch.empty_like(q)
     if lse is None:
         lse = torch.empty((H, T), dtype=torch.float32, device=q.device)
+    if residual and out_lo is None and dt == CP_BF16:
+        out_lo = torch.empty_like(q)
     cu = _b.cu_array(cu_seqlens)
     n = len(cu_seqlens) - 1
     L = _b.lib()
     nbytes = L.cp_attn_fwd_workspace_size(dt, T, H, d, cu, n, P, prefix_len)
     if nbytes == 0:  # invalid arguments: let the library name the problem
         _b.check(L.cp_attn_fwd(_ptr(q), _ptr(k), _ptr(v), dt, T, H, d, cu, n, P, prefix_len,
-                               float(softmax_scale), _ptr(out), _ptr(lse), None, 0,
+                               float(softmax_scale), _ptr(out), _ptr(lse), _ptr(out_lo), None, 0,
                                _stream(q.device)))
     ws = _ws(workspace, q.device, nbytes, "fwd")
     _b.check(L.cp_attn_fwd(_ptr(q), _ptr(k), _ptr(v), dt, T, H, d, cu, n, P, prefix_len,
-                           float(softmax_scale), _ptr(out), _ptr(lse), ctypes.c_void_p(ws.ptr()),
-                           ws.nbytes(), _stream(q.device)))
+                           float(softmax_scale), _ptr(out), _ptr(lse), _ptr(out_lo),
+                           ctypes.c_void_p(ws.ptr()), ws.nbytes(), _stream(q.device)))
+    if residual:
+        return out, lse, out_lo
     return out, lse
 
 
@@ -166,11 +174,12 @@ def cp_lse_merge(part_out: torch.Tensor, part_lse: torch.Tensor, out_dtype=torch
 
 def cp_attn_bwd(q, k, v, out, lse, dout, cu_seqlens, P: int, prefix_len: int,
                 softmax_scale: float, per_rank_prefix: bool = False,
-                workspace: Optional[Workspace] = None, grads=None):
+                workspace: Optional[Workspace] = None, grads=None, out_lo=None):
     """Backward; returns ``(dq, dk, dv)`` fp32 ``[T,H,d]`` and, with
     ``per_rank_prefix``, the per-rank prefix gradients
-    ``[2, P+1, n*prefix_len, H, d]`` (slot P: prefix queries' own term)."""
-    _need_cuda(q, k, v, out, lse, dout)
+    ``[2, P+1, n*prefix_len, H, d]`` (slot P: prefix queries' own term).
+    ``out_lo``: the remainder returned by ``cp_attn_fwd(..., residual=True)``."""
+    _need_cuda(q, k, v, out, lse, dout, out_lo)
     T, H, d = q.shape
     dt = _dt(q)
     if grads is None:
@@ -186,14 +195,15 @@ def cp_attn_bwd(q, k, v, out, lse, dout, cu_seqlens, P: int, prefix_len: int,
     L = _b.lib()
     nbytes = L.cp_attn_bwd_workspace_size(dt, T, H, d, cu, n, P, prefix_len)
     if nbytes == 0:  # invalid arguments: let the library name the problem
-        _b.check(L.cp_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout), dt,
-                               T, H, d, cu, n, P, prefix_len, float(softmax_scale), _ptr(dq),
-                               _ptr(dk), _ptr(dv), _ptr(pgrad), None, 0, _stream(q.device)))
+        _b.check(L.cp_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(out_lo), _ptr(lse),
+                               _ptr(dout), dt, T, H, d, cu, n, P, prefix_len,
+                               float(softmax_scale), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(pgrad),
+                               None, 0, _stream(q.device)))
     ws = _ws(workspace, q.device, nbytes, "bwd")
-    _b.check(L.cp_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout), dt, T, H,
-                           d, cu, n, P, prefix_len, float(softmax_scale), _ptr(dq), _ptr(dk),
-                           _ptr(dv), _ptr(pgrad), ctypes.c_void_p(ws.ptr()), ws.nbytes(),
-                           _stream(q.device)))
+    _b.check(L.cp_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(out_lo), _ptr(lse),
+                           _ptr(dout), dt, T, H, d, cu, n, P, prefix_len, float(softmax_scale),
+                           _ptr(dq), _ptr(dk), _ptr(dv), _ptr(pgrad), ctypes.c_void_p(ws.ptr()),
+                           ws.nbytes(), _stream(q.device)))
     if per_rank_prefix:
         return dq, dk, dv, pgrad
     return dq, dk, dv
@@ -214,6 +224,23 @@ def cp_set_wait_limit(rounds: int):
     _b.lib().cp_set_wait_limit(int(rounds))
 
 
+PROFILE_KINDS = ("zigzag_index", "zigzag_gather", "tc_fwd_step", "bwd_preprocess",
+                 "tc_bwd_step", "prefix_reduce", "simt_fwd_step", "simt_bwd_step")
+
+
+def cp_profile_begin():
+    """Start recording CUDA events around every kernel the library launches."""
+    _b.lib().cp_profile_begin()
+
+
+def cp_profile_end():
+    """Stop recording; returns {kind: (total_ms, launches)}."""
+    ms = (ctypes.c_double * 8)()
+    n = (ctypes.c_int64 * 8)()
+    _b.check(_b.lib().cp_profile_end(ms, n))
+    return {k: (float(ms[i]), int(n[i])) for i, k in enumerate(PROFILE_KINDS)}
+
+
 def cp_plan_pairs(cu_seqlens, prefix_len: int, P: int):
     """Host-only: visible pairs and items per ring step of both work lists."""
     arrs = [(ctypes.c_int64 * P)() for _ in range(4)]
@@ -229,12 +256,14 @@ def attention_host(q, k, v, dout, cu_seqlens, P: int, prefix_len: int, softmax_s
     copy results back.  Returns host tensors ``(out, lse[, dq, dk, dv])``."""
     dev = torch.device(device)
     qd, kd, vd = (x.to(dev, non_blocking=True) for x in (q, k, v))
-    out, lse = cp_attn_fwd(qd, kd, vd, cu_seqlens, P, prefix_len, softmax_scale)
+    keep = dout is not None and qd.dtype == torch.bfloat16
+    r = cp_attn_fwd(qd, kd, vd, cu_seqlens, P, prefix_len, softmax_scale, residual=keep)
+    out, lse = r[0], r[1]
     res = [out, lse]
     if dout is not None:
         dod = dout.to(dev, non_blocking=True)
         res += list(cp_attn_bwd(qd, kd, vd, out, lse, dod, cu_seqlens, P, prefix_len,
-                                softmax_scale))
+                                softmax_scale, out_lo=r[2] if keep else None))
     if host_out is None:
         host_out = [torch.empty(r.shape, dtype=r.dtype, pin_memory=True) for r in res]
     for h, r in zip(host_out, res):

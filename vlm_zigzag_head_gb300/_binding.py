@@ -36,13 +36,15 @@ SIGNATURES = {
                                                      ctypes.c_int, ctypes.c_int]),
     "cp_attn_fwd": (ctypes.c_int, [c_vp, c_vp, c_vp, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                    ctypes.c_int, c_i32p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
-                                   ctypes.c_float, c_vp, c_vp, c_vp, ctypes.c_size_t, c_vp]),
+                                   ctypes.c_float, c_vp, c_vp, c_vp, c_vp, ctypes.c_size_t,
+                                   c_vp]),
     "cp_lse_merge": (ctypes.c_int, [ctypes.c_int, c_vp, c_vp, ctypes.c_int, ctypes.c_int,
                                     ctypes.c_int, c_vp, ctypes.c_int, c_vp, c_vp]),
     "cp_attn_bwd_workspace_size": (ctypes.c_size_t, [ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                                      ctypes.c_int, c_i32p, ctypes.c_int,
                                                      ctypes.c_int, ctypes.c_int]),
-    "cp_attn_bwd": (ctypes.c_int, [c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, ctypes.c_int, ctypes.c_int,
+    "cp_attn_bwd": (ctypes.c_int, [c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, ctypes.c_int,
+                                   ctypes.c_int,
                                    ctypes.c_int, ctypes.c_int, c_i32p, ctypes.c_int, ctypes.c_int,
                                    ctypes.c_int, ctypes.c_float, c_vp, c_vp, c_vp, c_vp, c_vp,
                                    ctypes.c_size_t, c_vp]),
@@ -50,6 +52,8 @@ SIGNATURES = {
     "cp_plan_pairs": (ctypes.c_int, [c_i32p, ctypes.c_int, ctypes.c_int, ctypes.c_int, c_i64p,
                                      c_i64p, c_i64p, c_i64p]),
     "cp_set_wait_limit": (None, [ctypes.c_longlong]),
+    "cp_profile_begin": (None, []),
+    "cp_profile_end": (ctypes.c_int, [ctypes.POINTER(ctypes.c_double), c_i64p]),
 }
 
 

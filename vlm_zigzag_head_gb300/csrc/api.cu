@@ -189,6 +189,8 @@ struct BwdWs {
   size_t status = 0, items = 0, qitems = 0, cu = 0, D = 0, lse2 = 0, slots = 0, total = 0;
 };
 
+inline int64_t ld_pitch(int64_t T) { return (T + 3) / 4 * 4; }
+
 BwdWs bwd_layout(const PlanSet& ps, int H, int d, bool simt, bool own_slots) {
   BwdWs w;
   const Problem& pb = ps.pb;
@@ -198,8 +200,10 @@ BwdWs bwd_layout(const PlanSet& ps, int H, int d, bool simt, bool own_slots) {
   w.qitems = o;
   if (simt) o = align_up(o + ps.fwd_nat.items.size() * sizeof(FwdItem), 256);
   w.cu = o; o = align_up(o + pb.cu.size() * sizeof(int32_t), 256);
-  w.D = o; o = align_up(o + (size_t)pb.T * H * sizeof(float), 256);
-  w.lse2 = o; o = align_up(o + (size_t)pb.T * H * sizeof(float), 256);
+  // lse2 and D planes [2][H][pitch], pitch = T rounded up to 4 (16-byte rows for TMA)
+  w.lse2 = o;
+  w.D = o + (size_t)ld_pitch(pb.T) * H * sizeof(float);  // plane 1 directly after plane 0
+  o = align_up(o + 2 * (size_t)ld_pitch(pb.T) * H * sizeof(float), 256);
   w.slots = o;
   if (own_slots)
     o = align_up(o + 2ull * (pb.P + 1) * pb.n_seqs * pb.N * H * d * sizeof(float), 256);
@@ -244,6 +248,39 @@ long long wait_limit() {
   long long w = g_wait_limit.load();
   return w > 0 ? w : (1LL << 22);
 }
+
+// ---------------------------------------------------------------------------
+// optional per-launch timing: CUDA events recorded on the launching stream
+// around every kernel of the path while profiling is on
+// ---------------------------------------------------------------------------
+constexpr int kProfKinds = 8;
+struct ProfRec {
+  int kind;
+  cudaEvent_t a, b;
+};
+std::mutex g_prof_mu;
+std::atomic<bool> g_prof_on{false};
+std::vector<ProfRec> g_prof;
+
+struct ProfScope {
+  int kind;
+  cudaStream_t st;
+  cudaEvent_t a = nullptr, b = nullptr;
+  ProfScope(int k, cudaStream_t s) : kind(k), st(s) {
+    if (!g_prof_on.load()) return;
+    if (cudaEventCreate(&a) != cudaSuccess || cudaEventCreate(&b) != cudaSuccess) {
+      a = b = nullptr;
+      return;
+    }
+    cudaEventRecord(a, st);
+  }
+  ~ProfScope() {
+    if (!a) return;
+    cudaEventRecord(b, st);
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    g_prof.push_back({kind, a, b});
+  }
+};
 
 }  // namespace
 
@@ -335,10 +372,13 @@ size_t cp_attn_fwd_workspace_size(cp_dtype_t dt, int T, int H, int d, const int3
 
 cp_status_t cp_attn_fwd(const void* q, const void* k, const void* v, cp_dtype_t dt, int T, int H,
                         int d, const int32_t* cu, int n_seqs, int P, int N, float scale,
-                        void* out, float* lse, void* ws, size_t ws_bytes, void* stream) {
+                        void* out, float* lse, void* out_lo, void* ws, size_t ws_bytes,
+                        void* stream) {
   const void* ptrs[5] = {q, k, v, out, lse};
   cp_status_t s = check_common(ptrs, 5, dt, T, H, d, cu, n_seqs, P, N, scale);
   if (s != CP_OK) return s;
+  if (out_lo && dt != CP_BF16) return fail(CP_ERR_DTYPE, "out_lo is for bf16 outputs only");
+  if (out_lo && !aligned16(out_lo)) return fail(CP_ERR_ALIGNMENT, "out_lo alignment");
   std::shared_ptr<PlanSet> ps;
   s = get_plans(cu, n_seqs, N, P, T, H, d, &ps);
   if (s != CP_OK) return s;
@@ -363,13 +403,20 @@ cp_status_t cp_attn_fwd(const void* q, const void* k, const void* v, cp_dtype_t 
           "upload sample table");
   int32_t* idx = reinterpret_cast<int32_t*>(w + L.idx);
   // get_batch_on_this_cp_rank: zigzag table, then index_select of q, k, v text rows
-  CP_CUDA(launch_zigzag_index(reinterpret_cast<const int32_t*>(w + L.samples), n_seqs, P, pb.R,
-                              idx, nullptr, st),
-          "zigzag index kernel");
+  {
+    ProfScope ps_(0, st);
+    CP_CUDA(launch_zigzag_index(reinterpret_cast<const int32_t*>(w + L.samples), n_seqs, P, pb.R,
+                                idx, nullptr, st),
+            "zigzag index kernel");
+  }
   const void* src[3] = {q, k, v};
   void* dst[3] = {w + L.qkv[0], w + L.qkv[1], w + L.qkv[2]};
-  CP_CUDA(launch_gather_rows(src, dst, 3, (size_t)H * d * elem, idx, (int)pb.text_rows, false, st),
-          "zigzag gather");
+  {
+    ProfScope ps_(1, st);
+    CP_CUDA(launch_gather_rows(src, dst, 3, (size_t)H * d * elem, idx, (int)pb.text_rows, false,
+                               st),
+            "zigzag gather");
+  }
   const FwdItem* items = reinterpret_cast<const FwdItem*>(w + L.items);
   float* o_run = reinterpret_cast<float*>(w + L.o_run);
   float* lse_run = reinterpret_cast<float*>(w + L.lse_run);
@@ -387,12 +434,13 @@ cp_status_t cp_attn_fwd(const void* q, const void* k, const void* v, cp_dtype_t 
     a.H = H; a.d = d;
     a.scale_log2 = scale * 1.4426950408889634f;
     a.o_run = o_run; a.lse_run = lse_run; a.run_rows = PR;
-    a.out = out; a.lse = lse; a.T = T;
+    a.out = out; a.lse = lse; a.T = T; a.out_lo = out_lo;
     a.status = reinterpret_cast<int32_t*>(w + L.status);
     a.wait_limit = wait_limit();
     for (int step = 0; step < P; ++step) {
       a.items = items + ps->fwd.step_begin[step];
       a.n_items = ps->fwd.step_begin[step + 1] - ps->fwd.step_begin[step];
+      ProfScope ps_(2, st);
       CP_CUDA(launch_tc_fwd(a, st), "tensor-core ring step");
     }
     return CP_OK;
@@ -406,6 +454,7 @@ cp_status_t cp_attn_fwd(const void* q, const void* k, const void* v, cp_dtype_t 
   for (int step = 0; step < P; ++step) {
     a.items = items + ps->fwd.step_begin[step];
     a.n_items = ps->fwd.step_begin[step + 1] - ps->fwd.step_begin[step];
+    ProfScope ps_(6, st);
     CP_CUDA(launch_simt_fwd(a, bf16, st), "ring step");
   }
   return CP_OK;
@@ -438,7 +487,8 @@ size_t cp_attn_bwd_workspace_size(cp_dtype_t dt, int T, int H, int d, const int3
 }
 
 cp_status_t cp_attn_bwd(const void* q, const void* k, const void* v, const void* out,
-                        const float* lse, const void* dout, cp_dtype_t dt, int T, int H, int d,
+                        const void* out_lo, const float* lse, const void* dout, cp_dtype_t dt,
+                        int T, int H, int d,
                         const int32_t* cu, int n_seqs, int P, int N, float scale, float* dq,
                         float* dk, float* dv, float* pgrad, void* ws, size_t ws_bytes,
                         void* stream) {
@@ -446,6 +496,8 @@ cp_status_t cp_attn_bwd(const void* q, const void* k, const void* v, const void*
   cp_status_t s = check_common(ptrs, 9, dt, T, H, d, cu, n_seqs, P, N, scale);
   if (s != CP_OK) return s;
   if (pgrad && !aligned16(pgrad)) return fail(CP_ERR_ALIGNMENT, "prefix_grad_per_rank alignment");
+  if (out_lo && dt != CP_BF16) return fail(CP_ERR_DTYPE, "out_lo is for bf16 outputs only");
+  if (out_lo && !aligned16(out_lo)) return fail(CP_ERR_ALIGNMENT, "out_lo alignment");
   std::shared_ptr<PlanSet> ps;
   s = get_plans(cu, n_seqs, N, P, T, H, d, &ps);
   if (s != CP_OK) return s;
@@ -473,7 +525,12 @@ cp_status_t cp_attn_bwd(const void* q, const void* k, const void* v, const void*
                           ps->bwd.items.size() * sizeof(BwdItem), st),
           "upload work list");
   CP_CUDA(stager().upload(w + L.cu, pb.cu.data(), pb.cu.size() * 4, st), "upload cu_seqlens");
-  CP_CUDA(launch_bwd_preprocess(out, dout, bf16, lse, T, H, d, Dd, lse2, st), "bwd preprocess");
+  const int64_t pitch = ld_pitch(T);
+  {
+    ProfScope ps_(3, st);
+    CP_CUDA(launch_bwd_preprocess(out, out_lo, dout, bf16, lse, T, H, d, Dd, lse2, pitch, st),
+            "bwd preprocess");
+  }
   const BwdItem* items = reinterpret_cast<const BwdItem*>(w + L.items);
   if (tc) {
     CP_CUDA(cudaMemsetAsync(dq, 0, (size_t)T * H * d * sizeof(float), st), "clear dq");
@@ -482,10 +539,11 @@ cp_status_t cp_attn_bwd(const void* q, const void* k, const void* v, const void*
     bool ok = make_tmap_thd(&a.tm_q, q, T, H, d, kBwdTileQ, &terr) &&
               make_tmap_thd(&a.tm_k, k, T, H, d, kBwdTileK, &terr) &&
               make_tmap_thd(&a.tm_v, v, T, H, d, kBwdTileK, &terr) &&
-              make_tmap_thd(&a.tm_do, dout, T, H, d, kBwdTileQ, &terr);
+              make_tmap_thd(&a.tm_do, dout, T, H, d, kBwdTileQ, &terr) &&
+              make_tmap_ld(&a.tm_ld, lse2, pitch, H, kBwdTileQ + 4, &terr);
     if (!ok) return fail(CP_ERR_CUDA, std::string("tensor map: ") + (terr ? terr : "?"));
     a.H = H; a.d = d; a.scale = scale; a.scale_log2 = scale * 1.4426950408889634f;
-    a.D = Dd; a.lse2 = lse2; a.T = T;
+    a.T = T;
     a.dq = dq; a.dk = dk; a.dv = dv;
     a.pre_k = pre_k; a.pre_v = pre_v; a.pre_rows = pre_rows;
     a.status = reinterpret_cast<int32_t*>(w + L.status);
@@ -493,6 +551,7 @@ cp_status_t cp_attn_bwd(const void* q, const void* k, const void* v, const void*
     for (int step = 0; step < P; ++step) {
       a.items = items + ps->bwd.step_begin[step];
       a.n_items = ps->bwd.step_begin[step + 1] - ps->bwd.step_begin[step];
+      ProfScope ps_(4, st);
       CP_CUDA(launch_tc_bwd(a, st), "tensor-core backward ring step");
     }
   } else {
@@ -501,7 +560,7 @@ cp_status_t cp_attn_bwd(const void* q, const void* k, const void* v, const void*
             "upload dq work list");
     const FwdItem* qitems = reinterpret_cast<const FwdItem*>(w + L.qitems);
     SimtBwdArgs a;
-    a.q = q; a.k = k; a.v = v; a.dout = dout; a.D = Dd; a.lse2 = lse2;
+    a.q = q; a.k = k; a.v = v; a.dout = dout; a.D = Dd; a.lse2 = lse2; a.pitch = pitch;
     a.H = H; a.d = d; a.scale = scale; a.T = T;
     a.dq = dq; a.dk = dk; a.dv = dv; a.pre_k = pre_k; a.pre_v = pre_v; a.pre_rows = pre_rows;
     for (int step = 0; step < P; ++step) {
@@ -509,12 +568,14 @@ cp_status_t cp_attn_bwd(const void* q, const void* k, const void* v, const void*
       a.n_q_items = ps->fwd_nat.step_begin[step + 1] - ps->fwd_nat.step_begin[step];
       a.k_items = items + ps->bwd.step_begin[step];
       a.n_k_items = ps->bwd.step_begin[step + 1] - ps->bwd.step_begin[step];
+      ProfScope ps_(7, st);
       CP_CUDA(launch_simt_bwd_dq(a, bf16, st), "backward dq step");
       CP_CUDA(launch_simt_bwd_dkdv(a, bf16, st), "backward dk/dv step");
     }
   }
   if (N > 0) {
     // the AllReduce of the replicated prefix gradient: fixed-order sum of slots
+    ProfScope ps_(5, st);
     CP_CUDA(launch_prefix_reduce(pre_k, pre_v, P + 1, reinterpret_cast<const int32_t*>(w + L.cu),
                                  n_seqs, N, H, d, dk, dv, st),
             "prefix gradient sum");
@@ -533,6 +594,40 @@ cp_status_t cp_workspace_status(const void* ws, void* stream) {
     return fail(CP_ERR_TIMEOUT, buf);
   }
   return CP_OK;
+}
+
+void cp_profile_begin(void) {
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  for (auto& r : g_prof) {
+    cudaEventDestroy(r.a);
+    cudaEventDestroy(r.b);
+  }
+  g_prof.clear();
+  g_prof_on.store(true);
+}
+
+cp_status_t cp_profile_end(double* ms, int64_t* launches) {
+  g_prof_on.store(false);
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  for (int k = 0; k < kProfKinds; ++k) {
+    if (ms) ms[k] = 0.0;
+    if (launches) launches[k] = 0;
+  }
+  cp_status_t st = CP_OK;
+  for (auto& r : g_prof) {
+    float t = 0.f;
+    cudaError_t e = cudaEventSynchronize(r.b);
+    if (e == cudaSuccess) e = cudaEventElapsedTime(&t, r.a, r.b);
+    if (e != cudaSuccess) st = cuda_fail(e, "profile events");
+    if (r.kind >= 0 && r.kind < kProfKinds) {
+      if (ms) ms[r.kind] += t;
+      if (launches) launches[r.kind] += 1;
+    }
+    cudaEventDestroy(r.a);
+    cudaEventDestroy(r.b);
+  }
+  g_prof.clear();
+  return st;
 }
 
 cp_status_t cp_plan_pairs(const int32_t* cu, int n_seqs, int N, int P, int64_t* fwd_pairs,

@@ -171,8 +171,8 @@ __global__ void __launch_bounds__(kSimtQ) simt_bwd_dq_kernel(SimtBwdArgs a, int 
   }
   const bool valid = t < it.q_len;
   const long long qrow = it.q_row0 + t;
-  const float lse2 = valid ? a.lse2[(long long)h * a.T + qrow] : 0.f;
-  const float Dt = valid ? a.D[(long long)h * a.T + qrow] : 0.f;
+  const float lse2 = valid ? a.lse2[(long long)h * a.pitch + qrow] : 0.f;
+  const float Dt = valid ? a.D[(long long)h * a.pitch + qrow] : 0.f;
   float acc[D];
 #pragma unroll
   for (int e = 0; e < D; ++e) acc[e] = 0.f;
@@ -268,7 +268,7 @@ __global__ void __launch_bounds__(2 * kBwdTileK) simt_bwd_dkdv_kernel(SimtBwdArg
       }
       for (int x = tid; x < kSimtQT; x += 2 * kBwdTileK) {
         const bool in = t0 + x < s.len;
-        const long long g = (long long)h * a.T + s.row0 + t0 + x;
+        const long long g = (long long)h * a.pitch + s.row0 + t0 + x;
         Ls[x] = in ? a.lse2[g] : 0.f;
         Dsm[x] = in ? a.D[g] : 0.f;
       }

@@ -25,9 +25,11 @@ cudaError_t launch_zigzag_index(const int32_t* samples_dev /*[n][4]: t0, c, off,
                                 cudaStream_t st);
 cudaError_t launch_lse_merge(int n_parts, const float* part_out, const float* part_lse, int rows,
                              int H, int d, void* out, bool out_bf16, float* lse, cudaStream_t st);
-// D[h][t] = sum_e dO[t][h][e] * O[t][h][e];  lse2[h][t] = lse[h][t] * log2(e)
-cudaError_t launch_bwd_preprocess(const void* out, const void* dout, bool bf16, const float* lse,
-                                  int T, int H, int d, float* D, float* lse2, cudaStream_t st);
+// D[h*pitch + t] = sum_e dO[t][h][e] * O[t][h][e];  lse2[h*pitch + t] = lse[h][t] * log2(e)
+// (out_lo nullable, bf16 only: D uses out + out_lo)
+cudaError_t launch_bwd_preprocess(const void* out, const void* out_lo, const void* dout, bool bf16,
+                                  const float* lse, int T, int H, int d, float* D, float* lse2,
+                                  int64_t pitch, cudaStream_t st);
 // dk/dv prefix rows = sum over slots 0..P of the per-rank prefix gradients
 cudaError_t launch_prefix_reduce(const float* slots_k, const float* slots_v, int n_slots,
                                  const int32_t* cu_dev, int n_seqs, int N, int H, int d,
@@ -46,7 +48,7 @@ cudaError_t launch_simt_fwd(const SimtFwdArgs& a, bool bf16, cudaStream_t st);
 
 struct SimtBwdArgs {
   const void* q; const void* k; const void* v; const void* dout;  // natural order
-  const float* D; const float* lse2;                              // [H][T]
+  const float* D; const float* lse2; int64_t pitch;               // [H][pitch]
   int H, d; float scale; int64_t T;
   const FwdItem* q_items; int n_q_items;   // dQ pass (natural-order forward plan)
   const BwdItem* k_items; int n_k_items;   // dK/dV pass

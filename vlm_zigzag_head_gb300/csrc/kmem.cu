@@ -136,9 +136,11 @@ __device__ __forceinline__ float to_f<__nv_bfloat16>(__nv_bfloat16 x) { return _
 // One warp per (head, token): D = dO . O in fp32, plus the log2-domain lse.
 template <typename T>
 __global__ void __launch_bounds__(kThreads) bwd_pre_kernel(const T* __restrict__ o,
+                                                           const T* __restrict__ o_lo,
                                                            const T* __restrict__ dout,
                                                            const float* __restrict__ lse, int Tn,
-                                                           int H, int d, float* D, float* lse2) {
+                                                           int H, int d, float* D, float* lse2,
+                                                           long long pitch) {
   const int lane = threadIdx.x & 31;
   const long long pairs = (long long)Tn * H;
   for (long long w = (long long)blockIdx.x * (kThreads / 32) + threadIdx.x / 32; w < pairs;
@@ -147,12 +149,17 @@ __global__ void __launch_bounds__(kThreads) bwd_pre_kernel(const T* __restrict__
     const long long t = w - (long long)h * Tn;
     const long long base = (t * H + h) * (long long)d;
     float acc = 0.f;
-    for (int e = lane; e < d; e += 32) acc += to_f(o[base + e]) * to_f(dout[base + e]);
+    if (o_lo) {
+      for (int e = lane; e < d; e += 32)
+        acc += (to_f(o[base + e]) + to_f(o_lo[base + e])) * to_f(dout[base + e]);
+    } else {
+      for (int e = lane; e < d; e += 32) acc += to_f(o[base + e]) * to_f(dout[base + e]);
+    }
 #pragma unroll
     for (int sh = 16; sh > 0; sh >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, sh);
     if (lane == 0) {
-      D[(long long)h * Tn + t] = acc;
-      lse2[(long long)h * Tn + t] = lse[(long long)h * Tn + t] * 1.4426950408889634f;
+      D[(long long)h * pitch + t] = acc;
+      lse2[(long long)h * pitch + t] = lse[(long long)h * Tn + t] * 1.4426950408889634f;
     }
   }
 }
@@ -231,19 +238,21 @@ cudaError_t launch_lse_merge(int n_parts, const float* po, const float* pl, int 
   return cudaGetLastError();
 }
 
-cudaError_t launch_bwd_preprocess(const void* out, const void* dout, bool bf16, const float* lse,
-                                  int T, int H, int d, float* D, float* lse2, cudaStream_t st) {
+cudaError_t launch_bwd_preprocess(const void* out, const void* out_lo, const void* dout, bool bf16,
+                                  const float* lse, int T, int H, int d, float* D, float* lse2,
+                                  int64_t pitch, cudaStream_t st) {
   const long long pairs = (long long)T * H;
   if (pairs == 0) return cudaSuccess;
   const int g = grid_for(pairs, kThreads / 32);
   if (bf16)
     bwd_pre_kernel<__nv_bfloat16><<<g, kThreads, 0, st>>>(
-        static_cast<const __nv_bfloat16*>(out), static_cast<const __nv_bfloat16*>(dout), lse, T,
-        H, d, D, lse2);
+        static_cast<const __nv_bfloat16*>(out), static_cast<const __nv_bfloat16*>(out_lo),
+        static_cast<const __nv_bfloat16*>(dout), lse, T,
+        H, d, D, lse2, pitch);
   else
-    bwd_pre_kernel<float><<<g, kThreads, 0, st>>>(static_cast<const float*>(out),
+    bwd_pre_kernel<float><<<g, kThreads, 0, st>>>(static_cast<const float*>(out), nullptr,
                                                   static_cast<const float*>(dout), lse, T, H, d,
-                                                  D, lse2);
+                                                  D, lse2, pitch);
   return cudaGetLastError();
 }
 

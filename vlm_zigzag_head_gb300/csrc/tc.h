@@ -12,6 +12,10 @@ namespace cpattn {
 // 128-byte swizzle.  Returns false (and a message) if encoding fails.
 bool make_tmap_thd(CUtensorMap* map, const void* base, int64_t rows, int H, int d,
                    int rows_per_box, const char** err);
+// 3-D tensor map over the fp32 planes [2][H][pitch] (lse2, D) of the backward
+// preprocess, box {box_rows, 1, 2}; pitch must be a multiple of 4.
+bool make_tmap_ld(CUtensorMap* map, const void* base, int64_t pitch, int H, int box_rows,
+                  const char** err);
 
 struct TcFwdArgs {
   CUtensorMap tm_q_text, tm_k_text, tm_v_text;  // rank-local (gathered) text rows
@@ -21,6 +25,7 @@ struct TcFwdArgs {
   float scale_log2;           // softmax scale * log2(e)
   float* o_run; float* lse_run; int64_t run_rows;
   void* out; float* lse; int64_t T;
+  void* out_lo;               // nullable: bf16 remainder o - bf16(o)
   int32_t* status;            // DevStatus of the workspace
   long long wait_limit;
 };
@@ -28,10 +33,11 @@ cudaError_t launch_tc_fwd(const TcFwdArgs& a, cudaStream_t st);
 
 struct TcBwdArgs {
   CUtensorMap tm_q, tm_k, tm_v, tm_do;  // natural order
+  CUtensorMap tm_ld;                     // [2][H][pitch] fp32: lse2, D
   const BwdItem* items;
   int n_items, H, d;
   float scale, scale_log2;
-  const float* D; const float* lse2; int64_t T;  // [H][T]
+  int64_t T;
   float* dq; float* dk; float* dv;
   float* pre_k; float* pre_v; int64_t pre_rows;
   int32_t* status;

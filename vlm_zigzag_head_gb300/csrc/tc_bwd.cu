@@ -11,8 +11,14 @@
 //   dV  += P^T dO           dK  += dS^T Q                      (TMEM, whole item)
 //   dQ^T = K^T dS^T  -> fp32 atomic adds into dQ (scaled)
 //
-// Warp roles (384 threads):
-//   warp 0       TMA producer (K, V once; Q, dO, lse2, D per query tile)
+// dS^T enters the dQ product as two bf16 terms, hi = bf16(dS^T) and
+// lo = bf16(dS^T - hi), accumulated in fp32: with a softmax scale of 1 the
+// dQ values are large enough that one bf16 rounding of dS would dominate the
+// error.  dK and dV use the single bf16 rounding of dS^T and P^T.
+//
+// Warp roles (384 threads; TMEM lane quarter of warp w is w % 4):
+//   warp 0       TMA producer (K, V once; Q, dO and the lse2 / D rows per query
+//                tile, 3 stages)
 //   warp 1       TMEM allocation; lane 0 issues every tcgen05.mma
 //   warps 2, 3   idle
 //   warps 4..7   P / dS computation, then the dK / dV epilogue; thread = key row
@@ -36,7 +42,8 @@ constexpr int kThreads = 384;
 constexpr int kD = 128;            // head dim of this kernel
 constexpr int kBK = kBwdTileK;     // 128 keys
 constexpr int kBQ = kBwdTileQ;     // 64 queries per inner tile
-constexpr int kStages = 2;
+constexpr int kStages = 3;        // Q / dO / (lse2, D) stages
+constexpr int kLdRows = kBQ + 4;  // lse2 / D box: 64 rows plus alignment slack
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0, kColDP = 64, kColDQ0 = 128, kColDQ1 = 192, kColDK = 256,
                    kColDV = 384;
@@ -45,23 +52,27 @@ constexpr long long kDrainLimit = 1LL << 24;
 struct L {
   static constexpr int kKVBox = 128 * 128;   // 128 rows x 128 bytes
   static constexpr int kQBox = kBQ * 128;    // 64 rows x 128 bytes
+  static constexpr int kLdBytes = 2 * kLdRows * 4;
   static constexpr int kK = 0;
   static constexpr int kV = kK + 2 * kKVBox;
   static constexpr int kQ = kV + 2 * kKVBox;              // [stage][2 boxes]
   static constexpr int kDO = kQ + kStages * 2 * kQBox;
-  static constexpr int kP = kDO + kStages * 2 * kQBox;     // [buf] 128 x 64 bf16
-  static constexpr int kDS = kP + 2 * kKVBox;
-  static constexpr int kLse = kDS + 2 * kKVBox;           // [stage][64] lse2, [stage][64] D
-  static constexpr int kBars = kLse + kStages * 2 * kBQ * 4;
+  static constexpr int kP = kDO + kStages * 2 * kQBox;     // 128 x 64 bf16
+  static constexpr int kDS = kP + kKVBox;                 // bf16(dS^T)
+  static constexpr int kDSL = kDS + kKVBox;               // bf16(dS^T - bf16(dS^T))
+  static constexpr int kLd = kDSL + kKVBox;               // [stage] {lse2[68], D[68]}
+  static constexpr int kItem = kLd + kStages * 1024;
+  static constexpr int kBars = kItem + 128;
   static constexpr int kBytes = kBars + 512;
   static constexpr int kAlloc = kBytes + 1024;
 };
+static_assert(L::kAlloc <= 227 * 1024, "shared memory budget");
 
 struct Bars {
   uint64_t kv_full;
   uint64_t qdo_full[kStages], qdo_empty[kStages];
   uint64_t sdp_full, sdp_empty;
-  uint64_t ps_full[2], ps_empty[2];
+  uint64_t ps_full, ps_empty;
   uint64_t dq_full[2], dq_empty[2];
   uint64_t dkv_done;
   uint64_t drain;
@@ -78,6 +89,21 @@ __device__ __forceinline__ int run_qstart(const Seg& s) {
   return s.causal && s.delta < 0 ? -s.delta : 0;
 }
 
+// The g-th query tile of the item: its run, the run's first query and the
+// tile index inside the run.
+__device__ __forceinline__ void tile_of(const BwdItem& it, int g, Seg& sg, int& q0, int& t) {
+  for (int s = 0; s < it.nseg; ++s) {
+    const int nt = run_qtiles(it.seg[s]);
+    if (g < nt) {
+      sg = it.seg[s];
+      q0 = run_qstart(sg);
+      t = g;
+      return;
+    }
+    g -= nt;
+  }
+}
+
 __device__ __forceinline__ void record_timeout(int32_t* status, volatile int* abort, int site) {
   if (atomicCAS(&status[0], 0, 1) == 0) status[1] = site;
   *abort = 1;
@@ -88,11 +114,13 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   Bars* bars = reinterpret_cast<Bars*>(smem + L::kBars);
-  float* lse_s = reinterpret_cast<float*>(smem + L::kLse);  // [stage][2][64]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int item_idx = blockIdx.x % a.n_items;
   const int h = blockIdx.x / a.n_items;
-  const BwdItem& it = a.items[item_idx];
+  BwdItem& it = *reinterpret_cast<BwdItem*>(smem + L::kItem);
+  if (warp == 0)  // the work item, copied once into shared memory (128 bytes)
+    reinterpret_cast<uint32_t*>(&it)[lane] =
+        reinterpret_cast<const uint32_t*>(a.items + item_idx)[lane];
   volatile int* abort = &bars->abort;
   const long long lim = a.wait_limit;
 
@@ -104,9 +132,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
     }
     mbar_init(&bars->sdp_full, 1);
     mbar_init(&bars->sdp_empty, 4);
+    mbar_init(&bars->ps_full, 4);
+    mbar_init(&bars->ps_empty, 1);
     for (int b = 0; b < 2; ++b) {
-      mbar_init(&bars->ps_full[b], 4);
-      mbar_init(&bars->ps_empty[b], 1);
       mbar_init(&bars->dq_full[b], 1);
       mbar_init(&bars->dq_empty[b], 4);
     }
@@ -127,6 +155,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
   const int nseg = it.nseg;
   int n_qt = 0;
   for (int s = 0; s < nseg; ++s) n_qt += run_qtiles(it.seg[s]);
+  // Every role walks the query tiles in the same rotated order.  Concurrent
+  // CTAs are neighbouring key tiles of one head that meet the same queries;
+  // the rotation keeps their dQ atomics on different rows.
+  const int rot = n_qt > 0 ? (int)(((long long)item_idx * 17 + (long long)h * 7) % n_qt) : 0;
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
@@ -144,12 +176,12 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
     }
     // decisions are taken by lane 0 and broadcast: the warp never diverges
     // around the __syncwarp below
-    int j = 0;
     bool go = true;
-    for (int s = 0; go && s < nseg; ++s) {
-      const Seg sg = it.seg[s];
-      const int q0 = run_qstart(sg), nt = run_qtiles(sg);
-      for (int t = 0; t < nt; ++t, ++j) {
+    for (int j = 0; go && j < n_qt; ++j) {
+      {
+        Seg sg;
+        int q0, t;
+        tile_of(it, (j + rot) % n_qt, sg, q0, t);
         const int st = j % kStages;
         int w_ok = 1;
         if (lane == 0) {
@@ -159,25 +191,19 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
         }
         go = __shfl_sync(0xffffffffu, w_ok, 0) != 0;
         if (!go) break;
-        // lse2 / D of the tile's 64 queries; rows past the run get lse2 = +inf (P = 0)
+        // Q, dO (64 rows each) and the lse2 / D rows of the tile; the lse2 / D
+        // box starts at the row rounded down to 4 (16-byte TMA alignment)
         const int row0 = q0 + t * kBQ;
-        float* ls = lse_s + st * 2 * kBQ;
-#pragma unroll
-        for (int x = lane; x < kBQ; x += 32) {
-          const bool in = row0 + x < sg.len;
-          const long long g = (long long)h * a.T + sg.row0 + row0 + x;
-          ls[x] = in ? a.lse2[g] : INFINITY;
-          ls[kBQ + x] = in ? a.D[g] : 0.f;
-        }
-        __syncwarp();
+        const int grow = sg.row0 + row0;
         if (lane == 0) {
-          mbar_expect_tx(&bars->qdo_full[st], 4 * L::kQBox);
+          mbar_expect_tx(&bars->qdo_full[st], 4 * L::kQBox + L::kLdBytes);
           for (int b = 0; b < 2; ++b) {
             tma_load_3d(&a.tm_q, &bars->qdo_full[st], smem + L::kQ + (st * 2 + b) * L::kQBox,
-                        b * 64, h, sg.row0 + row0);
+                        b * 64, h, grow);
             tma_load_3d(&a.tm_do, &bars->qdo_full[st], smem + L::kDO + (st * 2 + b) * L::kQBox,
-                        b * 64, h, sg.row0 + row0);
+                        b * 64, h, grow);
           }
+          tma_load_3d(&a.tm_ld, &bars->qdo_full[st], smem + L::kLd + st * 1024, grow & ~3, h, 0);
         }
         issued = j + 1;
       }
@@ -202,11 +228,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
       bool ok = n_qt == 0 || mbar_wait(&bars->kv_full, 0, lim, abort);
       auto issue_grads = [&](int i) -> bool {
         const int st = i % kStages, b = i & 1;
-        if (!mbar_wait(&bars->ps_full[b], (i >> 1) & 1, lim, abort)) return false;
+        if (!mbar_wait(&bars->ps_full, i & 1, lim, abort)) return false;
         if (i >= 2 && !mbar_wait(&bars->dq_empty[b], ((i >> 1) - 1) & 1, lim, abort)) return false;
         tc_fence_after();
-        const uint32_t p_addr = smem_u32(smem + L::kP + b * L::kKVBox);
-        const uint32_t ds_addr = smem_u32(smem + L::kDS + b * L::kKVBox);
+        const uint32_t p_addr = smem_u32(smem + L::kP);
+        const uint32_t ds_addr = smem_u32(smem + L::kDS);
         const uint32_t q_addr = smem_u32(smem + L::kQ + st * 2 * L::kQBox);
         const uint32_t do_addr = smem_u32(smem + L::kDO + st * 2 * L::kQBox);
 #pragma unroll
@@ -219,14 +245,17 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
           mma_bf16(tmem + kColDV, pa, ob, idesc_kv, acc);
           mma_bf16(tmem + kColDK, da, qb, idesc_kv, acc);
         }
+        const uint32_t dsl_addr = smem_u32(smem + L::kDSL);
 #pragma unroll
         for (int kk = 0; kk < kBK / 16; ++kk) {     // over keys
           const uint64_t ka = sdesc_sw128(k_addr + kk * 16 * 128, L::kKVBox, 1024);
           const uint64_t sb = sdesc_sw128(ds_addr + kk * 16 * 128, 16, 1024);
+          const uint64_t lb = sdesc_sw128(dsl_addr + kk * 16 * 128, 16, 1024);
           mma_bf16(tmem + (b ? kColDQ1 : kColDQ0), ka, sb, idesc_dq, kk > 0 ? 1u : 0u);
+          mma_bf16(tmem + (b ? kColDQ1 : kColDQ0), ka, lb, idesc_dq, 1u);
         }
         mma_commit(&bars->qdo_empty[st]);
-        mma_commit(&bars->ps_empty[b]);
+        mma_commit(&bars->ps_empty);
         mma_commit(&bars->dq_full[b]);
         return true;
       };
@@ -266,17 +295,17 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
     }
   } else if (warp >= 4 && warp < 8) {
     // ------------------------------------------------------------ P / dS
-    const int u = threadIdx.x - 128;             // key row == TMEM lane
-    const uint32_t lane_off = (uint32_t)((warp - 4) * 32) << 16;
+    const int u = (warp & 3) * 32 + lane;        // key row == TMEM lane
+    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     const float sl2 = a.scale_log2;
     const bool key_ok = u < it.k_len;
     bool ok = true;
-    int i = 0;
-    for (int s = 0; ok && s < nseg; ++s) {
-      const Seg sg = it.seg[s];
-      const int q0 = run_qstart(sg), nt = run_qtiles(sg);
-      for (int t = 0; t < nt; ++t, ++i) {
-        const int st = i % kStages, b = i & 1;
+    for (int i = 0; ok && i < n_qt; ++i) {
+      {
+        Seg sg;
+        int q0, t;
+        tile_of(it, (i + rot) % n_qt, sg, q0, t);
+        const int st = i % kStages;
         if (!mbar_wait(&bars->sdp_full, i & 1, lim, abort) ||
             !mbar_wait(&bars->qdo_full[st], (i / kStages) & 1, lim, abort)) {
           ok = false;
@@ -303,42 +332,51 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars->sdp_empty);
-        const float* ls = lse_s + st * 2 * kBQ;
         const int row0 = q0 + t * kBQ;            // query index inside the run
-        // causal: key u visible to query row0 + x iff u <= row0 + x + delta
-        const int first_vis = u - sg.delta - row0;  // smallest visible x
+        const float* ld = reinterpret_cast<const float*>(smem + L::kLd + st * 1024) +
+                          ((sg.row0 + row0) & 3);
+        // key u is visible to query row0 + x iff x < len - row0 and, for a causal
+        // run, u <= row0 + x + delta
+        const int first_vis = sg.causal ? u - sg.delta - row0 : 0;
+        const int end_vis = key_ok ? sg.len - row0 : 0;
+        // P^T, bf16(dS^T) and the remainder dS^T - bf16(dS^T), packed in pairs as
+        // they are produced (keeps the live register set small)
+        uint32_t pk[kBQ / 2], hk[kBQ / 2], lk[kBQ / 2];
 #pragma unroll
-        for (int x = 0; x < kBQ; ++x) {
-          float p = ex2(sv[x] * sl2 - ls[x]);
-          if (!key_ok || (sg.causal && x < first_vis)) p = 0.f;
-          sv[x] = p;
-          dp[x] = p * (dp[x] - ls[kBQ + x]);
+        for (int x = 0; x < kBQ; x += 2) {
+          float p0 = ex2(sv[x] * sl2 - ld[x]);
+          float p1 = ex2(sv[x + 1] * sl2 - ld[x + 1]);
+          if (x < first_vis || x >= end_vis) p0 = 0.f;
+          if (x + 1 < first_vis || x + 1 >= end_vis) p1 = 0.f;
+          const float d0 = p0 * (dp[x] - ld[kLdRows + x]);
+          const float d1 = p1 * (dp[x + 1] - ld[kLdRows + x + 1]);
+          const float h0 = __bfloat162float(__float2bfloat16_rn(d0));
+          const float h1 = __bfloat162float(__float2bfloat16_rn(d1));
+          pk[x / 2] = pack_bf16x2(p0, p1);
+          hk[x / 2] = pack_bf16x2(h0, h1);
+          lk[x / 2] = pack_bf16x2(d0 - h0, d1 - h1);
         }
-        if (i >= 2 && !mbar_wait(&bars->ps_empty[b], ((i >> 1) - 1) & 1, lim, abort)) {
+        if (i >= 1 && !mbar_wait(&bars->ps_empty, (i - 1) & 1, lim, abort)) {
           ok = false;
           break;
         }
-        uint8_t* prow = smem + L::kP + b * L::kKVBox + u * 128;
-        uint8_t* srow = smem + L::kDS + b * L::kKVBox + u * 128;
+        uint8_t* prow = smem + L::kP + u * 128;
+        uint8_t* srow = smem + L::kDS + u * 128;
+        uint8_t* lrow = smem + L::kDSL + u * 128;
 #pragma unroll
         for (int c = 0; c < kBQ / 8; ++c) {
-          uint4 pv, dv;
-          pv.x = pack_bf16x2(sv[c * 8 + 0], sv[c * 8 + 1]);
-          pv.y = pack_bf16x2(sv[c * 8 + 2], sv[c * 8 + 3]);
-          pv.z = pack_bf16x2(sv[c * 8 + 4], sv[c * 8 + 5]);
-          pv.w = pack_bf16x2(sv[c * 8 + 6], sv[c * 8 + 7]);
-          dv.x = pack_bf16x2(dp[c * 8 + 0], dp[c * 8 + 1]);
-          dv.y = pack_bf16x2(dp[c * 8 + 2], dp[c * 8 + 3]);
-          dv.z = pack_bf16x2(dp[c * 8 + 4], dp[c * 8 + 5]);
-          dv.w = pack_bf16x2(dp[c * 8 + 6], dp[c * 8 + 7]);
           const int sw = (c ^ (u & 7)) << 4;
-          *reinterpret_cast<uint4*>(prow + sw) = pv;
-          *reinterpret_cast<uint4*>(srow + sw) = dv;
+          *reinterpret_cast<uint4*>(prow + sw) =
+              make_uint4(pk[c * 4], pk[c * 4 + 1], pk[c * 4 + 2], pk[c * 4 + 3]);
+          *reinterpret_cast<uint4*>(srow + sw) =
+              make_uint4(hk[c * 4], hk[c * 4 + 1], hk[c * 4 + 2], hk[c * 4 + 3]);
+          *reinterpret_cast<uint4*>(lrow + sw) =
+              make_uint4(lk[c * 4], lk[c * 4 + 1], lk[c * 4 + 2], lk[c * 4 + 3]);
         }
         fence_proxy_async_smem();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&bars->ps_full[b]);
+        if (lane == 0) mbar_arrive(&bars->ps_full);
       }
     }
     // ------------------------------------------------------------ dK / dV epilogue
@@ -392,14 +430,14 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
     }
   } else if (warp >= 8) {
     // ------------------------------------------------------------ dQ drain
-    const int dd = threadIdx.x - 256;            // head-dim index == TMEM lane of dQ^T
-    const uint32_t lane_off = (uint32_t)((warp - 8) * 32) << 16;
+    const int dd = (warp & 3) * 32 + lane;       // head-dim index == TMEM lane of dQ^T
+    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     bool ok = true;
-    int i = 0;
-    for (int s = 0; ok && s < nseg; ++s) {
-      const Seg sg = it.seg[s];
-      const int q0 = run_qstart(sg), nt = run_qtiles(sg);
-      for (int t = 0; t < nt; ++t, ++i) {
+    for (int i = 0; ok && i < n_qt; ++i) {
+      {
+        Seg sg;
+        int q0, t;
+        tile_of(it, (i + rot) % n_qt, sg, q0, t);
         const int b = i & 1;
         if (!mbar_wait(&bars->dq_full[b], (i >> 1) & 1, lim, abort)) {
           ok = false;
@@ -425,7 +463,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
         const int nrow = min(kBQ, sg.len - row0);
         float* base = a.dq + ((long long)(sg.row0 + row0) * a.H + h) * kD + dd;
         const long long stride = (long long)a.H * kD;
-        for (int x = 0; x < nrow; ++x) atomicAdd(base + x * stride, v[x] * a.scale);
+#pragma unroll
+        for (int x = 0; x < kBQ; ++x)
+          if (x < nrow) atomicAdd(base + x * stride, v[x] * a.scale);
       }
     }
     if (!ok) record_timeout(a.status, abort, 14);

@@ -248,15 +248,18 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
         tc_fence_after();
         float x[kBN];
         {
-          uint32_t r[32];
+          // four 32-column loads in flight, one wait
+          uint32_t r[kBN];
+          const uint32_t s_col = tmem + lane_off + (sb ? kColS1 : kColS0);
 #pragma unroll
-          for (int c = 0; c < kBN / 32; ++c) {
-            tmem_ld32(tmem + lane_off + (sb ? kColS1 : kColS0) + c * 32, r);
-            tmem_ld_wait();
-            reg_fence32(r);
+          for (int c = 0; c < kBN / 32; ++c)
+            tmem_ld32(s_col + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&r[c * 32]));
+          tmem_ld_wait();
 #pragma unroll
-            for (int i = 0; i < 32; ++i) x[c * 32 + i] = __uint_as_float(r[i]) * sl2;
-          }
+          for (int c = 0; c < kBN / 32; ++c)
+            reg_fence32(*reinterpret_cast<uint32_t(*)[32]>(&r[c * 32]));
+#pragma unroll
+          for (int c = 0; c < kBN; ++c) x[c] = __uint_as_float(r[c]) * sl2;
         }
         tc_fence_before();
         __syncwarp();
@@ -270,9 +273,14 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
           for (int c = 0; c < kBN; ++c)
             if (u0 + c >= lim_u) x[c] = -INFINITY;
         }
-        float mt = -INFINITY;
+        // row max with 8 independent partial maxima (short dependency chains)
+        float mp[8];
 #pragma unroll
-        for (int c = 0; c < kBN; ++c) mt = fmaxf(mt, x[c]);
+        for (int i = 0; i < 8; ++i) mp[i] = x[i];
+#pragma unroll
+        for (int c = 8; c < kBN; ++c) mp[c & 7] = fmaxf(mp[c & 7], x[c]);
+        const float mt = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
+                               fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
         const float m_new = fmaxf(m, mt);
         const bool need = m_new > m + kRescaleThreshold || (m == -INFINITY && m_new != -INFINITY);
         if (__any_sync(0xffffffffu, need)) {
@@ -298,13 +306,15 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
           }
         }
         const float mu = m == -INFINITY ? 0.f : m;
-        float ls = 0.f;
+        float sp[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) sp[i] = 0.f;
 #pragma unroll
         for (int c = 0; c < kBN; ++c) {
           x[c] = ex2(x[c] - mu);
-          ls += x[c];
+          sp[c & 7] += x[c];
         }
-        l += ls;
+        l += ((sp[0] + sp[1]) + (sp[2] + sp[3])) + ((sp[4] + sp[5]) + (sp[6] + sp[7]));
         // P buffer is free once the PV of the previous tile has completed
         if (j > 0 && !mbar_wait(&bars->o_done, (j - 1) & 1, lim, abort)) { ok = false; break; }
         // P row t, 128-byte swizzle: 16-byte chunk q of a 128-byte row -> q ^ (t & 7)
@@ -349,8 +359,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
       }
       const float* orun = a.o_run + rrow * D;
       float* orun_w = a.o_run + rrow * D;
-      __nv_bfloat16* outp =
-          reinterpret_cast<__nv_bfloat16*>(a.out) + ((long long)(it.out_row0 + t) * a.H + h) * D;
+      const long long out_off = ((long long)(it.out_row0 + t) * a.H + h) * D;
+      __nv_bfloat16* outp = reinterpret_cast<__nv_bfloat16*>(a.out) + out_off;
+      __nv_bfloat16* lop =
+          a.out_lo ? reinterpret_cast<__nv_bfloat16*>(a.out_lo) + out_off : nullptr;
 #pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {
         uint32_t r[32];
@@ -380,6 +392,18 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
             v.z = pack_bf16x2(o[i + 4], o[i + 5]);
             v.w = pack_bf16x2(o[i + 6], o[i + 7]);
             *reinterpret_cast<uint4*>(outp + c * 32 + i) = v;
+            if (lop) {  // remainder o - bf16(o), itself rounded to bf16
+              float lo[8];
+#pragma unroll
+              for (int e = 0; e < 8; ++e)
+                lo[e] = o[i + e] - __bfloat162float(__float2bfloat16_rn(o[i + e]));
+              uint4 w;
+              w.x = pack_bf16x2(lo[0], lo[1]);
+              w.y = pack_bf16x2(lo[2], lo[3]);
+              w.z = pack_bf16x2(lo[4], lo[5]);
+              w.w = pack_bf16x2(lo[6], lo[7]);
+              *reinterpret_cast<uint4*>(lop + c * 32 + i) = w;
+            }
           }
         } else {
 #pragma unroll
