@@ -28,6 +28,8 @@
 // [192,256), dK [256,384), dV [384,512).
 #include <cuda_bf16.h>
 
+#include <type_traits>
+
 #include "kernels.h"
 #include "ptx.cuh"
 #include "tc.h"
@@ -48,6 +50,7 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0, kColDP = 64, kColDQ0 = 128, kColDQ1 = 192, kColDK = 256,
                    kColDV = 384;
 constexpr long long kDrainLimit = 1LL << 24;
+constexpr float kSplitScale = 0.25f;  // softmax scales above this use the dS hi + lo split
 
 struct L {
   static constexpr int kKVBox = 128 * 128;   // 128 rows x 128 bytes
@@ -109,10 +112,12 @@ __device__ __forceinline__ void record_timeout(int32_t* status, volatile int* ab
   *abort = 1;
 }
 
+template <bool kSplit>
 __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_constant__ TcBwdArgs a) {
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  // 1024-byte aligned base, derived from the shared array itself so that the
+  // compiler keeps shared-space (not generic) loads and stores
+  uint8_t* smem = smem_raw + ((1024u - (ptx::smem_u32(smem_raw) & 1023u)) & 1023u);
   Bars* bars = reinterpret_cast<Bars*>(smem + L::kBars);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int item_idx = blockIdx.x % a.n_items;
@@ -131,12 +136,12 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
       mbar_init(&bars->qdo_empty[s], 1);
     }
     mbar_init(&bars->sdp_full, 1);
-    mbar_init(&bars->sdp_empty, 4);
-    mbar_init(&bars->ps_full, 4);
+    mbar_init(&bars->sdp_empty, 8);
+    mbar_init(&bars->ps_full, 8);
     mbar_init(&bars->ps_empty, 1);
     for (int b = 0; b < 2; ++b) {
       mbar_init(&bars->dq_full[b], 1);
-      mbar_init(&bars->dq_empty[b], 4);
+      mbar_init(&bars->dq_empty[b], 8);
     }
     mbar_init(&bars->dkv_done, 1);
     mbar_init(&bars->drain, 1);
@@ -155,10 +160,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
   const int nseg = it.nseg;
   int n_qt = 0;
   for (int s = 0; s < nseg; ++s) n_qt += run_qtiles(it.seg[s]);
-  // Every role walks the query tiles in the same rotated order.  Concurrent
-  // CTAs are neighbouring key tiles of one head that meet the same queries;
-  // the rotation keeps their dQ atomics on different rows.
-  const int rot = n_qt > 0 ? (int)(((long long)item_idx * 17 + (long long)h * 7) % n_qt) : 0;
+  // Every role walks the query tiles in the same order.  Concurrent CTAs are
+  // neighbouring key tiles of one head that meet the same queries in the same
+  // order, so the Q / dO tiles they load are shared through L2 (a rotated
+  // order per CTA measured slower).
+  const int rot = 0;
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
@@ -252,7 +258,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
           const uint64_t sb = sdesc_sw128(ds_addr + kk * 16 * 128, 16, 1024);
           const uint64_t lb = sdesc_sw128(dsl_addr + kk * 16 * 128, 16, 1024);
           mma_bf16(tmem + (b ? kColDQ1 : kColDQ0), ka, sb, idesc_dq, kk > 0 ? 1u : 0u);
-          mma_bf16(tmem + (b ? kColDQ1 : kColDQ0), ka, lb, idesc_dq, 1u);
+          if (kSplit) mma_bf16(tmem + (b ? kColDQ1 : kColDQ0), ka, lb, idesc_dq, 1u);
         }
         mma_commit(&bars->qdo_empty[st]);
         mma_commit(&bars->ps_empty);
@@ -293,182 +299,185 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
         mbar_wait(&bars->drain, 0, kDrainLimit, &zero);
       }
     }
-  } else if (warp >= 4 && warp < 8) {
-    // ------------------------------------------------------------ P / dS
-    const int u = (warp & 3) * 32 + lane;        // key row == TMEM lane
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ P / dS, dQ drain
+    // Two warpgroups share every query tile: warpgroup g (warps 4+4g .. 7+4g)
+    // computes P^T / dS^T for query columns [32g, 32g + 32) of its key rows,
+    // then drains the same columns of the previous tile's dQ^T.
+    const int g = (warp - 4) >> 2;
+    const int u = (warp & 3) * 32 + lane;        // key row (and head-dim index for dQ^T)
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     const float sl2 = a.scale_log2;
     const bool key_ok = u < it.k_len;
     bool ok = true;
-    for (int i = 0; ok && i < n_qt; ++i) {
-      {
-        Seg sg;
-        int q0, t;
-        tile_of(it, (i + rot) % n_qt, sg, q0, t);
-        const int st = i % kStages;
-        if (!mbar_wait(&bars->sdp_full, i & 1, lim, abort) ||
-            !mbar_wait(&bars->qdo_full[st], (i / kStages) & 1, lim, abort)) {
-          ok = false;
-          break;
+    auto drain = [&](int j) -> bool {             // dQ^T columns of tile j, this half
+      Seg sgd;
+      int q0d, td;
+      tile_of(it, (j + rot) % n_qt, sgd, q0d, td);
+      const int b = j & 1;
+      if (!mbar_wait(&bars->dq_full[b], (j >> 1) & 1, lim, abort)) return false;
+      tc_fence_after();
+      uint32_t r[32];
+      tmem_ld32(tmem + lane_off + (b ? kColDQ1 : kColDQ0) + g * 32, r);
+      tmem_ld_wait();
+      reg_fence32(r);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->dq_empty[b]);
+      // quad transpose: lane 4k+i receives head dims 4k..4k+3 of query column
+      // 4c+i, so every atomic is a 16-byte vector
+      const int row0 = q0d + td * kBQ + g * 32;  // first query (inside the run) of this half
+      const int nrow = sgd.len - row0;
+      const long long stride = (long long)a.H * kD;
+      float* base = a.dq + ((long long)(sgd.row0 + row0) * a.H + h) * kD + (warp & 3) * 32 +
+                    (lane & ~3);
+      const bool b0 = lane & 1, b1 = lane & 2;
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        float v0 = __uint_as_float(r[4 * c]) * a.scale, v1 = __uint_as_float(r[4 * c + 1]) * a.scale;
+        float v2 = __uint_as_float(r[4 * c + 2]) * a.scale, v3 = __uint_as_float(r[4 * c + 3]) * a.scale;
+        float s0 = b0 ? v0 : v1, s1 = b0 ? v2 : v3;
+        s0 = __shfl_xor_sync(0xffffffffu, s0, 1);
+        s1 = __shfl_xor_sync(0xffffffffu, s1, 1);
+        if (b0) { v0 = s0; v2 = s1; } else { v1 = s0; v3 = s1; }
+        s0 = b1 ? v0 : v2;
+        s1 = b1 ? v1 : v3;
+        s0 = __shfl_xor_sync(0xffffffffu, s0, 2);
+        s1 = __shfl_xor_sync(0xffffffffu, s1, 2);
+        if (b1) { v0 = s0; v1 = s1; } else { v2 = s0; v3 = s1; }
+        const int x = 4 * c + (lane & 3);        // query column inside this half
+        if (x < nrow) {
+          float* p = base + x * stride;
+          asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(v0),
+                       "f"(v1), "f"(v2), "f"(v3)
+                       : "memory");
         }
-        tc_fence_after();
-        float sv[kBQ], dp[kBQ];
-        {
-          uint32_t r[32];
+      }
+      return true;
+    };
+    for (int i = 0; ok && i < n_qt; ++i) {
+      Seg sg;
+      int q0, t;
+      tile_of(it, (i + rot) % n_qt, sg, q0, t);
+      const int st = i % kStages;
+      if (!mbar_wait(&bars->sdp_full, i & 1, lim, abort) ||
+          !mbar_wait(&bars->qdo_full[st], (i / kStages) & 1, lim, abort)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      uint32_t rs[32], rd[32];
+      tmem_ld32(tmem + lane_off + kColS + g * 32, rs);
+      tmem_ld32(tmem + lane_off + kColDP + g * 32, rd);
+      tmem_ld_wait();
+      reg_fence32(rs);
+      reg_fence32(rd);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->sdp_empty);
+      const int row0 = q0 + t * kBQ + g * 32;     // first query of this half (inside the run)
+      const float* ld = reinterpret_cast<const float*>(smem + L::kLd + st * 1024) +
+                        ((sg.row0 + q0 + t * kBQ) & 3) + g * 32;
+      // key u is visible to query row0 + x iff x < len - row0 and, for a causal
+      // run, u <= row0 + x + delta
+      const int first_vis = sg.causal ? u - sg.delta - row0 : 0;
+      const int end_vis = key_ok ? sg.len - row0 : 0;
+      const bool whole = __all_sync(0xffffffffu, first_vis <= 0 && end_vis >= 32);
+      uint32_t pk[16], hk[16], lk[16];
+      auto compute = [&](auto masked) {
 #pragma unroll
-          for (int c = 0; c < kBQ / 32; ++c) {
-            tmem_ld32(tmem + lane_off + kColS + c * 32, r);
-            tmem_ld_wait();
-            reg_fence32(r);
-#pragma unroll
-            for (int x = 0; x < 32; ++x) sv[c * 32 + x] = __uint_as_float(r[x]);
-            tmem_ld32(tmem + lane_off + kColDP + c * 32, r);
-            tmem_ld_wait();
-            reg_fence32(r);
-#pragma unroll
-            for (int x = 0; x < 32; ++x) dp[c * 32 + x] = __uint_as_float(r[x]);
+        for (int x = 0; x < 32; x += 2) {
+          float p0 = ex2(fmaf(__uint_as_float(rs[x]), sl2, -ld[x]));
+          float p1 = ex2(fmaf(__uint_as_float(rs[x + 1]), sl2, -ld[x + 1]));
+          if (decltype(masked)::value) {
+            if (x < first_vis || x >= end_vis) p0 = 0.f;
+            if (x + 1 < first_vis || x + 1 >= end_vis) p1 = 0.f;
+          }
+          const float d0 = p0 * (__uint_as_float(rd[x]) - ld[kLdRows + x]);
+          const float d1 = p1 * (__uint_as_float(rd[x + 1]) - ld[kLdRows + x + 1]);
+          pk[x / 2] = pack_bf16x2(p0, p1);
+          if (kSplit) {
+            const float h0 = __bfloat162float(__float2bfloat16_rn(d0));
+            const float h1 = __bfloat162float(__float2bfloat16_rn(d1));
+            hk[x / 2] = pack_bf16x2(h0, h1);
+            lk[x / 2] = pack_bf16x2(d0 - h0, d1 - h1);
+          } else {
+            hk[x / 2] = pack_bf16x2(d0, d1);
           }
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bars->sdp_empty);
-        const int row0 = q0 + t * kBQ;            // query index inside the run
-        const float* ld = reinterpret_cast<const float*>(smem + L::kLd + st * 1024) +
-                          ((sg.row0 + row0) & 3);
-        // key u is visible to query row0 + x iff x < len - row0 and, for a causal
-        // run, u <= row0 + x + delta
-        const int first_vis = sg.causal ? u - sg.delta - row0 : 0;
-        const int end_vis = key_ok ? sg.len - row0 : 0;
-        // P^T, bf16(dS^T) and the remainder dS^T - bf16(dS^T), packed in pairs as
-        // they are produced (keeps the live register set small)
-        uint32_t pk[kBQ / 2], hk[kBQ / 2], lk[kBQ / 2];
+      };
+      if (whole) compute(std::integral_constant<bool, false>());
+      else compute(std::integral_constant<bool, true>());
+      if (i >= 1 && !mbar_wait(&bars->ps_empty, (i - 1) & 1, lim, abort)) {
+        ok = false;
+        break;
+      }
+      uint8_t* prow = smem + L::kP + u * 128;
+      uint8_t* srow = smem + L::kDS + u * 128;
+      uint8_t* lrow = smem + L::kDSL + u * 128;
 #pragma unroll
-        for (int x = 0; x < kBQ; x += 2) {
-          float p0 = ex2(sv[x] * sl2 - ld[x]);
-          float p1 = ex2(sv[x + 1] * sl2 - ld[x + 1]);
-          if (x < first_vis || x >= end_vis) p0 = 0.f;
-          if (x + 1 < first_vis || x + 1 >= end_vis) p1 = 0.f;
-          const float d0 = p0 * (dp[x] - ld[kLdRows + x]);
-          const float d1 = p1 * (dp[x + 1] - ld[kLdRows + x + 1]);
-          const float h0 = __bfloat162float(__float2bfloat16_rn(d0));
-          const float h1 = __bfloat162float(__float2bfloat16_rn(d1));
-          pk[x / 2] = pack_bf16x2(p0, p1);
-          hk[x / 2] = pack_bf16x2(h0, h1);
-          lk[x / 2] = pack_bf16x2(d0 - h0, d1 - h1);
-        }
-        if (i >= 1 && !mbar_wait(&bars->ps_empty, (i - 1) & 1, lim, abort)) {
-          ok = false;
-          break;
-        }
-        uint8_t* prow = smem + L::kP + u * 128;
-        uint8_t* srow = smem + L::kDS + u * 128;
-        uint8_t* lrow = smem + L::kDSL + u * 128;
-#pragma unroll
-        for (int c = 0; c < kBQ / 8; ++c) {
-          const int sw = (c ^ (u & 7)) << 4;
-          *reinterpret_cast<uint4*>(prow + sw) =
-              make_uint4(pk[c * 4], pk[c * 4 + 1], pk[c * 4 + 2], pk[c * 4 + 3]);
-          *reinterpret_cast<uint4*>(srow + sw) =
-              make_uint4(hk[c * 4], hk[c * 4 + 1], hk[c * 4 + 2], hk[c * 4 + 3]);
+      for (int c = 0; c < 4; ++c) {
+        const int sw = ((g * 4 + c) ^ (u & 7)) << 4;
+        *reinterpret_cast<uint4*>(prow + sw) =
+            make_uint4(pk[c * 4], pk[c * 4 + 1], pk[c * 4 + 2], pk[c * 4 + 3]);
+        *reinterpret_cast<uint4*>(srow + sw) =
+            make_uint4(hk[c * 4], hk[c * 4 + 1], hk[c * 4 + 2], hk[c * 4 + 3]);
+        if (kSplit)
           *reinterpret_cast<uint4*>(lrow + sw) =
               make_uint4(lk[c * 4], lk[c * 4 + 1], lk[c * 4 + 2], lk[c * 4 + 3]);
-        }
-        fence_proxy_async_smem();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bars->ps_full);
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->ps_full);
+      if (i >= 1 && !drain(i - 1)) {
+        ok = false;
+        break;
       }
     }
+    if (ok && n_qt > 0 && !drain(n_qt - 1)) ok = false;
     // ------------------------------------------------------------ dK / dV epilogue
     if (ok && n_qt > 0 && !mbar_wait(&bars->dkv_done, 0, lim, abort)) ok = false;
     if (!ok) {
       record_timeout(a.status, abort, 13);
     } else {
       tc_fence_after();
-      float* pk;
-      float* pv;
+      // warpgroup 0 writes dK (scaled), warpgroup 1 writes dV
+      float* dst;
       if (it.dk_mode == DK_TEXT) {
-        pk = a.dk + ((long long)(it.k_row0 + u) * a.H + h) * kD;
-        pv = a.dv + ((long long)(it.k_row0 + u) * a.H + h) * kD;
+        dst = (g == 0 ? a.dk : a.dv) + ((long long)(it.k_row0 + u) * a.H + h) * kD;
       } else {
         const long long row = (long long)it.slot * a.pre_rows + it.dk_row0 + u;
-        pk = a.pre_k + (row * a.H + h) * kD;
-        pv = a.pre_v + (row * a.H + h) * kD;
+        dst = (g == 0 ? a.pre_k : a.pre_v) + (row * a.H + h) * kD;
       }
       const bool first = (it.flags & F_FIRST) != 0;
+      const float mul = g == 0 ? a.scale : 1.f;
+      const uint32_t col = g == 0 ? kColDK : kColDV;
 #pragma unroll 1
-      for (int which = 0; which < 2; ++which) {
-        float* dst = which == 0 ? pk : pv;
-        const float mul = which == 0 ? a.scale : 1.f;
-        const uint32_t col = which == 0 ? kColDK : kColDV;
-#pragma unroll 1
-        for (int c = 0; c < kD / 32; ++c) {
-          uint32_t r[32];
-          if (n_qt > 0) {
-            tmem_ld32(tmem + lane_off + col + c * 32, r);
-            tmem_ld_wait();
-            reg_fence32(r);
-          } else {
+      for (int c = 0; c < kD / 32; ++c) {
+        uint32_t r[32];
+        if (n_qt > 0) {
+          tmem_ld32(tmem + lane_off + col + c * 32, r);
+          tmem_ld_wait();
+          reg_fence32(r);
+        } else {
 #pragma unroll
-            for (int x = 0; x < 32; ++x) r[x] = 0u;
-          }
-          if (!key_ok) continue;
+          for (int x = 0; x < 32; ++x) r[x] = 0u;
+        }
+        if (!key_ok) continue;
 #pragma unroll
-          for (int x = 0; x < 32; x += 4) {
-            float4 v = make_float4(__uint_as_float(r[x]) * mul, __uint_as_float(r[x + 1]) * mul,
-                                   __uint_as_float(r[x + 2]) * mul,
-                                   __uint_as_float(r[x + 3]) * mul);
-            float4* d4 = reinterpret_cast<float4*>(dst + c * 32 + x);
-            if (!first) {
-              const float4 o = *d4;
-              v.x += o.x; v.y += o.y; v.z += o.z; v.w += o.w;
-            }
-            *d4 = v;
+        for (int x = 0; x < 32; x += 4) {
+          float4 v = make_float4(__uint_as_float(r[x]) * mul, __uint_as_float(r[x + 1]) * mul,
+                                 __uint_as_float(r[x + 2]) * mul, __uint_as_float(r[x + 3]) * mul);
+          float4* d4 = reinterpret_cast<float4*>(dst + c * 32 + x);
+          if (!first) {
+            const float4 o = *d4;
+            v.x += o.x; v.y += o.y; v.z += o.z; v.w += o.w;
           }
+          *d4 = v;
         }
       }
     }
-  } else if (warp >= 8) {
-    // ------------------------------------------------------------ dQ drain
-    const int dd = (warp & 3) * 32 + lane;       // head-dim index == TMEM lane of dQ^T
-    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
-    bool ok = true;
-    for (int i = 0; ok && i < n_qt; ++i) {
-      {
-        Seg sg;
-        int q0, t;
-        tile_of(it, (i + rot) % n_qt, sg, q0, t);
-        const int b = i & 1;
-        if (!mbar_wait(&bars->dq_full[b], (i >> 1) & 1, lim, abort)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        float v[kBQ];
-        {
-          uint32_t r[32];
-#pragma unroll
-          for (int c = 0; c < kBQ / 32; ++c) {
-            tmem_ld32(tmem + lane_off + (b ? kColDQ1 : kColDQ0) + c * 32, r);
-            tmem_ld_wait();
-            reg_fence32(r);
-#pragma unroll
-            for (int x = 0; x < 32; ++x) v[c * 32 + x] = __uint_as_float(r[x]);
-          }
-        }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bars->dq_empty[b]);
-        const int row0 = q0 + t * kBQ;
-        const int nrow = min(kBQ, sg.len - row0);
-        float* base = a.dq + ((long long)(sg.row0 + row0) * a.H + h) * kD + dd;
-        const long long stride = (long long)a.H * kD;
-#pragma unroll
-        for (int x = 0; x < kBQ; ++x)
-          if (x < nrow) atomicAdd(base + x * stride, v[x] * a.scale);
-      }
-    }
-    if (!ok) record_timeout(a.status, abort, 14);
   }
   tc_fence_before();
   __syncthreads();
@@ -478,18 +487,25 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
   }
 }
 
+template <bool kSplit>
+cudaError_t launch_split(const TcBwdArgs& a, cudaStream_t st) {
+  cudaError_t e = cudaFuncSetAttribute(tc_bwd_kernel<kSplit>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
+  if (e != cudaSuccess) return e;
+  const long long blocks = (long long)a.n_items * a.H;
+  if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  tc_bwd_kernel<kSplit><<<(unsigned)blocks, kThreads, L::kAlloc, st>>>(a);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t launch_tc_bwd(const TcBwdArgs& a, cudaStream_t st) {
   if (a.n_items == 0) return cudaSuccess;
   if (a.d != kD) return cudaErrorNotSupported;
-  cudaError_t e = cudaFuncSetAttribute(tc_bwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       L::kAlloc);
-  if (e != cudaSuccess) return e;
-  const long long blocks = (long long)a.n_items * a.H;
-  if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  tc_bwd_kernel<<<(unsigned)blocks, kThreads, L::kAlloc, st>>>(a);
-  return cudaGetLastError();
+  // The dQ error from one bf16 rounding of dS grows with the softmax scale
+  // (dQ = scale * dS K).  Above kSplitScale the remainder term is added.
+  return a.scale > kSplitScale ? launch_split<true>(a, st) : launch_split<false>(a, st);
 }
 
 }  // namespace cpattn

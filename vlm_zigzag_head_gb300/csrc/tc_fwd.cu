@@ -81,8 +81,9 @@ __device__ __forceinline__ void record_timeout(int32_t* status, volatile int* ab
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_constant__ TcFwdArgs a) {
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  // 1024-byte aligned base, derived from the shared array itself so that the
+  // compiler keeps shared-space (not generic) loads and stores
+  uint8_t* smem = smem_raw + ((1024u - (ptx::smem_u32(smem_raw) & 1023u)) & 1023u);
   using L = Smem<D>;
   Bars* bars = reinterpret_cast<Bars*>(smem + L::kBars);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
