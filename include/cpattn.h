@@ -150,6 +150,43 @@ cp_status_t cp_attn_fwd(const void* q, const void* k, const void* v, cp_dtype_t 
                         void* out_lo, void* workspace, size_t ws_bytes, void* stream);
 
 /*
+ * cp_attn_fwd_noalloc -- cp_attn_fwd for callers that cannot allocate device
+ * memory.  The source pages have no counterpart to this entry point.
+ *
+ * Some callers are not allowed to allocate: a host framework that owns the
+ * whole device memory pool and forbids allocations outside its own allocator,
+ * or a deployment that runs inside a fixed memory budget reserved up front.
+ * Such callers cannot provide the workspace cp_attn_fwd needs.  This entry
+ * point takes the same arguments minus the workspace and uses a fixed scratch
+ * array of 64 MiB compiled into the library instead (every GPU that loads the
+ * library holds it until the process exits).  It calls no cudaMalloc,
+ * cudaFree or other allocating routine; work lists are copied from ordinary
+ * host memory.
+ *
+ *  - Capacity: the scratch holds the work list, the zigzag table, the
+ *    rank-local q/k/v (3 x rows x H x d elements) and the fp32 running result
+ *    (rows x H x (d + 1) x 4 bytes), rows = text tokens.  For bf16 and
+ *    d = 128 that is about 1.3 KB per (text token, head), so about 50 000
+ *    (token, head) pairs, e.g. 4096 tokens with 12 heads.  Larger problems
+ *    return CP_ERR_WORKSPACE with the number of bytes they would need.
+ *  - The first call on a device looks up the scratch's device address
+ *    (cudaGetSymbolAddress, with that device current); make that first call
+ *    before any stream capture.
+ *  - Every call shares the one array and leaves its contents behind; the
+ *    status word is cleared at the start of each call and everything else is
+ *    written before it is read.  Calls that overlap on the GPU (other streams,
+ *    other host threads) race on the scratch: order them on one stream.
+ *  - Results equal cp_attn_fwd's (same kernels).  cp_workspace_status does not
+ *    apply (there is no caller workspace).
+ * Errors: as cp_attn_fwd, plus CP_ERR_WORKSPACE when the problem exceeds the
+ * fixed scratch.
+ */
+cp_status_t cp_attn_fwd_noalloc(const void* q, const void* k, const void* v, cp_dtype_t dt,
+                                int T, int H, int d, const int32_t* cu_seqlens_h, int n_seqs,
+                                int P, int prefix_len, float softmax_scale, void* out,
+                                float* lse, void* out_lo, void* stream);
+
+/*
  * cp_lse_merge -- merge n_parts partial attention results over disjoint key
  * sets by log-sum-exp (the Ring Attention combination the CP-VLM page relies
  * on in §1 and §4.1 step 5):

@@ -23,6 +23,7 @@ from . import _binding as _b
 from ._binding import CP_BF16, CP_F32, CpError  # noqa: F401
 
 __all__ = ["cp_zigzag_index", "cp_zigzag_gather", "cp_zigzag_scatter", "cp_attn_fwd",
+           "cp_attn_fwd_noalloc",
            "cp_lse_merge", "cp_attn_bwd", "cp_workspace_status", "cp_set_wait_limit",
            "cp_plan_pairs", "cp_profile_begin", "cp_profile_end", "Workspace",
            "attention_host", "CpError"]
@@ -157,6 +158,29 @@ def cp_attn_fwd(q, k, v, cu_seqlens, P: int, prefix_len: int, softmax_scale: flo
                            ctypes.c_void_p(ws.ptr()), ws.nbytes(), _stream(q.device)))
     if residual:
         return out, lse, out_lo
+    return out, lse
+
+
+def cp_attn_fwd_noalloc(q, k, v, cu_seqlens, P: int, prefix_len: int, softmax_scale: float,
+                        out=None, lse=None, out_lo=None):
+    """The forward for callers that cannot allocate device memory (their
+    memory is owned by another allocator, or fixed up front): same result as
+    :func:`cp_attn_fwd`, but the library's fixed 64 MiB scratch replaces the
+    workspace.  Outputs may be passed in (``out``, ``lse``, ``out_lo``) so the
+    call allocates nothing; the first call on a device must precede any
+    stream capture; calls that overlap on the GPU race on the shared scratch."""
+    _need_cuda(q, k, v, out, lse, out_lo)
+    T, H, d = q.shape
+    dt = _dt(q)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((H, T), dtype=torch.float32, device=q.device)
+    cu = _b.cu_array(cu_seqlens)
+    _b.check(_b.lib().cp_attn_fwd_noalloc(_ptr(q), _ptr(k), _ptr(v), dt, T, H, d, cu,
+                                          len(cu_seqlens) - 1, P, prefix_len,
+                                          float(softmax_scale), _ptr(out), _ptr(lse),
+                                          _ptr(out_lo), _stream(q.device)))
     return out, lse
 
 

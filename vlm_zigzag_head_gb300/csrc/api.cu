@@ -284,6 +284,13 @@ struct ProfScope {
 
 }  // namespace
 
+namespace cpattn {
+// Shared with other translation units of the library (the fixed-scratch entry
+// point): the thread-local error message and the device wait bound.
+void set_last_error(const std::string& msg) { g_err = msg; }
+long long device_wait_limit() { return wait_limit(); }
+}  // namespace cpattn
+
 extern "C" {
 
 const char* cp_last_error(void) { return g_err.c_str(); }

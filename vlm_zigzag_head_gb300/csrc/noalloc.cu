@@ -1,0 +1,187 @@
+// cp_attn_fwd_noalloc: the forward for callers that cannot allocate device
+// memory.  Its scratch (work list, zigzag table, rank-local q/k/v, the fp32
+// running result) lives in one fixed array compiled into this library instead
+// of a caller-supplied workspace.  Host-side uploads are plain copies from the
+// plan's own vectors; nothing here calls cudaMalloc, cudaFree, cudaHostAlloc
+// or any other allocating routine.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdio>
+#include <mutex>
+#include <string>
+
+#include "../../include/cpattn.h"
+#include "kernels.h"
+#include "plan.h"
+#include "tc.h"
+
+namespace cpattn {
+void set_last_error(const std::string& msg);
+long long device_wait_limit();
+}  // namespace cpattn
+
+using namespace cpattn;
+
+namespace {
+
+// The fixed scratch: every GPU that loads the library holds it until exit.
+constexpr size_t kScratchBytes = 64ull << 20;
+static __device__ __align__(256) uint8_t g_scratch[kScratchBytes];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+void* g_scratch_addr[kMaxDevices] = {};
+
+cp_status_t fail(cp_status_t s, const std::string& m) {
+  set_last_error(m);
+  return s;
+}
+
+inline size_t up256(size_t x) { return (x + 255) / 256 * 256; }
+
+// Device address of the scratch on the current device (looked up once per
+// device, with that device current).
+cp_status_t scratch_address(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(CP_ERR_CUDA, std::string("cudaGetDevice: ") + cudaGetErrorString(e));
+  if (dev < 0 || dev >= kMaxDevices) return fail(CP_ERR_UNSUPPORTED, "device index out of range");
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_scratch_addr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_scratch);
+    if (e != cudaSuccess || !p)
+      return fail(CP_ERR_CUDA, std::string("cudaGetSymbolAddress: ") + cudaGetErrorString(e));
+    g_scratch_addr[dev] = p;
+  }
+  *out = g_scratch_addr[dev];
+  return CP_OK;
+}
+
+}  // namespace
+
+extern "C" cp_status_t cp_attn_fwd_noalloc(const void* q, const void* k, const void* v,
+                                           cp_dtype_t dt, int T, int H, int d,
+                                           const int32_t* cu, int n_seqs, int P, int N,
+                                           float scale, void* out, float* lse, void* out_lo,
+                                           void* stream) {
+  if (dt != CP_F32 && dt != CP_BF16) return fail(CP_ERR_DTYPE, "dtype must be CP_F32 or CP_BF16");
+  if (T < 0 || H < 1 || n_seqs < 1 || P < 1 || N < 0 || !cu)
+    return fail(CP_ERR_INVALID_ARG, "T >= 0, H >= 1, n_seqs >= 1, P >= 1, prefix_len >= 0, cu");
+  if (d != 64 && d != 128) return fail(CP_ERR_SHAPE, "head_dim must be 64 or 128");
+  if (!std::isfinite(scale)) return fail(CP_ERR_INVALID_ARG, "softmax_scale must be finite");
+  if (out_lo && dt != CP_BF16) return fail(CP_ERR_DTYPE, "out_lo is for bf16 outputs only");
+  const void* ptrs[6] = {q, k, v, out, lse, out_lo};
+  for (int i = 0; i < 6 && T > 0; ++i) {
+    if (!ptrs[i] && i < 5) return fail(CP_ERR_INVALID_ARG, "a tensor pointer is NULL");
+    if (ptrs[i] && (reinterpret_cast<uintptr_t>(ptrs[i]) & 15u))
+      return fail(CP_ERR_ALIGNMENT, "tensor pointers must be 16-byte aligned");
+  }
+  Problem pb;
+  std::string err = make_problem(cu, n_seqs, N, P, T, &pb);
+  if (!err.empty()) return fail(CP_ERR_SHAPE, err);
+  if (T == 0) return CP_OK;
+  const bool bf16 = dt == CP_BF16;
+  FwdPlan plan;
+  plan_forward(pb, true, &plan);
+  std::vector<int32_t> samples;
+  int64_t ord = 0;
+  for (int i = 0; i < n_seqs; ++i) {
+    samples.insert(samples.end(), {pb.cu[i] + N, pb.c[i], pb.off[i], (int32_t)ord});
+    ord += 2LL * P * pb.c[i];
+  }
+  // layout inside the fixed scratch
+  const size_t elem = bf16 ? 2 : 4;
+  size_t o = 0;
+  const size_t o_status = o; o += kStatusBytes;
+  const size_t o_items = o; o = up256(o + plan.items.size() * sizeof(FwdItem));
+  const size_t o_samples = o; o = up256(o + samples.size() * sizeof(int32_t));
+  const size_t o_idx = o; o = up256(o + (size_t)pb.text_rows * sizeof(int32_t));
+  size_t o_qkv[3];
+  for (int i = 0; i < 3; ++i) { o_qkv[i] = o; o = up256(o + (size_t)pb.text_rows * H * d * elem); }
+  const size_t o_run = o; o = up256(o + (size_t)pb.text_rows * H * d * sizeof(float));
+  const size_t o_lrun = o; o = up256(o + (size_t)pb.text_rows * H * sizeof(float));
+  if (o > kScratchBytes) {
+    char buf[160];
+    snprintf(buf, sizeof buf,
+             "this problem needs %zu bytes of scratch; the fixed scratch holds %zu (use cp_attn_fwd "
+             "with a workspace)", o, kScratchBytes);
+    return fail(CP_ERR_WORKSPACE, buf);
+  }
+  if (bf16) {
+    int dev = 0, major = 0, minor = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    if (major != 10 || minor != 3)
+      return fail(CP_ERR_UNSUPPORTED, "the bf16 path is built for sm_103a (compute capability 10.3)");
+  }
+  void* base = nullptr;
+  cp_status_t s = scratch_address(&base);
+  if (s != CP_OK) return s;
+  char* w = static_cast<char*>(base);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+#define NA_CUDA(call, what)                                                              \
+  do {                                                                                   \
+    cudaError_t e_ = (call);                                                             \
+    if (e_ != cudaSuccess) return fail(CP_ERR_CUDA, std::string(what) + ": " + cudaGetErrorString(e_)); \
+  } while (0)
+  // the status word must start at zero; everything else is written before it is read
+  NA_CUDA(cudaMemsetAsync(w + o_status, 0, kStatusBytes, st), "clear status");
+  NA_CUDA(cudaMemcpyAsync(w + o_items, plan.items.data(), plan.items.size() * sizeof(FwdItem),
+                          cudaMemcpyHostToDevice, st),
+          "upload work list");
+  NA_CUDA(cudaMemcpyAsync(w + o_samples, samples.data(), samples.size() * sizeof(int32_t),
+                          cudaMemcpyHostToDevice, st),
+          "upload sample table");
+  int32_t* idx = reinterpret_cast<int32_t*>(w + o_idx);
+  NA_CUDA(launch_zigzag_index(reinterpret_cast<const int32_t*>(w + o_samples), n_seqs, P, pb.R,
+                              idx, nullptr, st),
+          "zigzag index kernel");
+  const void* src[3] = {q, k, v};
+  void* dst[3] = {w + o_qkv[0], w + o_qkv[1], w + o_qkv[2]};
+  NA_CUDA(launch_gather_rows(src, dst, 3, (size_t)H * d * elem, idx, (int)pb.text_rows, false, st),
+          "zigzag gather");
+  const FwdItem* items = reinterpret_cast<const FwdItem*>(w + o_items);
+  float* orun = reinterpret_cast<float*>(w + o_run);
+  float* lrun = reinterpret_cast<float*>(w + o_lrun);
+  if (bf16) {
+    TcFwdArgs a;
+    const char* terr = nullptr;
+    const int64_t PR = pb.text_rows;
+    const bool ok = make_tmap_thd(&a.tm_q_text, dst[0], PR, H, d, 128, &terr) &&
+                    make_tmap_thd(&a.tm_k_text, dst[1], PR, H, d, 128, &terr) &&
+                    make_tmap_thd(&a.tm_v_text, dst[2], PR, H, d, 128, &terr) &&
+                    make_tmap_thd(&a.tm_q_nat, q, T, H, d, 128, &terr) &&
+                    make_tmap_thd(&a.tm_k_nat, k, T, H, d, 128, &terr) &&
+                    make_tmap_thd(&a.tm_v_nat, v, T, H, d, 128, &terr);
+    if (!ok) return fail(CP_ERR_CUDA, std::string("tensor map: ") + (terr ? terr : "?"));
+    a.H = H; a.d = d;
+    a.scale_log2 = scale * 1.4426950408889634f;
+    a.o_run = orun; a.lse_run = lrun; a.run_rows = PR;
+    a.out = out; a.lse = lse; a.T = T; a.out_lo = out_lo;
+    a.status = reinterpret_cast<int32_t*>(w + o_status);
+    a.wait_limit = device_wait_limit();
+    for (int step = 0; step < P; ++step) {
+      a.items = items + plan.step_begin[step];
+      a.n_items = plan.step_begin[step + 1] - plan.step_begin[step];
+      NA_CUDA(launch_tc_fwd(a, st), "tensor-core ring step");
+    }
+    return CP_OK;
+  }
+  SimtFwdArgs a;
+  a.q_text = dst[0]; a.k_text = dst[1]; a.v_text = dst[2];
+  a.q_nat = q; a.k_nat = k; a.v_nat = v;
+  a.H = H; a.d = d; a.scale = scale;
+  a.o_run = orun; a.lse_run = lrun; a.run_rows = pb.text_rows;
+  a.out = out; a.lse = lse; a.T = T;
+  for (int step = 0; step < P; ++step) {
+    a.items = items + plan.step_begin[step];
+    a.n_items = plan.step_begin[step + 1] - plan.step_begin[step];
+    NA_CUDA(launch_simt_fwd(a, false, st), "ring step");
+  }
+#undef NA_CUDA
+  return CP_OK;
+}
