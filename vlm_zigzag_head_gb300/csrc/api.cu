@@ -547,7 +547,8 @@ cp_status_t cp_attn_bwd(const void* q, const void* k, const void* v, const void*
               make_tmap_thd(&a.tm_k, k, T, H, d, kBwdTileK, &terr) &&
               make_tmap_thd(&a.tm_v, v, T, H, d, kBwdTileK, &terr) &&
               make_tmap_thd(&a.tm_do, dout, T, H, d, kBwdTileQ, &terr) &&
-              make_tmap_ld(&a.tm_ld, lse2, pitch, H, kBwdTileQ + 4, &terr);
+              make_tmap_ld(&a.tm_ld, lse2, pitch, H, kBwdTileQ + 4, &terr) &&
+              make_tmap_f32_thd(&a.tm_dq, dq, T, H, d, 16, &terr);
     if (!ok) return fail(CP_ERR_CUDA, std::string("tensor map: ") + (terr ? terr : "?"));
     a.H = H; a.d = d; a.scale = scale; a.scale_log2 = scale * 1.4426950408889634f;
     a.T = T;

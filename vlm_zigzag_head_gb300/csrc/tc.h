@@ -12,6 +12,10 @@ namespace cpattn {
 // 128-byte swizzle.  Returns false (and a message) if encoding fails.
 bool make_tmap_thd(CUtensorMap* map, const void* base, int64_t rows, int H, int d,
                    int rows_per_box, const char** err);
+// 3-D tensor map over an fp32 [rows][H][d] tensor, box {d, 1, box_rows}, no
+// swizzle (the dQ reduce-add target of the backward).
+bool make_tmap_f32_thd(CUtensorMap* map, void* base, int64_t rows, int H, int d, int box_rows,
+                       const char** err);
 // 3-D tensor map over the fp32 planes [2][H][pitch] (lse2, D) of the backward
 // preprocess, box {box_rows, 1, 2}; pitch must be a multiple of 4.
 bool make_tmap_ld(CUtensorMap* map, const void* base, int64_t pitch, int H, int box_rows,
@@ -34,6 +38,7 @@ cudaError_t launch_tc_fwd(const TcFwdArgs& a, cudaStream_t st);
 struct TcBwdArgs {
   CUtensorMap tm_q, tm_k, tm_v, tm_do;  // natural order
   CUtensorMap tm_ld;                     // [2][H][pitch] fp32: lse2, D
+  CUtensorMap tm_dq;                     // dq fp32 [T][H][d], box {d, 1, 16}: reduce-add target
   const BwdItem* items;
   int n_items, H, d;
   float scale, scale_log2;

@@ -16,13 +16,14 @@
 // dQ values are large enough that one bf16 rounding of dS would dominate the
 // error.  dK and dV use the single bf16 rounding of dS^T and P^T.
 //
-// Warp roles (384 threads; TMEM lane quarter of warp w is w % 4):
+// Warp roles (512 threads; TMEM lane quarter of warp w is w % 4):
 //   warp 0       TMA producer (K, V once; Q, dO and the lse2 / D rows per query
 //                tile, 3 stages)
 //   warp 1       TMEM allocation; lane 0 issues every tcgen05.mma
 //   warps 2, 3   idle
-//   warps 4..7   P / dS computation, then the dK / dV epilogue; thread = key row
-//   warps 8..11  dQ drain; thread = head-dim index (TMEM lane of dQ^T)
+//   warps 4..11  P / dS computation (two warpgroups, 32 query columns each),
+//                then the dK / dV epilogue; thread = key row
+//   warps 12..15 dQ drain; thread = head-dim index (TMEM lane of dQ^T)
 //
 // TMEM columns: S^T [0,64), dP^T [64,128), dQ^T ping-pong [128,192) and
 // [192,256), dK [256,384), dV [384,512).
@@ -40,7 +41,7 @@ namespace {
 
 using namespace ptx;
 
-constexpr int kThreads = 384;
+constexpr int kThreads = 512;
 constexpr int kD = 128;            // head dim of this kernel
 constexpr int kBK = kBwdTileK;     // 128 keys
 constexpr int kBQ = kBwdTileQ;     // 64 queries per inner tile
@@ -52,24 +53,30 @@ constexpr uint32_t kColS = 0, kColDP = 64, kColDQ0 = 128, kColDQ1 = 192, kColDK 
 constexpr long long kDrainLimit = 1LL << 24;
 constexpr float kSplitScale = 0.25f;  // softmax scales above this use the dS hi + lo split
 
-struct L {
+template <bool kSplit>
+struct Lay {
   static constexpr int kKVBox = 128 * 128;   // 128 rows x 128 bytes
   static constexpr int kQBox = kBQ * 128;    // 64 rows x 128 bytes
   static constexpr int kLdBytes = 2 * kLdRows * 4;
+  static constexpr int kNumStg = kSplit ? 1 : 2;          // dQ staging buffers
+  static constexpr int kStgRows = 16;                     // query rows per dQ reduce-add
+  static constexpr int kStgBytes = kStgRows * kD * 4;     // 8 KB
   static constexpr int kK = 0;
   static constexpr int kV = kK + 2 * kKVBox;
   static constexpr int kQ = kV + 2 * kKVBox;              // [stage][2 boxes]
   static constexpr int kDO = kQ + kStages * 2 * kQBox;
   static constexpr int kP = kDO + kStages * 2 * kQBox;     // 128 x 64 bf16
   static constexpr int kDS = kP + kKVBox;                 // bf16(dS^T)
-  static constexpr int kDSL = kDS + kKVBox;               // bf16(dS^T - bf16(dS^T))
-  static constexpr int kLd = kDSL + kKVBox;               // [stage] {lse2[68], D[68]}
+  static constexpr int kDSL = kDS + kKVBox;               // bf16(dS^T - bf16(dS^T)), split only
+  static constexpr int kStg = kDSL + (kSplit ? kKVBox : 0);  // [buf][16][128] fp32 dQ staging
+  static constexpr int kLd = kStg + kNumStg * kStgBytes;  // [stage] {lse2[68], D[68]}
   static constexpr int kItem = kLd + kStages * 1024;
   static constexpr int kBars = kItem + 128;
   static constexpr int kBytes = kBars + 512;
   static constexpr int kAlloc = kBytes + 1024;
 };
-static_assert(L::kAlloc <= 227 * 1024, "shared memory budget");
+static_assert(Lay<true>::kAlloc <= 227 * 1024, "shared memory budget");
+static_assert(Lay<false>::kAlloc <= 227 * 1024, "shared memory budget");
 
 struct Bars {
   uint64_t kv_full;
@@ -78,6 +85,7 @@ struct Bars {
   uint64_t ps_full, ps_empty;
   uint64_t dq_full[2], dq_empty[2];
   uint64_t dkv_done;
+  uint64_t stg_full[2], stg_free[2];   // dQ staging buffers (drain warps / elected thread)
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
@@ -114,6 +122,7 @@ __device__ __forceinline__ void record_timeout(int32_t* status, volatile int* ab
 
 template <bool kSplit>
 __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_constant__ TcBwdArgs a) {
+  using L = Lay<kSplit>;
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte aligned base, derived from the shared array itself so that the
   // compiler keeps shared-space (not generic) loads and stores
@@ -141,9 +150,13 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
     mbar_init(&bars->ps_empty, 1);
     for (int b = 0; b < 2; ++b) {
       mbar_init(&bars->dq_full[b], 1);
-      mbar_init(&bars->dq_empty[b], 8);
+      mbar_init(&bars->dq_empty[b], 4);
     }
     mbar_init(&bars->dkv_done, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&bars->stg_full[b], 4);
+      mbar_init(&bars->stg_free[b], 1);
+    }
     mbar_init(&bars->drain, 1);
     bars->abort = 0;
     fence_mbar_init();
@@ -299,62 +312,77 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
         mbar_wait(&bars->drain, 0, kDrainLimit, &zero);
       }
     }
-  } else if (warp >= 4) {
-    // ------------------------------------------------------------ P / dS, dQ drain
-    // Two warpgroups share every query tile: warpgroup g (warps 4+4g .. 7+4g)
-    // computes P^T / dS^T for query columns [32g, 32g + 32) of its key rows,
-    // then drains the same columns of the previous tile's dQ^T.
-    const int g = (warp - 4) >> 2;
-    const int u = (warp & 3) * 32 + lane;        // key row (and head-dim index for dQ^T)
+  } else if (warp >= 12) {
+    // ------------------------------------------------------------ dQ drain
+    // thread = head-dim index (warp & 3) * 32 + lane == TMEM lane of dQ^T.
+    // Each tile's dQ^T goes out in four rounds of 16 query columns: the four
+    // warps stage them as fp32 [16 rows][128] in shared memory and one elected
+    // thread adds the block into dQ with a bulk tensor reduce (the reduction
+    // runs in L2; no per-thread atomics).
+    const int dd = (warp & 3) * 32 + lane;
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
-    const float sl2 = a.scale_log2;
-    const bool key_ok = u < it.k_len;
+    const bool elected = warp == 12 && lane == 0;
+    constexpr int N = L::kNumStg;
     bool ok = true;
-    auto drain = [&](int j) -> bool {             // dQ^T columns of tile j, this half
+    int k = 0;                                   // round counter
+    for (int j = 0; ok && j < n_qt; ++j) {
       Seg sgd;
       int q0d, td;
       tile_of(it, (j + rot) % n_qt, sgd, q0d, td);
       const int b = j & 1;
-      if (!mbar_wait(&bars->dq_full[b], (j >> 1) & 1, lim, abort)) return false;
+      if (!mbar_wait(&bars->dq_full[b], (j >> 1) & 1, lim, abort)) { ok = false; break; }
       tc_fence_after();
-      uint32_t r[32];
-      tmem_ld32(tmem + lane_off + (b ? kColDQ1 : kColDQ0) + g * 32, r);
-      tmem_ld_wait();
-      reg_fence32(r);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->dq_empty[b]);
-      // quad transpose: lane 4k+i receives head dims 4k..4k+3 of query column
-      // 4c+i, so every atomic is a 16-byte vector
-      const int row0 = q0d + td * kBQ + g * 32;  // first query (inside the run) of this half
-      const int nrow = sgd.len - row0;
-      const long long stride = (long long)a.H * kD;
-      float* base = a.dq + ((long long)(sgd.row0 + row0) * a.H + h) * kD + (warp & 3) * 32 +
-                    (lane & ~3);
-      const bool b0 = lane & 1, b1 = lane & 2;
+      const int grow = sgd.row0 + q0d + td * kBQ;  // natural row of the tile's first query
+      for (int half = 0; ok && half < 2; ++half) {
+        uint32_t r[32];
+        tmem_ld32(tmem + lane_off + (b ? kColDQ1 : kColDQ0) + half * 32, r);
+        tmem_ld_wait();
+        reg_fence32(r);
+        if (half == 1) {                         // all of this tile's dQ^T is in registers
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars->dq_empty[b]);
+        }
+        for (int rr = 0; rr < 2; ++rr, ++k) {
+          const int sb = k % N;
+          if (k >= N && !mbar_wait(&bars->stg_free[sb], ((k / N) - 1) & 1, lim, abort)) {
+            ok = false;
+            break;
+          }
+          float* stg = reinterpret_cast<float*>(smem + L::kStg + sb * L::kStgBytes);
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        float v0 = __uint_as_float(r[4 * c]) * a.scale, v1 = __uint_as_float(r[4 * c + 1]) * a.scale;
-        float v2 = __uint_as_float(r[4 * c + 2]) * a.scale, v3 = __uint_as_float(r[4 * c + 3]) * a.scale;
-        float s0 = b0 ? v0 : v1, s1 = b0 ? v2 : v3;
-        s0 = __shfl_xor_sync(0xffffffffu, s0, 1);
-        s1 = __shfl_xor_sync(0xffffffffu, s1, 1);
-        if (b0) { v0 = s0; v2 = s1; } else { v1 = s0; v3 = s1; }
-        s0 = b1 ? v0 : v2;
-        s1 = b1 ? v1 : v3;
-        s0 = __shfl_xor_sync(0xffffffffu, s0, 2);
-        s1 = __shfl_xor_sync(0xffffffffu, s1, 2);
-        if (b1) { v0 = s0; v1 = s1; } else { v2 = s0; v3 = s1; }
-        const int x = 4 * c + (lane & 3);        // query column inside this half
-        if (x < nrow) {
-          float* p = base + x * stride;
-          asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(v0),
-                       "f"(v1), "f"(v2), "f"(v3)
-                       : "memory");
+          for (int x = 0; x < L::kStgRows; ++x)
+            stg[x * kD + dd] = __uint_as_float(r[rr * 16 + x]) * a.scale;
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars->stg_full[sb]);
+          if (elected) {
+            if (!mbar_wait(&bars->stg_full[sb], (k / N) & 1, lim, abort)) {
+              ok = false;
+              break;
+            }
+            // rows past the run carry exact zeros (P = 0 there); rows past T are
+            // clipped by the tensor map
+            tma_reduce_add_3d(&a.tm_dq, stg, 0, h, grow + half * 32 + rr * 16);
+            bulk_commit();
+            bulk_wait_read<N - 1>();             // the buffer of round k + 1 is readable again
+            if (k + 1 >= N) mbar_arrive(&bars->stg_free[(k + 1) % N]);
+          }
         }
       }
-      return true;
-    };
+    }
+    if (elected) bulk_wait_all();                // every reduce-add finished before exit
+    if (!ok) record_timeout(a.status, abort, 14);
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ P / dS
+    // Two warpgroups share every query tile: warpgroup g (warps 4+4g .. 7+4g)
+    // computes P^T / dS^T for query columns [32g, 32g + 32) of its key rows.
+    const int g = (warp - 4) >> 2;
+    const int u = (warp & 3) * 32 + lane;        // key row == TMEM lane
+    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+    const float sl2 = a.scale_log2;
+    const bool key_ok = u < it.k_len;
+    bool ok = true;
     for (int i = 0; ok && i < n_qt; ++i) {
       Seg sg;
       int q0, t;
@@ -430,12 +458,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars->ps_full);
-      if (i >= 1 && !drain(i - 1)) {
-        ok = false;
-        break;
-      }
     }
-    if (ok && n_qt > 0 && !drain(n_qt - 1)) ok = false;
     // ------------------------------------------------------------ dK / dV epilogue
     if (ok && n_qt > 0 && !mbar_wait(&bars->dkv_done, 0, lim, abort)) ok = false;
     if (!ok) {
@@ -489,12 +512,13 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
 
 template <bool kSplit>
 cudaError_t launch_split(const TcBwdArgs& a, cudaStream_t st) {
+  constexpr int smem = Lay<kSplit>::kAlloc;
   cudaError_t e = cudaFuncSetAttribute(tc_bwd_kernel<kSplit>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const long long blocks = (long long)a.n_items * a.H;
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  tc_bwd_kernel<kSplit><<<(unsigned)blocks, kThreads, L::kAlloc, st>>>(a);
+  tc_bwd_kernel<kSplit><<<(unsigned)blocks, kThreads, smem, st>>>(a);
   return cudaGetLastError();
 }
 

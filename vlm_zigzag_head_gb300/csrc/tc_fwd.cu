@@ -7,12 +7,17 @@
 // a fused log-sum-exp merge into the fp32 running result (or the final write
 // in natural order).
 //
-// Warp roles (256 threads):
-//   warp 0      TMA producer of Q and K tiles
-//   warp 1      TMEM allocation; lane 0 issues every tcgen05.mma
-//   warp 2      TMA producer of V tiles
-//   warp 3      idle
-//   warps 4..7  softmax and epilogue; thread t owns query row t (TMEM lane t)
+// Warp roles (384 threads; TMEM lane quarter of warp w is w % 4):
+//   warp 0       TMA producer of Q and K tiles
+//   warp 1       TMEM allocation; lane 0 issues every tcgen05.mma
+//   warp 2       TMA producer of V tiles
+//   warp 3       idle
+//   warps 4..7   softmax of key columns 0..63 of every S tile, then the
+//                epilogue of O columns [0, D/2); thread = query row = TMEM lane
+//   warps 8..11  the same for key columns 64..127 and O columns [D/2, D)
+// The two warps that share a query row exchange their partial row maxima
+// (and, at the end, their partial row sums) through shared memory; a per-pair
+// mbarrier (bounded waits, like every other wait here) orders the exchange.
 //
 // TMEM (512 columns): S ping-pong buffers at columns [0,128) and [128,256),
 // the O accumulator at [256, 256 + D).  Shared memory: Q (128 x D), two K and
@@ -30,7 +35,7 @@ namespace {
 
 using namespace ptx;
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 384;
 constexpr int kBM = kFwdTileQ;   // 128 query rows
 constexpr int kBN = kFwdTileK;   // 128 keys per KV tile
 constexpr int kStages = 2;
@@ -47,7 +52,8 @@ struct Smem {
   static constexpr int kK = kQ + kTile;
   static constexpr int kV = kK + kStages * kTile;
   static constexpr int kP = kV + kStages * kTile;
-  static constexpr int kBars = kP + kBM * kBN * 2;
+  static constexpr int kXch = kP + kBM * kBN * 2;       // [parity][half][128] float exchange
+  static constexpr int kBars = kXch + 4 * kBM * 4;
   static constexpr int kBytes = kBars + 256;
   static constexpr int kAlloc = kBytes + 1024;     // slack for 1024-byte alignment
 };
@@ -59,6 +65,7 @@ struct Bars {
   uint64_t s_full[2], s_empty[2];
   uint64_t p_full, o_done;
   uint64_t drain;
+  uint64_t pair[4];   // the two softmax warps of each TMEM lane quarter
   uint32_t tmem_base;
   int abort;
 };
@@ -103,11 +110,12 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&bars->s_full[b], 1);
-      mbar_init(&bars->s_empty[b], 4);
+      mbar_init(&bars->s_empty[b], 8);
     }
-    mbar_init(&bars->p_full, 4);
+    mbar_init(&bars->p_full, 8);
     mbar_init(&bars->o_done, 1);
     mbar_init(&bars->drain, 1);
+    for (int q = 0; q < 4; ++q) mbar_init(&bars->pair[q], 2);
     bars->abort = 0;
     fence_mbar_init();
   }
@@ -232,13 +240,25 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
     }
   } else if (warp >= 4) {
     // ------------------------------------------------------------ softmax
-    const int t = threadIdx.x - 128;           // query row == TMEM lane
-    const uint32_t lane_off = (uint32_t)((warp - 4) * 32) << 16;
+    const int g = (warp - 4) >> 2;             // key-column half of S / O-column half
+    const int t = (warp & 3) * 32 + lane;      // query row == TMEM lane
+    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+    uint64_t* pair = &bars->pair[warp & 3];
+    float* xch = reinterpret_cast<float*>(smem + L::kXch);  // [parity][half][128]
+    // exchange a per-row value with the partner warp; phase k of the pair barrier
+    auto exchange = [&](float v, int k, float* partner) -> bool {
+      xch[((k & 1) * 2 + g) * kBM + t] = v;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(pair);
+      if (!mbar_wait(pair, k & 1, lim, abort)) return false;
+      *partner = xch[((k & 1) * 2 + (1 - g)) * kBM + t];
+      return true;
+    };
     const float sl2 = a.scale_log2;
     float m = -INFINITY;   // running max of scaled scores (log2 units), may lag
-    float l = 0.f;
+    float l = 0.f;         // partial row sum over this thread's columns
     bool ok = true;
-    uint8_t* p_smem = smem + L::kP;
+    uint8_t* p_smem = smem + L::kP + g * L::kBox;
     int j = 0;
     for (int s = 0; ok && s < nseg; ++s) {
       const Seg sg = it.seg[s];
@@ -247,41 +267,44 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
         const int sb = j & 1;
         if (!mbar_wait(&bars->s_full[sb], (j >> 1) & 1, lim, abort)) { ok = false; break; }
         tc_fence_after();
-        float x[kBN];
+        constexpr int kH = kBN / 2;              // 64 columns per thread
+        float x[kH];
         {
-          // four 32-column loads in flight, one wait
-          uint32_t r[kBN];
-          const uint32_t s_col = tmem + lane_off + (sb ? kColS1 : kColS0);
+          uint32_t r[kH];
+          const uint32_t s_col = tmem + lane_off + (sb ? kColS1 : kColS0) + g * kH;
 #pragma unroll
-          for (int c = 0; c < kBN / 32; ++c)
+          for (int c = 0; c < kH / 32; ++c)
             tmem_ld32(s_col + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&r[c * 32]));
           tmem_ld_wait();
 #pragma unroll
-          for (int c = 0; c < kBN / 32; ++c)
+          for (int c = 0; c < kH / 32; ++c)
             reg_fence32(*reinterpret_cast<uint32_t(*)[32]>(&r[c * 32]));
 #pragma unroll
-          for (int c = 0; c < kBN; ++c) x[c] = __uint_as_float(r[c]) * sl2;
+          for (int c = 0; c < kH; ++c) x[c] = __uint_as_float(r[c]) * sl2;
         }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars->s_empty[sb]);
         // mask: key u = u0 + c visible iff u < len and (!causal or u <= t + delta)
-        const int u0 = tt * kBN;
-        const bool full = (u0 + kBN <= sg.len) && (!sg.causal || u0 + kBN - 1 <= sg.delta);
+        const int u0 = tt * kBN + g * kH;
+        const bool full = (u0 + kH <= sg.len) && (!sg.causal || u0 + kH - 1 <= sg.delta);
         if (!full) {
           const int lim_u = sg.causal ? min(sg.len, t + sg.delta + 1) : sg.len;
 #pragma unroll
-          for (int c = 0; c < kBN; ++c)
+          for (int c = 0; c < kH; ++c)
             if (u0 + c >= lim_u) x[c] = -INFINITY;
         }
-        // row max with 8 independent partial maxima (short dependency chains)
         float mp[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) mp[i] = x[i];
 #pragma unroll
-        for (int c = 8; c < kBN; ++c) mp[c & 7] = fmaxf(mp[c & 7], x[c]);
-        const float mt = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
-                               fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
+        for (int c = 8; c < kH; ++c) mp[c & 7] = fmaxf(mp[c & 7], x[c]);
+        float mt = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
+                         fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
+        // combine with the partner half of the row (same value in both threads)
+        float mo;
+        if (!exchange(mt, j, &mo)) { ok = false; break; }
+        mt = fmaxf(mt, mo);
         const float m_new = fmaxf(m, mt);
         const bool need = m_new > m + kRescaleThreshold || (m == -INFINITY && m_new != -INFINITY);
         if (__any_sync(0xffffffffu, need)) {
@@ -290,18 +313,19 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
             l *= alpha;
             m = m_new;
           }
-          if (j > 0) {  // O holds PV of earlier tiles: wait for the last, rescale
+          if (j > 0) {  // O holds PV of earlier tiles: wait for the last, rescale our half
             if (!mbar_wait(&bars->o_done, (j - 1) & 1, lim, abort)) { ok = false; break; }
             tc_fence_after();
 #pragma unroll 1
-            for (int c = 0; c < D / 32; ++c) {
+            for (int c = 0; c < D / 64; ++c) {
               uint32_t r[32];
-              tmem_ld32(tmem + lane_off + kColO + c * 32, r);
+              const uint32_t col = tmem + lane_off + kColO + g * (D / 2) + c * 32;
+              tmem_ld32(col, r);
               tmem_ld_wait();
               reg_fence32(r);
 #pragma unroll
               for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
-              tmem_st32(tmem + lane_off + kColO + c * 32, r);
+              tmem_st32(col, r);
             }
             tmem_st_wait();
           }
@@ -311,23 +335,22 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
 #pragma unroll
         for (int i = 0; i < 8; ++i) sp[i] = 0.f;
 #pragma unroll
-        for (int c = 0; c < kBN; ++c) {
+        for (int c = 0; c < kH; ++c) {
           x[c] = ex2(x[c] - mu);
           sp[c & 7] += x[c];
         }
         l += ((sp[0] + sp[1]) + (sp[2] + sp[3])) + ((sp[4] + sp[5]) + (sp[6] + sp[7]));
         // P buffer is free once the PV of the previous tile has completed
         if (j > 0 && !mbar_wait(&bars->o_done, (j - 1) & 1, lim, abort)) { ok = false; break; }
-        // P row t, 128-byte swizzle: 16-byte chunk q of a 128-byte row -> q ^ (t & 7)
+        // P row t, this half's 64 columns = one 128-byte swizzled box row
 #pragma unroll
-        for (int c = 0; c < kBN / 8; ++c) {
+        for (int c = 0; c < kH / 8; ++c) {
           uint4 v;
           v.x = pack_bf16x2(x[c * 8 + 0], x[c * 8 + 1]);
           v.y = pack_bf16x2(x[c * 8 + 2], x[c * 8 + 3]);
           v.z = pack_bf16x2(x[c * 8 + 4], x[c * 8 + 5]);
           v.w = pack_bf16x2(x[c * 8 + 6], x[c * 8 + 7]);
-          const int half = c >> 3, q = c & 7;
-          *reinterpret_cast<uint4*>(p_smem + half * L::kBox + t * 128 + ((q ^ (t & 7)) << 4)) = v;
+          *reinterpret_cast<uint4*>(p_smem + t * 128 + ((c ^ (t & 7)) << 4)) = v;
         }
         fence_proxy_async_smem();
         tc_fence_before();
@@ -337,6 +360,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
     }
     // ------------------------------------------------------------ epilogue
     if (ok && n_tiles > 0 && !mbar_wait(&bars->o_done, (n_tiles - 1) & 1, lim, abort)) ok = false;
+    // the row's two partial sums
+    float lo_part = 0.f;
+    if (ok && !exchange(l, n_tiles, &lo_part)) ok = false;
+    l += lo_part;
     if (!ok) {
       record_timeout(a.status, abort, 5);
     } else {
@@ -358,16 +385,17 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
           lse_s = mm + logf(tot);
         }
       }
-      const float* orun = a.o_run + rrow * D;
-      float* orun_w = a.o_run + rrow * D;
-      const long long out_off = ((long long)(it.out_row0 + t) * a.H + h) * D;
+      const int c0 = g * (D / 2);               // this thread's O columns
+      const float* orun = a.o_run + rrow * D + c0;
+      float* orun_w = a.o_run + rrow * D + c0;
+      const long long out_off = ((long long)(it.out_row0 + t) * a.H + h) * D + c0;
       __nv_bfloat16* outp = reinterpret_cast<__nv_bfloat16*>(a.out) + out_off;
       __nv_bfloat16* lop =
           a.out_lo ? reinterpret_cast<__nv_bfloat16*>(a.out_lo) + out_off : nullptr;
 #pragma unroll 1
-      for (int c = 0; c < D / 32; ++c) {
+      for (int c = 0; c < D / 64; ++c) {
         uint32_t r[32];
-        tmem_ld32(tmem + lane_off + kColO + c * 32, r);
+        tmem_ld32(tmem + lane_off + kColO + c0 + c * 32, r);
         tmem_ld_wait();
         reg_fence32(r);
         if (!valid) continue;
@@ -413,7 +441,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
                 make_float4(o[i], o[i + 1], o[i + 2], o[i + 3]);
         }
       }
-      if (valid) {
+      if (valid && g == 0) {
         if (flags & F_FINAL) a.lse[(long long)h * a.T + it.out_row0 + t] = lse_s;
         else a.lse_run[rrow] = lse_s;
       }
