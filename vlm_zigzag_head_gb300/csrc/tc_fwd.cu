@@ -20,9 +20,12 @@
 // mbarrier (bounded waits, like every other wait here) orders the exchange.
 //
 // TMEM (512 columns): S ping-pong buffers at columns [0,128) and [128,256),
-// the O accumulator at [256, 256 + D).  Shared memory: Q (128 x D), two K and
-// two V stages (128 x D each), P (128 x 128 bf16), all in the 128-byte
-// swizzled layout TMA writes, 1024-byte aligned.
+// the O accumulator at [256, 256 + D), Q as bf16 pairs at [384, 384 + D/2).
+// P (bf16) overwrites the S buffer it was computed from: the warp of key
+// half g writes its 64 probabilities at buffer columns [64g, 64g + 32).  Both
+// products read their A operand (Q, P) from TMEM and only B (K, V) from
+// shared memory.  Shared memory: Q (128 x D), two K and two V stages
+// (128 x D each), in the 128-byte swizzled layout TMA writes.
 #include <cuda_bf16.h>
 
 #include "kernels.h"
@@ -40,7 +43,7 @@ constexpr int kBM = kFwdTileQ;   // 128 query rows
 constexpr int kBN = kFwdTileK;   // 128 keys per KV tile
 constexpr int kStages = 2;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO = 256;
+constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO = 256, kColQ = 384;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: stale max may lag by 2^8
 constexpr long long kDrainLimit = 1LL << 24;
 
@@ -52,7 +55,7 @@ struct Smem {
   static constexpr int kK = kQ + kTile;
   static constexpr int kV = kK + kStages * kTile;
   static constexpr int kP = kV + kStages * kTile;
-  static constexpr int kXch = kP + kBM * kBN * 2;       // [parity][half][128] float exchange
+  static constexpr int kXch = kP;                       // [parity][half][128] float exchange
   static constexpr int kBars = kXch + 4 * kBM * 4;
   static constexpr int kBytes = kBars + 256;
   static constexpr int kAlloc = kBytes + 1024;     // slack for 1024-byte alignment
@@ -62,7 +65,8 @@ struct Bars {
   uint64_t q_full;
   uint64_t k_full[kStages], k_empty[kStages];
   uint64_t v_full[kStages], v_empty[kStages];
-  uint64_t s_full[2], s_empty[2];
+  uint64_t s_full[2];
+  uint64_t q_tmem;    // Q copied into TMEM by the softmax warps
   uint64_t p_full, o_done;
   uint64_t drain;
   uint64_t pair[4];   // the two softmax warps of each TMEM lane quarter
@@ -108,10 +112,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
       mbar_init(&bars->v_full[s], 1);
       mbar_init(&bars->v_empty[s], 1);
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&bars->s_full[b], 1);
-      mbar_init(&bars->s_empty[b], 8);
-    }
+    for (int b = 0; b < 2; ++b) mbar_init(&bars->s_full[b], 1);
+    mbar_init(&bars->q_tmem, 8);
     mbar_init(&bars->p_full, 8);
     mbar_init(&bars->o_done, 1);
     mbar_init(&bars->drain, 1);
@@ -186,9 +188,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
     if (lane == 0) {
       constexpr uint32_t idesc_qk = idesc_bf16(kBM, kBN, 0, 0);
       constexpr uint32_t idesc_pv = idesc_bf16(kBM, D, 0, 1);
-      const uint32_t q_addr = smem_u32(smem + L::kQ);
-      const uint32_t p_addr = smem_u32(smem + L::kP);
-      bool ok = n_tiles == 0 || mbar_wait(&bars->q_full, 0, lim, abort);
+      bool ok = n_tiles == 0 || mbar_wait(&bars->q_tmem, 0, lim, abort);
       if (!ok) record_timeout(a.status, abort, 3);
       auto issue_pv = [&](int i) -> bool {
         const int st = i % kStages;
@@ -196,11 +196,12 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
         if (!mbar_wait(&bars->v_full[st], (i / kStages) & 1, lim, abort)) return false;
         tc_fence_after();
         const uint32_t v_addr = smem_u32(smem + L::kV + st * L::kTile);
+        const uint32_t p_tmem = tmem + ((i & 1) ? kColS1 : kColS0);
 #pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk) {
-          const uint64_t ad = sdesc_sw128(p_addr + (kk / 4) * L::kBox + (kk % 4) * 32, 16, 1024);
+        for (int kk = 0; kk < kBN / 16; ++kk) {   // keys 16kk..: half kk/4, column (kk%4)*8
           const uint64_t bd = sdesc_sw128(v_addr + kk * 16 * 128, L::kBox, 1024);
-          mma_bf16(tmem + kColO, ad, bd, idesc_pv, (i > 0 || kk > 0) ? 1u : 0u);
+          mma_bf16_ts(tmem + kColO, p_tmem + (kk / 4) * 64 + (kk % 4) * 8, bd, idesc_pv,
+                      (i > 0 || kk > 0) ? 1u : 0u);
         }
         mma_commit(&bars->v_empty[st]);
         mma_commit(&bars->o_done);
@@ -208,8 +209,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
       };
       for (int j = 0; ok && j < n_tiles; ++j) {
         const int st = j % kStages, sb = j & 1;
-        if (!mbar_wait(&bars->k_full[st], (j / kStages) & 1, lim, abort) ||
-            (j >= 2 && !mbar_wait(&bars->s_empty[sb], ((j >> 1) - 1) & 1, lim, abort))) {
+        // the S buffer of tile j last held P_{j-2}, read by PV_{j-2}, issued
+        // (and so executed) before this product
+        if (!mbar_wait(&bars->k_full[st], (j / kStages) & 1, lim, abort)) {
           ok = false;
           break;
         }
@@ -217,10 +219,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
         const uint32_t k_addr = smem_u32(smem + L::kK + st * L::kTile);
         const uint32_t s_tmem = tmem + (sb ? kColS1 : kColS0);
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
+        for (int kk = 0; kk < D / 16; ++kk) {     // head dims 16kk..: Q columns 8kk..
           const uint32_t off = (kk / 4) * L::kBox + (kk % 4) * 32;
-          mma_bf16(s_tmem, sdesc_sw128(q_addr + off, 16, 1024),
-                   sdesc_sw128(k_addr + off, 16, 1024), idesc_qk, kk > 0 ? 1u : 0u);
+          mma_bf16_ts(s_tmem, tmem + kColQ + kk * 8, sdesc_sw128(k_addr + off, 16, 1024),
+                      idesc_qk, kk > 0 ? 1u : 0u);
         }
         mma_commit(&bars->k_empty[st]);
         mma_commit(&bars->s_full[sb]);
@@ -258,7 +260,27 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
     float m = -INFINITY;   // running max of scaled scores (log2 units), may lag
     float l = 0.f;         // partial row sum over this thread's columns
     bool ok = true;
-    uint8_t* p_smem = smem + L::kP + g * L::kBox;
+    // Q row t into TMEM (bf16 pairs): warp half g copies head dims [64g, 64g + 64)
+    if (n_tiles > 0) {
+      if (!mbar_wait(&bars->q_full, 0, lim, abort)) ok = false;
+      if (ok && g * 64 < D) {
+        uint32_t r[32];
+        const uint8_t* qrow = smem + L::kQ + g * L::kBox + t * 128;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const uint4 v = *reinterpret_cast<const uint4*>(qrow + ((c ^ (t & 7)) << 4));
+          r[c * 4 + 0] = v.x;
+          r[c * 4 + 1] = v.y;
+          r[c * 4 + 2] = v.z;
+          r[c * 4 + 3] = v.w;
+        }
+        tmem_st32(tmem + lane_off + kColQ + g * 32, r);
+        tmem_st_wait();
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->q_tmem);
+    }
     int j = 0;
     for (int s = 0; ok && s < nseg; ++s) {
       const Seg sg = it.seg[s];
@@ -282,9 +304,6 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
 #pragma unroll
           for (int c = 0; c < kH; ++c) x[c] = __uint_as_float(r[c]) * sl2;
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bars->s_empty[sb]);
         // mask: key u = u0 + c visible iff u < len and (!causal or u <= t + delta)
         const int u0 = tt * kBN + g * kH;
         const bool full = (u0 + kH <= sg.len) && (!sg.causal || u0 + kH - 1 <= sg.delta);
@@ -340,19 +359,15 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
           sp[c & 7] += x[c];
         }
         l += ((sp[0] + sp[1]) + (sp[2] + sp[3])) + ((sp[4] + sp[5]) + (sp[6] + sp[7]));
-        // P buffer is free once the PV of the previous tile has completed
-        if (j > 0 && !mbar_wait(&bars->o_done, (j - 1) & 1, lim, abort)) { ok = false; break; }
-        // P row t, this half's 64 columns = one 128-byte swizzled box row
+        // P (bf16 pairs) over this thread's own S columns: buffer columns
+        // [64g, 64g + 32); PV_j reads it from there
+        {
+          uint32_t pk[kH / 2];
 #pragma unroll
-        for (int c = 0; c < kH / 8; ++c) {
-          uint4 v;
-          v.x = pack_bf16x2(x[c * 8 + 0], x[c * 8 + 1]);
-          v.y = pack_bf16x2(x[c * 8 + 2], x[c * 8 + 3]);
-          v.z = pack_bf16x2(x[c * 8 + 4], x[c * 8 + 5]);
-          v.w = pack_bf16x2(x[c * 8 + 6], x[c * 8 + 7]);
-          *reinterpret_cast<uint4*>(p_smem + t * 128 + ((c ^ (t & 7)) << 4)) = v;
+          for (int c = 0; c < kH / 2; ++c) pk[c] = pack_bf16x2(x[2 * c], x[2 * c + 1]);
+          tmem_st32(tmem + lane_off + (sb ? kColS1 : kColS0) + g * 64, pk);
+          tmem_st_wait();
         }
-        fence_proxy_async_smem();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars->p_full);
