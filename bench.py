@@ -35,6 +35,11 @@ from vlm_zigzag_head_gb300 import workloads as W  # noqa: E402
 
 METRIC = "CP causal attention TFLOP/s fwd & fwd+bwd, % of GB300 BF16 tensor peak"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) per launch of the
+# backward ring-step kernel, mean over the 8 launches of one step, from one ncu
+# capture of this kernel on the named workload.  Set an entry to None when the
+# kernel changes until it is captured again.
+MEASURED_TRAFFIC = {"long": 14.48e9}
 
 
 def causal_pairs(w) -> int:
@@ -257,7 +262,8 @@ def run_cuda(args, w, rank, world, dist):
         roof = {"kernel": "tc_bwd_kernel (backward ring step)", "bound": "tensor",
                 "achieved": ach, "peak": peak_sus, "unit": "TFLOP/s", "frac": ach / peak_sus,
                 "peak_source": "%s bf16_tflops_sustained" % peak_src,
-                "traffic": args.traffic, "launch_ms": avg,
+                "traffic": (args.traffic if args.traffic is not None
+                            else MEASURED_TRAFFIC.get(w.name)), "launch_ms": avg,
                 "flops_per_launch": bwd_launch_flops}
     kernels = {}
     for k, (kms, n) in prof.items():

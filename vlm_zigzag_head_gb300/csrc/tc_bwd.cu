@@ -9,7 +9,8 @@
 //   S^T  = K Q^T            dP^T = V dO^T                      (TMEM)
 //   P^T  = exp2(S^T * scale*log2e - lse2),  dS^T = P^T (dP^T - D)   (registers)
 //   dV  += P^T dO           dK  += dS^T Q                      (TMEM, whole item)
-//   dQ^T = K^T dS^T  -> fp32 atomic adds into dQ (scaled)
+//   dQ^T = K^T dS^T  -> staged in shared memory, added into fp32 dQ (scaled)
+//                       by bulk tensor reduce-adds
 //
 // dS^T enters the dQ product as two bf16 terms, hi = bf16(dS^T) and
 // lo = bf16(dS^T - hi), accumulated in fp32: with a softmax scale of 1 the
