@@ -72,6 +72,7 @@ struct Lay {
   static constexpr int kStg = kDSL + (kSplit ? kKVBox : 0);  // [buf][16][128] fp32 dQ staging
   static constexpr int kLd = kStg + kNumStg * kStgBytes;  // [stage] {lse2[68], D[68]}
   static constexpr int kItem = kLd + kStages * 1024;
+  static_assert(kLd % 16 == 0 && (kLdRows * 4) % 16 == 0, "16-byte lse2 / D loads");
   static constexpr int kBars = kItem + 128;
   static constexpr int kBytes = kBars + 512;
   static constexpr int kAlloc = kBytes + 1024;
@@ -413,30 +414,57 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
       const int end_vis = key_ok ? sg.len - row0 : 0;
       const bool whole = __all_sync(0xffffffffu, first_vis <= 0 && end_vis >= 32);
       uint32_t pk[16], hk[16], lk[16];
-      auto compute = [&](auto masked) {
+      // lse2 / D of the 32 queries: every thread reads the same words, so
+      // 16-byte loads (when the tile starts on a 4-row boundary) cut the
+      // shared-memory wavefronts four-fold
+      auto compute = [&](auto masked, auto vec) {
 #pragma unroll
-        for (int x = 0; x < 32; x += 2) {
-          float p0 = ex2(fmaf(__uint_as_float(rs[x]), sl2, -ld[x]));
-          float p1 = ex2(fmaf(__uint_as_float(rs[x + 1]), sl2, -ld[x + 1]));
-          if (decltype(masked)::value) {
-            if (x < first_vis || x >= end_vis) p0 = 0.f;
-            if (x + 1 < first_vis || x + 1 >= end_vis) p1 = 0.f;
-          }
-          const float d0 = p0 * (__uint_as_float(rd[x]) - ld[kLdRows + x]);
-          const float d1 = p1 * (__uint_as_float(rd[x + 1]) - ld[kLdRows + x + 1]);
-          pk[x / 2] = pack_bf16x2(p0, p1);
-          if (kSplit) {
-            const float h0 = __bfloat162float(__float2bfloat16_rn(d0));
-            const float h1 = __bfloat162float(__float2bfloat16_rn(d1));
-            hk[x / 2] = pack_bf16x2(h0, h1);
-            lk[x / 2] = pack_bf16x2(d0 - h0, d1 - h1);
+        for (int x = 0; x < 32; x += 4) {
+          float l[4], dd[4];
+          if (decltype(vec)::value) {
+            const float4 l4 = *reinterpret_cast<const float4*>(ld + x);
+            const float4 d4 = *reinterpret_cast<const float4*>(ld + kLdRows + x);
+            l[0] = l4.x; l[1] = l4.y; l[2] = l4.z; l[3] = l4.w;
+            dd[0] = d4.x; dd[1] = d4.y; dd[2] = d4.z; dd[3] = d4.w;
           } else {
-            hk[x / 2] = pack_bf16x2(d0, d1);
+#pragma unroll
+            for (int y = 0; y < 4; ++y) {
+              l[y] = ld[x + y];
+              dd[y] = ld[kLdRows + x + y];
+            }
+          }
+#pragma unroll
+          for (int y = 0; y < 4; y += 2) {
+            float p0 = ex2(fmaf(__uint_as_float(rs[x + y]), sl2, -l[y]));
+            float p1 = ex2(fmaf(__uint_as_float(rs[x + y + 1]), sl2, -l[y + 1]));
+            if (decltype(masked)::value) {
+              if (x + y < first_vis || x + y >= end_vis) p0 = 0.f;
+              if (x + y + 1 < first_vis || x + y + 1 >= end_vis) p1 = 0.f;
+            }
+            const float d0 = p0 * (__uint_as_float(rd[x + y]) - dd[y]);
+            const float d1 = p1 * (__uint_as_float(rd[x + y + 1]) - dd[y + 1]);
+            pk[(x + y) / 2] = pack_bf16x2(p0, p1);
+            if (kSplit) {
+              const float h0 = __bfloat162float(__float2bfloat16_rn(d0));
+              const float h1 = __bfloat162float(__float2bfloat16_rn(d1));
+              hk[(x + y) / 2] = pack_bf16x2(h0, h1);
+              lk[(x + y) / 2] = pack_bf16x2(d0 - h0, d1 - h1);
+            } else {
+              hk[(x + y) / 2] = pack_bf16x2(d0, d1);
+            }
           }
         }
       };
-      if (whole) compute(std::integral_constant<bool, false>());
-      else compute(std::integral_constant<bool, true>());
+      using T_ = std::integral_constant<bool, true>;
+      using F_ = std::integral_constant<bool, false>;
+      const bool aligned = ((sg.row0 + q0 + t * kBQ) & 3) == 0;
+      if (aligned) {
+        if (whole) compute(F_(), T_());
+        else compute(T_(), T_());
+      } else {
+        if (whole) compute(F_(), F_());
+        else compute(T_(), F_());
+      }
       if (i >= 1 && !mbar_wait(&bars->ps_empty, (i - 1) & 1, lim, abort)) {
         ok = false;
         break;
