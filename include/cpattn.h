@@ -246,8 +246,11 @@ cp_status_t cp_workspace_status(const void* workspace, void* stream);
  * cp_plan_pairs -- host-only introspection of the ring-step work lists: for
  * every step s < P, the number of visible (query, key) pairs the forward and
  * the backward work lists cover (prefix-query pairs are part of step 0) and
- * the number of work items.  Any output may be NULL.  Needs no GPU.
- * Errors: CP_ERR_INVALID_ARG, CP_ERR_SHAPE.
+ * the number of work items.  Forward figures are those of the 256-query items
+ * of the tensor-core kernel; the 128-query items of the CUDA-core kernel are
+ * checked to cover the same pairs.  Any output may be NULL.  Needs no GPU.
+ * Errors: CP_ERR_INVALID_ARG, CP_ERR_SHAPE, CP_ERR_UNSUPPORTED (the two
+ * forward work lists disagree: an internal error).
  */
 cp_status_t cp_plan_pairs(const int32_t* cu_seqlens_h, int n_seqs, int prefix_len, int P,
                           int64_t* fwd_pairs, int64_t* bwd_pairs, int64_t* fwd_items,

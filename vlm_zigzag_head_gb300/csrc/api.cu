@@ -111,7 +111,8 @@ Stager& stager() {
 // ---------------------------------------------------------------------------
 struct PlanSet {
   Problem pb;
-  FwdPlan fwd;       // text rows in rank-local order
+  FwdPlan fwd;       // text rows in rank-local order, 128-row items (CUDA cores)
+  FwdPlan fwd2;      // text rows in rank-local order, 256-row items (tensor cores)
   FwdPlan fwd_nat;   // text rows in natural order (fp32 dQ pass)
   BwdPlan bwd;
   std::vector<int32_t> samples;  // [n][4]: t0, c, off, ord0 (index kernel)
@@ -145,6 +146,7 @@ cp_status_t get_plans(const int32_t* cu, int n_seqs, int N, int P, int T, int H,
   auto ps = std::make_shared<PlanSet>();
   ps->pb = pb;
   plan_forward(pb, true, &ps->fwd);
+  plan_forward(pb, true, &ps->fwd2, kFwdPairQ);
   plan_forward(pb, false, &ps->fwd_nat);
   plan_backward(pb, &ps->bwd);
   int64_t ord = 0;
@@ -403,8 +405,8 @@ cp_status_t cp_attn_fwd(const void* q, const void* k, const void* v, cp_dtype_t 
   char* w = static_cast<char*>(ws);
   const Problem& pb = ps->pb;
   CP_CUDA(cudaMemsetAsync(w + L.status, 0, kStatusBytes, st), "clear status");
-  CP_CUDA(stager().upload(w + L.items, ps->fwd.items.data(),
-                          ps->fwd.items.size() * sizeof(FwdItem), st),
+  const FwdPlan& fp = tc ? ps->fwd2 : ps->fwd;  // items of 256 (tensor cores) / 128 rows
+  CP_CUDA(stager().upload(w + L.items, fp.items.data(), fp.items.size() * sizeof(FwdItem), st),
           "upload work list");
   CP_CUDA(stager().upload(w + L.samples, ps->samples.data(), ps->samples.size() * 4, st),
           "upload sample table");
@@ -445,8 +447,8 @@ cp_status_t cp_attn_fwd(const void* q, const void* k, const void* v, cp_dtype_t 
     a.status = reinterpret_cast<int32_t*>(w + L.status);
     a.wait_limit = wait_limit();
     for (int step = 0; step < P; ++step) {
-      a.items = items + ps->fwd.step_begin[step];
-      a.n_items = ps->fwd.step_begin[step + 1] - ps->fwd.step_begin[step];
+      a.items = items + fp.step_begin[step];
+      a.n_items = fp.step_begin[step + 1] - fp.step_begin[step];
       ProfScope ps_(2, st);
       CP_CUDA(launch_tc_fwd(a, st), "tensor-core ring step");
     }
@@ -459,8 +461,8 @@ cp_status_t cp_attn_fwd(const void* q, const void* k, const void* v, cp_dtype_t 
   a.o_run = o_run; a.lse_run = lse_run; a.run_rows = pb.text_rows;
   a.out = out; a.lse = lse; a.T = T;
   for (int step = 0; step < P; ++step) {
-    a.items = items + ps->fwd.step_begin[step];
-    a.n_items = ps->fwd.step_begin[step + 1] - ps->fwd.step_begin[step];
+    a.items = items + fp.step_begin[step];
+    a.n_items = fp.step_begin[step + 1] - fp.step_begin[step];
     ProfScope ps_(6, st);
     CP_CUDA(launch_simt_fwd(a, bf16, st), "ring step");
   }
@@ -644,22 +646,30 @@ cp_status_t cp_plan_pairs(const int32_t* cu, int n_seqs, int N, int P, int64_t* 
   Problem pb;
   std::string err = make_problem(cu, n_seqs, N, P, -1, &pb);
   if (!err.empty()) return fail(CP_ERR_SHAPE, err);
-  FwdPlan f;
+  // forward: the 256-row items of the tensor-core kernel, checked against the
+  // 128-row items of the CUDA-core kernel (both must cover the same pairs)
+  FwdPlan f, f1;
   BwdPlan b;
-  plan_forward(pb, true, &f);
+  plan_forward(pb, true, &f, kFwdPairQ);
+  plan_forward(pb, true, &f1, kFwdTileQ);
   plan_backward(pb, &b);
-  for (int s = 0; s < P; ++s) {
-    int64_t fp = 0, bp = 0;
-    for (int x = f.step_begin[s]; x < f.step_begin[s + 1]; ++x) {
-      const FwdItem& it = f.items[x];
+  auto fwd_step_pairs = [](const FwdPlan& fp_, int s) {
+    int64_t n = 0;
+    for (int x = fp_.step_begin[s]; x < fp_.step_begin[s + 1]; ++x) {
+      const FwdItem& it = fp_.items[x];
       for (int t = 0; t < it.q_len; ++t)
         for (int g = 0; g < it.nseg; ++g) {
           const Seg& sg = it.seg[g];
-          int64_t vis = sg.causal ? std::min<int64_t>(sg.len, std::max<int64_t>(0, t + sg.delta + 1))
-                                  : sg.len;
-          fp += vis;
+          n += sg.causal ? std::min<int64_t>(sg.len, std::max<int64_t>(0, t + sg.delta + 1))
+                         : sg.len;
         }
     }
+    return n;
+  };
+  for (int s = 0; s < P; ++s) {
+    int64_t fp = fwd_step_pairs(f, s), bp = 0;
+    if (fp != fwd_step_pairs(f1, s))
+      return fail(CP_ERR_UNSUPPORTED, "forward work lists of 128- and 256-row items disagree");
     for (int x = b.step_begin[s]; x < b.step_begin[s + 1]; ++x) {
       const BwdItem& it = b.items[x];
       for (int u = 0; u < it.k_len; ++u)

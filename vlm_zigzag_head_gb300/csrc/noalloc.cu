@@ -85,7 +85,7 @@ extern "C" cp_status_t cp_attn_fwd_noalloc(const void* q, const void* k, const v
   if (T == 0) return CP_OK;
   const bool bf16 = dt == CP_BF16;
   FwdPlan plan;
-  plan_forward(pb, true, &plan);
+  plan_forward(pb, true, &plan, bf16 ? kFwdPairQ : kFwdTileQ);
   std::vector<int32_t> samples;
   int64_t ord = 0;
   for (int i = 0; i < n_seqs; ++i) {

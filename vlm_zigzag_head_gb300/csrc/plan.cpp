@@ -111,7 +111,7 @@ void zigzag_tables(const Problem& pb, int32_t* fwd_idx, int32_t* inv_idx) {
   }
 }
 
-void plan_forward(const Problem& pb, bool text_perm, FwdPlan* plan) {
+void plan_forward(const Problem& pb, bool text_perm, FwdPlan* plan, int tile_q) {
   const int P = pb.P;
   Geo g{pb, text_perm};
   plan->items.clear();
@@ -121,10 +121,10 @@ void plan_forward(const Problem& pb, bool text_perm, FwdPlan* plan) {
     if (s == 0) {
       // prefix queries: causal self-attention of the prefix, computed once
       for (int i = 0; i < pb.n_seqs && pb.N > 0; ++i) {
-        for (int64_t t0 = 0; t0 < pb.N; t0 += kFwdTileQ) {
+        for (int64_t t0 = 0; t0 < pb.N; t0 += tile_q) {
           FwdItem it{};
           it.q_row0 = (int32_t)(pb.cu[i] + t0);
-          it.q_len = (int32_t)std::min<int64_t>(kFwdTileQ, pb.N - t0);
+          it.q_len = (int32_t)std::min<int64_t>(tile_q, pb.N - t0);
           it.q_src = SRC_NAT;
           it.seg[0] = make_seg(pb.cu[i], pb.N, SRC_NAT, true, t0);
           it.nseg = 1;
@@ -149,9 +149,9 @@ void plan_forward(const Problem& pb, bool text_perm, FwdPlan* plan) {
             const int j2 = ((r - s2) % P + P) % P;
             if (chunk_id(P, j2, 0) < cq || chunk_id(P, j2, 1) < cq) last = s2;
           }
-          for (int64_t t0 = 0; t0 < c; t0 += kFwdTileQ) {
+          for (int64_t t0 = 0; t0 < c; t0 += tile_q) {
             FwdItem it{};
-            it.q_len = (int32_t)std::min<int64_t>(kFwdTileQ, c - t0);
+            it.q_len = (int32_t)std::min<int64_t>(tile_q, c - t0);
             it.q_row0 = (int32_t)(g.chunk_row(i, r, w) + t0);
             it.q_src = g.text_src();
             int n = 0;

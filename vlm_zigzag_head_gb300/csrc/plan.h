@@ -16,7 +16,8 @@
 
 namespace cpattn {
 
-constexpr int kFwdTileQ = 128;  // query rows of one forward work item
+constexpr int kFwdTileQ = 128;  // query rows of one forward work item (CUDA-core path)
+constexpr int kFwdPairQ = 256;  // query rows of one tensor-core forward item (two 128-row tiles)
 constexpr int kFwdTileK = 128;  // keys per forward KV tile
 constexpr int kBwdTileK = 128;  // keys of one backward work item
 constexpr int kBwdTileQ = 64;   // query rows per backward inner tile
@@ -85,8 +86,11 @@ struct BwdPlan {
 };
 
 // text_perm = true: text rows address the rank-local (gathered) buffer;
-// false: they address natural order (used by the fp32 dQ pass).
-void plan_forward(const Problem& pb, bool text_perm, FwdPlan* plan);
+// false: they address natural order (used by the fp32 dQ pass).  tile_q:
+// query rows per item (kFwdTileQ, or kFwdPairQ for the tensor-core kernel,
+// which splits an item into two 128-row tiles; a causal rule then holds for
+// the second tile with delta + 128).
+void plan_forward(const Problem& pb, bool text_perm, FwdPlan* plan, int tile_q = kFwdTileQ);
 void plan_backward(const Problem& pb, BwdPlan* plan);
 
 }  // namespace cpattn

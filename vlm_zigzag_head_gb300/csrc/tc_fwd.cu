@@ -1,31 +1,30 @@
 // Ring-step attention forward on 5th-generation tensor cores (sm_103a).
 //
-// One CTA computes one work item of a ring step for one head: a tile of 128
-// query rows against the key runs the step gives it (page
-// "context-parallel-multimodal": §1.1 zigzag chunks, §1 ring order, §4.1
-// replicated prefix in step 0), with an online softmax over the KV tiles and
-// a fused log-sum-exp merge into the fp32 running result (or the final write
-// in natural order).
+// One CTA computes one work item of a ring step for one head: up to 256 query
+// rows, taken as two 128-row tiles A and B, against the key runs the step
+// gives them (page "context-parallel-multimodal": §1.1 zigzag chunks, §1 ring
+// order, §4.1 replicated prefix in step 0), with an online softmax over the
+// KV tiles and a fused log-sum-exp merge into the fp32 running result (or the
+// final write in natural order).  Both tiles share every K / V tile.
+//
+// The two tiles ping-pong: the tensor core computes one tile's products while
+// the other tile's softmax runs.  Issue order for KV tile j >= 1:
+//   PV_A(j-1)  S_A(j)  PV_B(j-1)  S_B(j)
+// (S_A(j) overwrites the TMEM that holds P_A(j-1), so PV_A(j-1) goes first).
 //
 // Warp roles (384 threads; TMEM lane quarter of warp w is w % 4):
-//   warp 0       TMA producer of Q and K tiles
+//   warp 0       TMA producer of Q (both tiles) and K
 //   warp 1       TMEM allocation; lane 0 issues every tcgen05.mma
-//   warp 2       TMA producer of V tiles
+//   warp 2       TMA producer of V
 //   warp 3       idle
-//   warps 4..7   softmax of key columns 0..63 of every S tile, then the
-//                epilogue of O columns [0, D/2); thread = query row = TMEM lane
-//   warps 8..11  the same for key columns 64..127 and O columns [D/2, D)
-// The two warps that share a query row exchange their partial row maxima
-// (and, at the end, their partial row sums) through shared memory; a per-pair
-// mbarrier (bounded waits, like every other wait here) orders the exchange.
+//   warps 4..7   softmax + epilogue of tile A; thread = query row = TMEM lane
+//   warps 8..11  softmax + epilogue of tile B
 //
-// TMEM (512 columns): S ping-pong buffers at columns [0,128) and [128,256),
-// the O accumulator at [256, 256 + D), Q as bf16 pairs at [384, 384 + D/2).
-// P (bf16) overwrites the S buffer it was computed from: the warp of key
-// half g writes its 64 probabilities at buffer columns [64g, 64g + 32).  Both
-// products read their A operand (Q, P) from TMEM and only B (K, V) from
-// shared memory.  Shared memory: Q (128 x D), two K and two V stages
-// (128 x D each), in the 128-byte swizzled layout TMA writes.
+// TMEM (512 columns): S_A [0,128), S_B [128,256), O_A [256, 256 + D),
+// O_B [384, 384 + D).  P (bf16 pairs, 64 columns) overwrites the first half of
+// its S buffer and is the A operand of PV, read straight from TMEM.  Shared
+// memory: Q_A, Q_B, two K and two V stages (128 x D each) in the 128-byte
+// swizzled layout TMA writes, 1024-byte aligned.
 #include <cuda_bf16.h>
 
 #include "kernels.h"
@@ -39,11 +38,13 @@ namespace {
 using namespace ptx;
 
 constexpr int kThreads = 384;
-constexpr int kBM = kFwdTileQ;   // 128 query rows
+constexpr int kBM = 128;         // rows of one query tile
 constexpr int kBN = kFwdTileK;   // 128 keys per KV tile
 constexpr int kStages = 2;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO = 256, kColQ = 384;
+// TMEM columns of tile x's S buffer and O accumulator
+__device__ __forceinline__ uint32_t col_s(int x) { return x ? 128u : 0u; }
+__device__ __forceinline__ uint32_t col_o(int x) { return x ? 384u : 256u; }
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: stale max may lag by 2^8
 constexpr long long kDrainLimit = 1LL << 24;
 
@@ -51,30 +52,28 @@ template <int D>
 struct Smem {
   static constexpr int kTile = kBM * D * 2;        // bytes of a 128 x D bf16 tile
   static constexpr int kBox = 128 * 128;           // one 128-row x 128-byte TMA box
-  static constexpr int kQ = 0;
-  static constexpr int kK = kQ + kTile;
+  static constexpr int kQ = 0;                     // [tile A, tile B]
+  static constexpr int kK = kQ + 2 * kTile;
   static constexpr int kV = kK + kStages * kTile;
-  static constexpr int kP = kV + kStages * kTile;
-  static constexpr int kXch = kP;                       // [parity][half][128] float exchange
-  static constexpr int kBars = kXch + 4 * kBM * 4;
+  static constexpr int kBars = kV + kStages * kTile;
   static constexpr int kBytes = kBars + 256;
   static constexpr int kAlloc = kBytes + 1024;     // slack for 1024-byte alignment
 };
+static_assert(Smem<128>::kAlloc <= 227 * 1024, "shared memory budget");
 
 struct Bars {
   uint64_t q_full;
   uint64_t k_full[kStages], k_empty[kStages];
   uint64_t v_full[kStages], v_empty[kStages];
-  uint64_t s_full[2];
-  uint64_t q_tmem;    // Q copied into TMEM by the softmax warps
-  uint64_t p_full, o_done;
+  uint64_t s_full[2];   // per tile: S(j) in TMEM
+  uint64_t p_full[2];   // per tile: P(j) in TMEM (4 softmax warps)
+  uint64_t o_done[2];   // per tile: PV(j) accumulated
   uint64_t drain;
-  uint64_t pair[4];   // the two softmax warps of each TMEM lane quarter
   uint32_t tmem_base;
   int abort;
 };
 
-// Tiles of one key run visible to a query tile of q_len rows.
+// Tiles of one key run visible to query rows 0 .. q_len-1 of the item.
 __device__ __forceinline__ int run_tiles(const Seg& s, int q_len) {
   int vis = s.len;
   if (s.causal) {
@@ -112,12 +111,12 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
       mbar_init(&bars->v_full[s], 1);
       mbar_init(&bars->v_empty[s], 1);
     }
-    for (int b = 0; b < 2; ++b) mbar_init(&bars->s_full[b], 1);
-    mbar_init(&bars->q_tmem, 8);
-    mbar_init(&bars->p_full, 8);
-    mbar_init(&bars->o_done, 1);
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(&bars->s_full[x], 1);
+      mbar_init(&bars->p_full[x], 4);
+      mbar_init(&bars->o_done[x], 1);
+    }
     mbar_init(&bars->drain, 1);
-    for (int q = 0; q < 4; ++q) mbar_init(&bars->pair[q], 2);
     bars->abort = 0;
     fence_mbar_init();
   }
@@ -129,23 +128,30 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
+  // 384 threads launch with 168 registers each; warpgroup 0 (TMA, MMA) drops
+  // to 72 and the two softmax warpgroups rise to 216, enough to hold a whole
+  // 128-column S row: 128 * 72 + 256 * 216 = 384 * 168
 
-  const int q_len = it.q_len;
+  const int q_len = it.q_len;   // rows of the item (tile A: first 128, tile B: the rest)
   const int nseg = it.nseg;
   int n_tiles = 0;
   for (int s = 0; s < nseg; ++s) n_tiles += run_tiles(it.seg[s], q_len);
 
+  if (warp < 4) {
+  setmaxnreg_dec<72>();
   if (warp == 0 || warp == 2) {
     // ------------------------------------------------------------ TMA producers
     if (lane == 0) {
       const bool is_k = warp == 0;
-      int issued = 0;  // tiles issued by this producer
+      int issued = 0;
       bool q_issued = false;
       if (is_k && n_tiles > 0) {
         const CUtensorMap* qm = it.q_src == SRC_TEXT ? &a.tm_q_text : &a.tm_q_nat;
-        mbar_expect_tx(&bars->q_full, L::kTile);
-        for (int b = 0; b < D / 64; ++b)
-          tma_load_3d(qm, &bars->q_full, smem + L::kQ + b * L::kBox, b * 64, h, it.q_row0);
+        mbar_expect_tx(&bars->q_full, 2 * L::kTile);
+        for (int x = 0; x < 2; ++x)
+          for (int b = 0; b < D / 64; ++b)
+            tma_load_3d(qm, &bars->q_full, smem + L::kQ + x * L::kTile + b * L::kBox, b * 64, h,
+                        it.q_row0 + x * kBM);
         q_issued = true;
       }
       int j = 0;
@@ -188,50 +194,52 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
     if (lane == 0) {
       constexpr uint32_t idesc_qk = idesc_bf16(kBM, kBN, 0, 0);
       constexpr uint32_t idesc_pv = idesc_bf16(kBM, D, 0, 1);
-      bool ok = n_tiles == 0 || mbar_wait(&bars->q_tmem, 0, lim, abort);
+      const uint32_t q_addr = smem_u32(smem + L::kQ);
+      bool ok = n_tiles == 0 || mbar_wait(&bars->q_full, 0, lim, abort);
       if (!ok) record_timeout(a.status, abort, 3);
-      auto issue_pv = [&](int i) -> bool {
-        const int st = i % kStages;
-        if (!mbar_wait(&bars->p_full, i & 1, lim, abort)) return false;
-        if (!mbar_wait(&bars->v_full[st], (i / kStages) & 1, lim, abort)) return false;
+      // S_x(j) = Q_x K_j^T into tile x's S buffer
+      auto issue_s = [&](int x, int j) {
+        const uint32_t k_addr = smem_u32(smem + L::kK + (j % kStages) * L::kTile);
+        const uint32_t qx = q_addr + x * L::kTile;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk / 4) * L::kBox + (kk % 4) * 32;
+          mma_bf16(tmem + col_s(x), sdesc_sw128(qx + off, 16, 1024),
+                   sdesc_sw128(k_addr + off, 16, 1024), idesc_qk, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(&bars->s_full[x]);
+      };
+      // O_x += P_x(j) V_j, P from TMEM (keys 16kk.. 16kk+15: columns 8kk .. 8kk+7)
+      auto issue_pv = [&](int x, int j) -> bool {
+        const int st = j % kStages;
+        if (!mbar_wait(&bars->p_full[x], j & 1, lim, abort)) return false;
+        if (x == 0 && !mbar_wait(&bars->v_full[st], (j / kStages) & 1, lim, abort)) return false;
         tc_fence_after();
         const uint32_t v_addr = smem_u32(smem + L::kV + st * L::kTile);
-        const uint32_t p_tmem = tmem + ((i & 1) ? kColS1 : kColS0);
 #pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk) {   // keys 16kk..: half kk/4, column (kk%4)*8
+        for (int kk = 0; kk < kBN / 16; ++kk) {
           const uint64_t bd = sdesc_sw128(v_addr + kk * 16 * 128, L::kBox, 1024);
-          mma_bf16_ts(tmem + kColO, p_tmem + (kk / 4) * 64 + (kk % 4) * 8, bd, idesc_pv,
-                      (i > 0 || kk > 0) ? 1u : 0u);
+          mma_bf16_ts(tmem + col_o(x), tmem + col_s(x) + kk * 8, bd, idesc_pv,
+                      (j > 0 || kk > 0) ? 1u : 0u);
         }
-        mma_commit(&bars->v_empty[st]);
-        mma_commit(&bars->o_done);
+        mma_commit(&bars->o_done[x]);
+        if (x == 1) mma_commit(&bars->v_empty[st]);
         return true;
       };
       for (int j = 0; ok && j < n_tiles; ++j) {
-        const int st = j % kStages, sb = j & 1;
-        // the S buffer of tile j last held P_{j-2}, read by PV_{j-2}, issued
-        // (and so executed) before this product
+        const int st = j % kStages;
         if (!mbar_wait(&bars->k_full[st], (j / kStages) & 1, lim, abort)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint32_t k_addr = smem_u32(smem + L::kK + st * L::kTile);
-        const uint32_t s_tmem = tmem + (sb ? kColS1 : kColS0);
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {     // head dims 16kk..: Q columns 8kk..
-          const uint32_t off = (kk / 4) * L::kBox + (kk % 4) * 32;
-          mma_bf16_ts(s_tmem, tmem + kColQ + kk * 8, sdesc_sw128(k_addr + off, 16, 1024),
-                      idesc_qk, kk > 0 ? 1u : 0u);
-        }
+        if (j >= 1 && !issue_pv(0, j - 1)) { ok = false; break; }
+        issue_s(0, j);
+        if (j >= 1 && !issue_pv(1, j - 1)) { ok = false; break; }
+        issue_s(1, j);
         mma_commit(&bars->k_empty[st]);
-        mma_commit(&bars->s_full[sb]);
-        if (j >= 1 && !issue_pv(j - 1)) {
-          ok = false;
-          break;
-        }
       }
-      if (ok && n_tiles > 0 && !issue_pv(n_tiles - 1)) ok = false;
+      if (ok && n_tiles > 0 && !(issue_pv(0, n_tiles - 1) && issue_pv(1, n_tiles - 1))) ok = false;
       if (!ok) {
         record_timeout(a.status, abort, 4);
         // drain: nothing issued by this thread may still be running at exit
@@ -240,90 +248,54 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
         mbar_wait(&bars->drain, 0, kDrainLimit, &zero);
       }
     }
-  } else if (warp >= 4) {
+  }
+  } else {
+    setmaxnreg_inc<216>();
     // ------------------------------------------------------------ softmax
-    const int g = (warp - 4) >> 2;             // key-column half of S / O-column half
-    const int t = (warp & 3) * 32 + lane;      // query row == TMEM lane
+    const int x = (warp - 4) >> 2;             // tile: 0 = A, 1 = B
+    const int t = (warp & 3) * 32 + lane;      // query row of the tile == TMEM lane
+    const int tq = x * kBM + t;                // query row of the item
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
-    uint64_t* pair = &bars->pair[warp & 3];
-    float* xch = reinterpret_cast<float*>(smem + L::kXch);  // [parity][half][128]
-    // exchange a per-row value with the partner warp; phase k of the pair barrier
-    auto exchange = [&](float v, int k, float* partner) -> bool {
-      xch[((k & 1) * 2 + g) * kBM + t] = v;
-      __syncwarp();
-      if (lane == 0) mbar_arrive(pair);
-      if (!mbar_wait(pair, k & 1, lim, abort)) return false;
-      *partner = xch[((k & 1) * 2 + (1 - g)) * kBM + t];
-      return true;
-    };
+    const uint32_t s_col = tmem + lane_off + col_s(x);
     const float sl2 = a.scale_log2;
     float m = -INFINITY;   // running max of scaled scores (log2 units), may lag
-    float l = 0.f;         // partial row sum over this thread's columns
+    float l = 0.f;
     bool ok = true;
-    // Q row t into TMEM (bf16 pairs): warp half g copies head dims [64g, 64g + 64)
-    if (n_tiles > 0) {
-      if (!mbar_wait(&bars->q_full, 0, lim, abort)) ok = false;
-      if (ok && g * 64 < D) {
-        uint32_t r[32];
-        const uint8_t* qrow = smem + L::kQ + g * L::kBox + t * 128;
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          const uint4 v = *reinterpret_cast<const uint4*>(qrow + ((c ^ (t & 7)) << 4));
-          r[c * 4 + 0] = v.x;
-          r[c * 4 + 1] = v.y;
-          r[c * 4 + 2] = v.z;
-          r[c * 4 + 3] = v.w;
-        }
-        tmem_st32(tmem + lane_off + kColQ + g * 32, r);
-        tmem_st_wait();
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->q_tmem);
-    }
     int j = 0;
     for (int s = 0; ok && s < nseg; ++s) {
       const Seg sg = it.seg[s];
       const int nt = run_tiles(sg, q_len);
+      // key u of the run is visible to this row iff u < lim_u
+      const int lim_u = sg.causal ? min(sg.len, tq + sg.delta + 1) : sg.len;
       for (int tt = 0; tt < nt; ++tt, ++j) {
-        const int sb = j & 1;
-        if (!mbar_wait(&bars->s_full[sb], (j >> 1) & 1, lim, abort)) { ok = false; break; }
+        if (!mbar_wait(&bars->s_full[x], j & 1, lim, abort)) { ok = false; break; }
         tc_fence_after();
-        constexpr int kH = kBN / 2;              // 64 columns per thread
-        float x[kH];
-        {
-          uint32_t r[kH];
-          const uint32_t s_col = tmem + lane_off + (sb ? kColS1 : kColS0) + g * kH;
+        // the whole 128-column S row of this thread in registers: one TMEM
+        // round trip per tile
+        uint32_t r[kBN / 32][32];
 #pragma unroll
-          for (int c = 0; c < kH / 32; ++c)
-            tmem_ld32(s_col + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&r[c * 32]));
-          tmem_ld_wait();
+        for (int c = 0; c < kBN / 32; ++c) tmem_ld32(s_col + c * 32, r[c]);
+        tmem_ld_wait();
 #pragma unroll
-          for (int c = 0; c < kH / 32; ++c)
-            reg_fence32(*reinterpret_cast<uint32_t(*)[32]>(&r[c * 32]));
-#pragma unroll
-          for (int c = 0; c < kH; ++c) x[c] = __uint_as_float(r[c]) * sl2;
-        }
-        // mask: key u = u0 + c visible iff u < len and (!causal or u <= t + delta)
-        const int u0 = tt * kBN + g * kH;
-        const bool full = (u0 + kH <= sg.len) && (!sg.causal || u0 + kH - 1 <= sg.delta);
-        if (!full) {
-          const int lim_u = sg.causal ? min(sg.len, t + sg.delta + 1) : sg.len;
-#pragma unroll
-          for (int c = 0; c < kH; ++c)
-            if (u0 + c >= lim_u) x[c] = -INFINITY;
-        }
+        for (int c = 0; c < kBN / 32; ++c) reg_fence32(r[c]);
+        // keys at or past `vis` (tile-relative) are masked for this row
+        const int vis = lim_u - tt * kBN;
+        const bool whole = __all_sync(0xffffffffu, vis >= kBN);
         float mp[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) mp[i] = x[i];
+        for (int i = 0; i < 8; ++i) mp[i] = -INFINITY;
+        if (whole) {
 #pragma unroll
-        for (int c = 8; c < kH; ++c) mp[c & 7] = fmaxf(mp[c & 7], x[c]);
-        float mt = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
-                         fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
-        // combine with the partner half of the row (same value in both threads)
-        float mo;
-        if (!exchange(mt, j, &mo)) { ok = false; break; }
-        mt = fmaxf(mt, mo);
+          for (int i = 0; i < kBN; ++i)
+            mp[i & 7] = fmaxf(mp[i & 7], __uint_as_float(r[i / 32][i % 32]));
+        } else {
+#pragma unroll
+          for (int i = 0; i < kBN; ++i)
+            mp[i & 7] = fmaxf(mp[i & 7], i < vis ? __uint_as_float(r[i / 32][i % 32]) : -INFINITY);
+        }
+        // max of the raw scores, then to scaled log2 units (scale > 0)
+        const float mt = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
+                               fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7]))) * sl2;
         const float m_new = fmaxf(m, mt);
         const bool need = m_new > m + kRescaleThreshold || (m == -INFINITY && m_new != -INFINITY);
         if (__any_sync(0xffffffffu, need)) {
@@ -332,63 +304,70 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
             l *= alpha;
             m = m_new;
           }
-          if (j > 0) {  // O holds PV of earlier tiles: wait for the last, rescale our half
-            if (!mbar_wait(&bars->o_done, (j - 1) & 1, lim, abort)) { ok = false; break; }
+          if (j > 0) {  // O holds PV of earlier tiles (complete: PV_x(j-1) precedes S_x(j))
+            if (!mbar_wait(&bars->o_done[x], (j - 1) & 1, lim, abort)) { ok = false; break; }
             tc_fence_after();
 #pragma unroll 1
-            for (int c = 0; c < D / 64; ++c) {
-              uint32_t r[32];
-              const uint32_t col = tmem + lane_off + kColO + g * (D / 2) + c * 32;
-              tmem_ld32(col, r);
+            for (int c = 0; c < D / 32; ++c) {
+              uint32_t o[32];
+              const uint32_t col = tmem + lane_off + col_o(x) + c * 32;
+              tmem_ld32(col, o);
               tmem_ld_wait();
-              reg_fence32(r);
+              reg_fence32(o);
 #pragma unroll
-              for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
-              tmem_st32(col, r);
+              for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+              tmem_st32(col, o);
             }
             tmem_st_wait();
           }
         }
+        // probabilities, row sum, and P (bf16 pairs) over S columns [0, 64)
         const float mu = m == -INFINITY ? 0.f : m;
         float sp[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) sp[i] = 0.f;
+        uint32_t pk[2][32];
+        if (whole) {
 #pragma unroll
-        for (int c = 0; c < kH; ++c) {
-          x[c] = ex2(x[c] - mu);
-          sp[c & 7] += x[c];
+          for (int i = 0; i < kBN; i += 2) {
+            const float p0 = ex2(fmaf(__uint_as_float(r[i / 32][i % 32]), sl2, -mu));
+            const float p1 = ex2(fmaf(__uint_as_float(r[i / 32][i % 32 + 1]), sl2, -mu));
+            sp[(i >> 1) & 7] += p0 + p1;
+            pk[i / 64][(i / 2) % 32] = pack_bf16x2(p0, p1);
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < kBN; i += 2) {
+            float p0 = ex2(fmaf(__uint_as_float(r[i / 32][i % 32]), sl2, -mu));
+            float p1 = ex2(fmaf(__uint_as_float(r[i / 32][i % 32 + 1]), sl2, -mu));
+            if (i >= vis) p0 = 0.f;
+            if (i + 1 >= vis) p1 = 0.f;
+            sp[(i >> 1) & 7] += p0 + p1;
+            pk[i / 64][(i / 2) % 32] = pack_bf16x2(p0, p1);
+          }
         }
+        tmem_st32(s_col, pk[0]);
+        tmem_st32(s_col + 32, pk[1]);
         l += ((sp[0] + sp[1]) + (sp[2] + sp[3])) + ((sp[4] + sp[5]) + (sp[6] + sp[7]));
-        // P (bf16 pairs) over this thread's own S columns: buffer columns
-        // [64g, 64g + 32); PV_j reads it from there
-        {
-          uint32_t pk[kH / 2];
-#pragma unroll
-          for (int c = 0; c < kH / 2; ++c) pk[c] = pack_bf16x2(x[2 * c], x[2 * c + 1]);
-          tmem_st32(tmem + lane_off + (sb ? kColS1 : kColS0) + g * 64, pk);
-          tmem_st_wait();
-        }
+        tmem_st_wait();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&bars->p_full);
+        if (lane == 0) mbar_arrive(&bars->p_full[x]);
       }
     }
     // ------------------------------------------------------------ epilogue
-    if (ok && n_tiles > 0 && !mbar_wait(&bars->o_done, (n_tiles - 1) & 1, lim, abort)) ok = false;
-    // the row's two partial sums
-    float lo_part = 0.f;
-    if (ok && !exchange(l, n_tiles, &lo_part)) ok = false;
-    l += lo_part;
+    if (ok && n_tiles > 0 && !mbar_wait(&bars->o_done[x], (n_tiles - 1) & 1, lim, abort))
+      ok = false;
     if (!ok) {
       record_timeout(a.status, abort, 5);
     } else {
       tc_fence_after();
-      const bool valid = t < q_len;
+      const bool valid = tq < q_len;
       float lse_s = l > 0.f ? (m + __log2f(l)) * 0.6931471805599453f : -INFINITY;
       const float inv = l > 0.f ? 1.f / l : 0.f;
       const int flags = it.flags;
       const long long rrow =
-          it.run_row0 >= 0 ? (long long)h * a.run_rows + it.run_row0 + t : 0;
+          it.run_row0 >= 0 ? (long long)h * a.run_rows + it.run_row0 + tq : 0;
       float ca = 0.f, cb = 1.f;
       if (valid && !(flags & F_FIRST)) {
         const float lr = a.lse_run[rrow];
@@ -400,17 +379,16 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
           lse_s = mm + logf(tot);
         }
       }
-      const int c0 = g * (D / 2);               // this thread's O columns
-      const float* orun = a.o_run + rrow * D + c0;
-      float* orun_w = a.o_run + rrow * D + c0;
-      const long long out_off = ((long long)(it.out_row0 + t) * a.H + h) * D + c0;
+      const float* orun = a.o_run + rrow * D;
+      float* orun_w = a.o_run + rrow * D;
+      const long long out_off = ((long long)(it.out_row0 + tq) * a.H + h) * D;
       __nv_bfloat16* outp = reinterpret_cast<__nv_bfloat16*>(a.out) + out_off;
       __nv_bfloat16* lop =
           a.out_lo ? reinterpret_cast<__nv_bfloat16*>(a.out_lo) + out_off : nullptr;
 #pragma unroll 1
-      for (int c = 0; c < D / 64; ++c) {
+      for (int c = 0; c < D / 32; ++c) {
         uint32_t r[32];
-        tmem_ld32(tmem + lane_off + kColO + c0 + c * 32, r);
+        tmem_ld32(tmem + lane_off + col_o(x) + c * 32, r);
         tmem_ld_wait();
         reg_fence32(r);
         if (!valid) continue;
@@ -456,8 +434,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
                 make_float4(o[i], o[i + 1], o[i + 2], o[i + 3]);
         }
       }
-      if (valid && g == 0) {
-        if (flags & F_FINAL) a.lse[(long long)h * a.T + it.out_row0 + t] = lse_s;
+      if (valid) {
+        if (flags & F_FINAL) a.lse[(long long)h * a.T + it.out_row0 + tq] = lse_s;
         else a.lse_run[rrow] = lse_s;
       }
     }
