@@ -21,10 +21,12 @@
 //   warp 0       TMA producer (K, V once; Q, dO and the lse2 / D rows per query
 //                tile, 3 stages)
 //   warp 1       TMEM allocation; lane 0 issues every tcgen05.mma
-//   warps 2, 3   idle
+//   warp 2       idle
+//   warp 3       lane 0 issues the dQ bulk reduce-adds of the drain
 //   warps 4..11  P / dS computation (two warpgroups, 32 query columns each),
 //                then the dK / dV epilogue; thread = key row
-//   warps 12..15 dQ drain; thread = head-dim index (TMEM lane of dQ^T)
+//   warps 12..15 dQ drain into shared-memory staging; thread = head-dim
+//                index (TMEM lane of dQ^T)
 //
 // TMEM columns: S^T [0,64), dP^T [64,128), dQ^T ping-pong [128,192) and
 // [192,256), dK [256,384), dV [384,512).
@@ -318,12 +320,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
     // ------------------------------------------------------------ dQ drain
     // thread = head-dim index (warp & 3) * 32 + lane == TMEM lane of dQ^T.
     // Each tile's dQ^T goes out in four rounds of 16 query columns: the four
-    // warps stage them as fp32 [16 rows][128] in shared memory and one elected
-    // thread adds the block into dQ with a bulk tensor reduce (the reduction
-    // runs in L2; no per-thread atomics).
+    // warps stage them as fp32 [16 rows][128] in shared memory; warp 3 adds
+    // each staged block into dQ with a bulk tensor reduce (the reduction runs
+    // in L2; no per-thread atomics).
     const int dd = (warp & 3) * 32 + lane;
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
-    const bool elected = warp == 12 && lane == 0;
     constexpr int N = L::kNumStg;
     bool ok = true;
     int k = 0;                                   // round counter
@@ -358,23 +359,41 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) mbar_arrive(&bars->stg_full[sb]);
-          if (elected) {
-            if (!mbar_wait(&bars->stg_full[sb], (k / N) & 1, lim, abort)) {
-              ok = false;
-              break;
-            }
-            // rows past the run carry exact zeros (P = 0 there); rows past T are
-            // clipped by the tensor map
-            tma_reduce_add_3d(&a.tm_dq, stg, 0, h, grow + half * 32 + rr * 16);
-            bulk_commit();
-            bulk_wait_read<N - 1>();             // the buffer of round k + 1 is readable again
-            if (k + 1 >= N) mbar_arrive(&bars->stg_free[(k + 1) % N]);
-          }
         }
       }
     }
-    if (elected) bulk_wait_all();                // every reduce-add finished before exit
     if (!ok) record_timeout(a.status, abort, 14);
+  } else if (warp == 3) {
+    // ------------------------------------------------------------ dQ reduce issue
+    // One thread, alone in its warp (a waiting thread never holds up a warp
+    // that stages): round k of the drain is staged in buffer k % N.
+    if (lane == 0) {
+      constexpr int N = L::kNumStg;
+      bool ok = true;
+      int k = 0;
+      for (int j = 0; ok && j < n_qt; ++j) {
+        Seg sgd;
+        int q0d, td;
+        tile_of(it, (j + rot) % n_qt, sgd, q0d, td);
+        const int grow = sgd.row0 + q0d + td * kBQ;
+        for (int r4 = 0; r4 < 4; ++r4, ++k) {
+          const int sb = k % N;
+          if (!mbar_wait(&bars->stg_full[sb], (k / N) & 1, lim, abort)) {
+            ok = false;
+            break;
+          }
+          // rows past the run carry exact zeros (P = 0 there); rows past T are
+          // clipped by the tensor map
+          tma_reduce_add_3d(&a.tm_dq, smem + L::kStg + sb * L::kStgBytes, 0, h,
+                            grow + r4 * L::kStgRows);
+          bulk_commit();
+          bulk_wait_read<N - 1>();               // the buffer of round k + 1 is readable again
+          if (k + 1 >= N) mbar_arrive(&bars->stg_free[(k + 1) % N]);
+        }
+      }
+      bulk_wait_all();                           // every reduce-add finished before exit
+      if (!ok) record_timeout(a.status, abort, 15);
+    }
   } else if (warp >= 4) {
     // ------------------------------------------------------------ P / dS
     // Two warpgroups share every query tile: warpgroup g (warps 4+4g .. 7+4g)
