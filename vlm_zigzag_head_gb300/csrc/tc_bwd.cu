@@ -387,8 +387,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
           tma_reduce_add_3d(&a.tm_dq, smem + L::kStg + sb * L::kStgBytes, 0, h,
                             grow + r4 * L::kStgRows);
           bulk_commit();
-          bulk_wait_read<N - 1>();               // the buffer of round k + 1 is readable again
-          if (k + 1 >= N) mbar_arrive(&bars->stg_free[(k + 1) % N]);
+          // free this round's buffer as soon as the reduce has read it, so the
+          // staging warps can run up to N rounds ahead of this thread
+          bulk_wait_read<0>();
+          mbar_arrive(&bars->stg_free[sb]);
         }
       }
       bulk_wait_all();                           // every reduce-add finished before exit
