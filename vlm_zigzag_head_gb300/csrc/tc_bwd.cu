@@ -336,30 +336,31 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
       if (!mbar_wait(&bars->dq_full[b], (j >> 1) & 1, lim, abort)) { ok = false; break; }
       tc_fence_after();
       const int grow = sgd.row0 + q0d + td * kBQ;  // natural row of the tile's first query
-      for (int half = 0; ok && half < 2; ++half) {
-        uint32_t r[32];
-        tmem_ld32(tmem + lane_off + (b ? kColDQ1 : kColDQ0) + half * 32, r);
-        tmem_ld_wait();
-        reg_fence32(r);
-        if (half == 1) {                         // all of this tile's dQ^T is in registers
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&bars->dq_empty[b]);
-        }
-        for (int rr = 0; rr < 2; ++rr, ++k) {
-          const int sb = k % N;
-          if (k >= N && !mbar_wait(&bars->stg_free[sb], ((k / N) - 1) & 1, lim, abort)) {
-            ok = false;
-            break;
-          }
-          float* stg = reinterpret_cast<float*>(smem + L::kStg + sb * L::kStgBytes);
+      // the whole dQ^T tile (64 query columns) into registers first, so its
+      // TMEM buffer is free for the next dQ product before any staging
+      uint32_t r[2][32];
+      tmem_ld32(tmem + lane_off + (b ? kColDQ1 : kColDQ0), r[0]);
+      tmem_ld32(tmem + lane_off + (b ? kColDQ1 : kColDQ0) + 32, r[1]);
+      tmem_ld_wait();
+      reg_fence32(r[0]);
+      reg_fence32(r[1]);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->dq_empty[b]);
 #pragma unroll
-          for (int x = 0; x < L::kStgRows; ++x)
-            stg[x * kD + dd] = __uint_as_float(r[rr * 16 + x]) * a.scale;
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&bars->stg_full[sb]);
+      for (int r4 = 0; r4 < 4; ++r4, ++k) {
+        const int sb = k % N;
+        if (k >= N && !mbar_wait(&bars->stg_free[sb], ((k / N) - 1) & 1, lim, abort)) {
+          ok = false;
+          break;
         }
+        float* stg = reinterpret_cast<float*>(smem + L::kStg + sb * L::kStgBytes);
+#pragma unroll
+        for (int x = 0; x < L::kStgRows; ++x)
+          stg[x * kD + dd] = __uint_as_float(r[r4 >> 1][(r4 & 1) * 16 + x]) * a.scale;
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->stg_full[sb]);
       }
     }
     if (!ok) record_timeout(a.status, abort, 14);
