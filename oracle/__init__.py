@@ -16,6 +16,11 @@ Source pages (cited by short name in every docstring):
 * "Parallelism page" -- *Parallelism* (lizn-zn.github.io), §6 (CP: attention
   cost grows with the square of the length; KV is exchanged around a ring).
 
+Grouped KV heads (GQA / MQA) are not on the pages: where ``k``/``v`` hold
+``H_kv < H`` heads, query head ``h`` reads KV head ``h // (H / H_kv)``, the
+layout models with fewer KV heads use, and KV-side gradients are summed over
+each KV head's query heads.
+
 Every function is either the plain definition of the result (unpartitioned
 causal softmax attention per sample and its gradient) or a literal, step by
 step restatement of the partitioned method in the pages' order.  Pins that
@@ -33,4 +38,5 @@ from .attention import (  # noqa: F401
     cp_ring_fwd,
     cp_ring_bwd,
     cp_pair_counts,
+    kv_group,
 )

@@ -53,6 +53,27 @@ def _take(x, rows, heads):
     return np.asarray(x, dtype=np.float64)[np.asarray(rows)][:, heads]
 
 
+def kv_group(H, H_kv):
+    """Grouped-query attention: query head ``h`` reads KV head ``h // G`` with
+    ``G = H / H_kv`` (consecutive grouping; ``H_kv = H`` is plain multi-head
+    attention, ``H_kv = 1`` is multi-query attention)."""
+    if H_kv < 1 or H % H_kv != 0:
+        raise ValueError("H=%d is not a multiple of H_kv=%d" % (H, H_kv))
+    return H // H_kv
+
+
+def _expand_kv(x, H):
+    """[T, H_kv, d] -> [T, H, d]: KV head j copied to query heads jG .. jG+G-1."""
+    return np.repeat(x, kv_group(H, x.shape[1]), axis=1)
+
+
+def _fold_kv(g, H_kv):
+    """Adjoint of :func:`_expand_kv`: the gradients of the G copies of a KV
+    head are summed.  [..., H, d] -> [..., H_kv, d]."""
+    G = kv_group(g.shape[-2], H_kv)
+    return g.reshape(g.shape[:-2] + (H_kv, G, g.shape[-1])).sum(axis=-2)
+
+
 def _samples(cu_seqlens):
     cu = [int(c) for c in cu_seqlens]
     if any(b < a for a, b in zip(cu, cu[1:])):
@@ -158,9 +179,11 @@ def causal_attention_fwd(q, k, v, cu_seqlens, scale, row_block=1024):
     """Unpartitioned causal attention of every sample (the method reaches this
     exactly, only partitioned).  Returns ``out [T,H,d]`` and ``lse [H,T]``.
     Query rows are evaluated ``row_block`` at a time; every row is computed
-    from its full set of visible keys."""
+    from its full set of visible keys.  ``k``/``v`` may hold fewer heads than
+    ``q`` (grouped-query attention, :func:`kv_group`)."""
     q, k, v = _f64(q), _f64(k), _f64(v)
     T, H, d = q.shape
+    k, v = _expand_kv(k, H), _expand_kv(v, H)
     out = np.zeros((T, H, d))
     lse = np.full((H, T), NEG_INF)
     for a, b in _samples(cu_seqlens):
@@ -178,9 +201,12 @@ def causal_attention_bwd(q, k, v, dout, cu_seqlens, scale, row_block=1024):
     backward, which the CP-VLM page's §3.2/§4.2 gradient path needs):
     P = softmax(S), dV = P^T dO, dP = dO V^T, D_i = dO_i . o_i,
     dS = P * (dP - D), dQ = scale dS K, dK = scale dS^T Q.
-    o is this oracle's own forward result.  Returns ``dq, dk, dv`` (THD)."""
+    o is this oracle's own forward result.  Returns ``dq, dk, dv`` (THD).
+    With grouped KV heads, dk/dv of a KV head sum its query heads' terms."""
     q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(dout)
     T, H, d = q.shape
+    H_kv = k.shape[1]
+    k, v = _expand_kv(k, H), _expand_kv(v, H)
     dq = np.zeros((T, H, d))
     dk = np.zeros((T, H, d))
     dv = np.zeros((T, H, d))
@@ -196,7 +222,7 @@ def causal_attention_bwd(q, k, v, dout, cu_seqlens, scale, row_block=1024):
                 dS = Pm * (dP - D)
                 dq[r0:r1, h] = scale * (dS @ K)
                 dk[a:r1, h] += scale * (dS.T @ Q)
-    return dq, dk, dv
+    return dq, _fold_kv(dk, H_kv), _fold_kv(dv, H_kv)
 
 
 def _sample_of(cu_seqlens, t):
@@ -212,6 +238,8 @@ def causal_attention_fwd_rows(q, k, v, cu_seqlens, scale, rows, heads=None, dout
     workloads too large for the full oracle).  Returns ``out [n,Hs,d]``,
     ``lse [Hs,n]`` and, when ``dout`` is given, ``dq [n,Hs,d]`` (the row's
     own dP and D make dQ_i computable row by row)."""
+    if k.shape[1] != q.shape[1]:
+        raise ValueError("the row-sampled oracle takes as many KV heads as query heads")
     rows = np.asarray(rows, dtype=np.int64)
     heads = list(range(q.shape[1])) if heads is None else list(heads)
     qf = _take(q, rows, heads)
@@ -258,6 +286,8 @@ def causal_attention_bwd_keys(q, k, v, dout, cu_seqlens, scale, keys, heads=None
     softmax and D_i = dO_i . o_i taken over its full set of visible keys.
     Cost grows with (sample end - smallest key) x sample length, so pick keys
     near the end of long samples.  Returns ``dk, dv [n,Hs,d]``."""
+    if k.shape[1] != q.shape[1]:
+        raise ValueError("the key-sampled oracle takes as many KV heads as query heads")
     keys = np.asarray(keys, dtype=np.int64)
     heads = list(range(q.shape[1])) if heads is None else list(heads)
     n, d = len(keys), q.shape[2]
@@ -362,9 +392,11 @@ def cp_ring_fwd(q, k, v, cu_seqlens, prefix_len, P, scale, return_partials=False
     5. results are written back to natural order (the inverse of the gather).
 
     Prefix query rows attend to their own prefix once.  Returns ``out, lse``
-    (and, with ``return_partials``, the per (rank, step) partials)."""
+    (and, with ``return_partials``, the per (rank, step) partials).  Grouped
+    KV heads are read through :func:`kv_group`."""
     q, k, v = _f64(q), _f64(k), _f64(v)
     T, H, d = q.shape
+    k, v = _expand_kv(k, H), _expand_kv(v, H)
     sid, pos = _positions(cu_seqlens)
     local = rank_local_rows(cu_seqlens, prefix_len, P)
     pre = _prefix_rows(cu_seqlens, prefix_len)
@@ -423,9 +455,13 @@ def cp_ring_bwd(q, k, v, dout, cu_seqlens, prefix_len, P, scale):
 
     Returns ``dq, dk, dv`` (THD) and the per-rank prefix partials
     ``pdk, pdv`` of shape ``[P + 1, n_prefix_rows, H, d]`` (slot P holds the
-    prefix queries' own term)."""
+    prefix queries' own term).  With grouped KV heads (:func:`kv_group`) the
+    KV-side gradients, per-rank prefix partials included, are summed over
+    each KV head's query heads."""
     q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(dout)
     T, H, d = q.shape
+    H_kv = k.shape[1]
+    k, v = _expand_kv(k, H), _expand_kv(v, H)
     out, lse = cp_ring_fwd(q, k, v, cu_seqlens, prefix_len, P, scale)
     D = (do * out).sum(axis=2)                     # [T, H]
     sid, pos = _positions(cu_seqlens)
@@ -467,7 +503,8 @@ def cp_ring_bwd(q, k, v, dout, cu_seqlens, prefix_len, P, scale):
             sv += pdv[r]
         dk[pre] += sk
         dv[pre] += sv
-    return dq, dk, dv, pdk, pdv
+    return (dq, _fold_kv(dk, H_kv), _fold_kv(dv, H_kv), _fold_kv(pdk, H_kv),
+            _fold_kv(pdv, H_kv))
 
 
 def cp_pair_counts(cu_seqlens, prefix_len, P):

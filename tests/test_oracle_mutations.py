@@ -88,3 +88,26 @@ def test_dropped_scale_in_dk_is_caught(monkeypatch):
     monkeypatch.setattr(oa, "causal_attention_bwd", no_scale)
     with pytest.raises(AssertionError):
         _check_bwd()
+
+
+def _check_gqa():
+    from test_oracle_pins import _gqa_inputs, _sdpa_gqa
+    cu = _cu(2, [10])
+    q, k, v = _gqa_inputs(cu[-1], 4, 2, 4, 9)
+    do = _rand((cu[-1], 4, 4), 10)
+    out, _ = oa.causal_attention_fwd(q, k, v, cu, 0.5)
+    dk = oa.causal_attention_bwd(q, k, v, do, cu, 0.5)[1]
+    ro, _, rk, _ = _sdpa_gqa(q, k, v, do, cu, 0.5)
+    np.testing.assert_allclose(out, ro, atol=1e-11)
+    np.testing.assert_allclose(dk, rk, atol=1e-11)
+
+
+def test_unmutated_gqa_check_passes():
+    _check_gqa()
+
+
+def test_interleaved_kv_grouping_is_caught(monkeypatch):
+    # query head h reading KV head h % H_kv instead of h // G
+    monkeypatch.setattr(oa, "_expand_kv", lambda x, H: np.tile(x, (1, oa.kv_group(H, x.shape[1]), 1)))
+    with pytest.raises(AssertionError):
+        _check_gqa()

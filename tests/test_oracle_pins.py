@@ -353,3 +353,79 @@ def test_sampled_rows_and_keys_match_autograd():
                                               row_block=4)
     np.testing.assert_allclose(dk, rk[keys][:, heads], rtol=0, atol=1e-12)
     np.testing.assert_allclose(dv, rv[keys][:, heads], rtol=0, atol=1e-12)
+
+
+# ---------------------------------------------------------------------------
+# grouped KV heads (GQA / MQA): query head h reads KV head h // (H / H_kv)
+# ---------------------------------------------------------------------------
+def _gqa_inputs(T, H, H_kv, d, seed):
+    return _rand((T, H, d), seed), _rand((T, H_kv, d), seed + 1), _rand((T, H_kv, d), seed + 2)
+
+
+def _sdpa_gqa(q, k, v, do, cu, scale):
+    """torch SDPA with its own grouped-query option (fp64), per sample, and its
+    autograd gradients: an implementation of GQA independent of the oracle."""
+    qs, ks, vs = (x.clone().requires_grad_(True) for x in (q, k, v))
+    outs = []
+    for a, b in zip(cu, cu[1:]):
+        o = torch.nn.functional.scaled_dot_product_attention(
+            qs[a:b].transpose(0, 1), ks[a:b].transpose(0, 1), vs[a:b].transpose(0, 1),
+            is_causal=True, scale=scale, enable_gqa=True)
+        outs.append(o.transpose(0, 1))
+        (o.transpose(0, 1) * do[a:b]).sum().backward()
+    out = torch.cat(outs).detach().numpy()
+    return out, qs.grad.numpy(), ks.grad.numpy(), vs.grad.numpy()
+
+
+@pytest.mark.parametrize("H,H_kv", [(4, 2), (6, 3), (4, 1), (3, 3)])
+def test_gqa_matches_torch_sdpa_enable_gqa(H, H_kv):
+    cu = _cu(3, [10, 6])
+    q, k, v = _gqa_inputs(cu[-1], H, H_kv, 8, 90 + H)
+    do = _rand((cu[-1], H, 8), 95 + H)
+    out, _ = oracle.causal_attention_fwd(q, k, v, cu, 0.45, row_block=4)
+    dq, dk, dv = oracle.causal_attention_bwd(q, k, v, do, cu, 0.45, row_block=4)
+    ro, rq, rk, rv = _sdpa_gqa(q, k, v, do, cu, 0.45)
+    assert dk.shape == (cu[-1], H_kv, 8) and dv.shape == (cu[-1], H_kv, 8)
+    for a, b in ((out, ro), (dq, rq), (dk, rk), (dv, rv)):
+        np.testing.assert_allclose(a, b, rtol=0, atol=1e-11)
+
+
+def test_gqa_fwd_matches_scalar_brute_force():
+    """Scalar loops that pick the KV head of query head h as h // G by hand."""
+    cu = _cu(1, [5])
+    H, H_kv, d = 4, 2, 3
+    q, k, v = _gqa_inputs(cu[-1], H, H_kv, d, 100)
+    out, lse = oracle.causal_attention_fwd(q, k, v, cu, 0.9)
+    for h in range(H):
+        hk = h // (H // H_kv)
+        bo, bl = _brute_force_fwd(q[:, h:h + 1].numpy(), k[:, hk:hk + 1].numpy(),
+                                  v[:, hk:hk + 1].numpy(), cu, 0.9)
+        np.testing.assert_allclose(out[:, h:h + 1], bo, rtol=0, atol=1e-12)
+        np.testing.assert_allclose(lse[h:h + 1], bl, rtol=0, atol=1e-12)
+
+
+def test_gqa_rejects_indivisible_heads():
+    cu = _cu(0, [8])
+    q, k, v = _gqa_inputs(8, 3, 2, 4, 110)
+    with pytest.raises(ValueError):
+        oracle.causal_attention_fwd(q, k, v, cu, 0.5)
+
+
+@pytest.mark.parametrize("P,prefix,texts,H,H_kv", [(2, 4, [8, 16], 4, 2), (3, 5, [12, 0, 24], 6, 2),
+                                                   (4, 2, [32], 4, 1)])
+def test_gqa_partition_invariant_and_prefix_sum(P, prefix, texts, H, H_kv):
+    cu = _cu(prefix, texts)
+    q, k, v = _gqa_inputs(cu[-1], H, H_kv, 4, 120 + P)
+    do = _rand((cu[-1], H, 4), 125 + P)
+    o1, l1 = oracle.causal_attention_fwd(q, k, v, cu, 0.6)
+    o2, l2 = oracle.cp_ring_fwd(q, k, v, cu, prefix, P, 0.6)
+    np.testing.assert_allclose(o2, o1, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(l2, l1, rtol=0, atol=1e-12)
+    _, rq, rk, rv = _sdpa_gqa(q, k, v, do, cu, 0.6)
+    cq, ck, cv, pdk, pdv = oracle.cp_ring_bwd(q, k, v, do, cu, prefix, P, 0.6)
+    for a, b in ((cq, rq), (ck, rk), (cv, rv)):
+        np.testing.assert_allclose(a, b, rtol=0, atol=1e-11)
+    pre = oa._prefix_rows(cu, prefix)
+    assert pdk.shape == (P + 1, len(pre), H_kv, 4)
+    np.testing.assert_allclose(pdk.sum(0), rk[pre], rtol=0, atol=1e-11)
+    np.testing.assert_allclose(pdv.sum(0), rv[pre], rtol=0, atol=1e-11)
