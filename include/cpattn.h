@@ -236,6 +236,43 @@ cp_status_t cp_attn_bwd(const void* q, const void* k, const void* v, const void*
                         void* stream);
 
 /*
+ * cp_attn_fwd_gqa / cp_attn_bwd_gqa -- cp_attn_fwd / cp_attn_bwd with grouped
+ * KV heads (grouped-query attention; H_kv = 1 is multi-query attention).
+ * The pages do not define this variant: every model they describe has one KV
+ * head per query head.  It is the layout of models that keep fewer KV heads,
+ * read this way: query head h attends with KV head h / G, G = H / H_kv (runs
+ * of G consecutive query heads share a KV head).  With H_kv == H these calls
+ * are exactly cp_attn_fwd / cp_attn_bwd.
+ *
+ *   q, out, dout, dq    [T][H][d]          lse [H][T]
+ *   k, v, dk, dv        [T][H_kv][d]       (dk, dv sum the G query heads'
+ *                                           contributions of each KV head)
+ *   prefix_grad_per_rank  NULL or [2][P+1][n_seqs*prefix_len][H_kv][d] fp32
+ *   workspace           >= cp_attn_{fwd,bwd}_workspace_size_gqa(...) bytes
+ * Every other argument, the ring-step order, the merge and the prefix sum
+ * are those of cp_attn_fwd / cp_attn_bwd.
+ * Errors: as cp_attn_fwd / cp_attn_bwd, plus CP_ERR_SHAPE when H_kv < 1 or H
+ * is not a multiple of H_kv.
+ */
+size_t cp_attn_fwd_workspace_size_gqa(cp_dtype_t dt, int T, int H, int H_kv, int d,
+                                      const int32_t* cu_seqlens_h, int n_seqs, int P,
+                                      int prefix_len);
+cp_status_t cp_attn_fwd_gqa(const void* q, const void* k, const void* v, cp_dtype_t dt, int T,
+                            int H, int H_kv, int d, const int32_t* cu_seqlens_h, int n_seqs,
+                            int P, int prefix_len, float softmax_scale, void* out, float* lse,
+                            void* out_lo, void* workspace, size_t ws_bytes, void* stream);
+size_t cp_attn_bwd_workspace_size_gqa(cp_dtype_t dt, int T, int H, int H_kv, int d,
+                                      const int32_t* cu_seqlens_h, int n_seqs, int P,
+                                      int prefix_len);
+cp_status_t cp_attn_bwd_gqa(const void* q, const void* k, const void* v, const void* out,
+                            const void* out_lo, const float* lse, const void* dout,
+                            cp_dtype_t dt, int T, int H, int H_kv, int d,
+                            const int32_t* cu_seqlens_h, int n_seqs, int P, int prefix_len,
+                            float softmax_scale, float* dq, float* dk, float* dv,
+                            float* prefix_grad_per_rank, void* workspace, size_t ws_bytes,
+                            void* stream);
+
+/*
  * cp_workspace_status -- synchronise `stream` and report whether a kernel of
  * the last cp_attn_fwd / cp_attn_bwd call that used `workspace` gave up on a
  * bounded device wait (CP_ERR_TIMEOUT) or CP_OK.

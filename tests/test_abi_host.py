@@ -123,3 +123,26 @@ def test_bad_arguments_return_status(cplib):
     L.cp_zigzag_index(cu, 1, 0, 2, None, None, 0, None)
     assert b"not divisible" in L.cp_last_error()
     assert L.cp_status_string(7) == b"CP_ERR_TIMEOUT"
+
+
+def test_grouped_kv_arguments(cplib):
+    """The grouped-KV entry points: H must be a positive multiple of H_kv, the
+    KV-side workspace shrinks with H_kv, and H_kv == H sizes like the plain
+    calls."""
+    L = cplib
+    cu = B.cu_array([0, 16])
+    assert L.cp_attn_fwd_workspace_size_gqa(1, 16, 6, 4, 128, cu, 1, 2, 0) == 0
+    assert L.cp_attn_bwd_workspace_size_gqa(1, 16, 4, 0, 128, cu, 1, 2, 0) == 0
+    assert L.cp_attn_fwd_workspace_size_gqa(1, 16, 8, 8, 128, cu, 1, 2, 0) == \
+        L.cp_attn_fwd_workspace_size(1, 16, 8, 128, cu, 1, 2, 0)
+    assert L.cp_attn_bwd_workspace_size_gqa(0, 16, 8, 8, 64, cu, 1, 2, 0) == \
+        L.cp_attn_bwd_workspace_size(0, 16, 8, 64, cu, 1, 2, 0)
+    assert 0 < L.cp_attn_fwd_workspace_size_gqa(1, 16, 8, 2, 128, cu, 1, 2, 0) < \
+        L.cp_attn_fwd_workspace_size_gqa(1, 16, 8, 8, 128, cu, 1, 2, 0)
+    fake = ctypes.c_void_p(1 << 20)
+    st = L.cp_attn_fwd_gqa(fake, fake, fake, 1, 16, 6, 4, 128, cu, 1, 2, 0, 1.0, fake, fake,
+                           None, fake, 1 << 20, None)
+    assert st == 2 and b"multiple of H_kv" in L.cp_last_error()
+    st = L.cp_attn_bwd_gqa(fake, fake, fake, fake, None, fake, fake, 1, 16, 4, 3, 128, cu, 1, 2,
+                           0, 1.0, fake, fake, fake, None, fake, 1 << 20, None)
+    assert st == 2

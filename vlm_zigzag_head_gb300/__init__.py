@@ -9,6 +9,7 @@ Functions keep the names of the C entry points:
 
 * :func:`cp_zigzag_index`, :func:`cp_zigzag_gather`, :func:`cp_zigzag_scatter`
 * :func:`cp_attn_fwd`, :func:`cp_lse_merge`, :func:`cp_attn_bwd`
+* :func:`cp_attn_fwd_gqa`, :func:`cp_attn_bwd_gqa` -- grouped KV heads
 * :func:`cp_workspace_status`, :func:`cp_set_wait_limit`, :func:`cp_plan_pairs`
 * :func:`attention_host` -- end-to-end call on host (pinned) tensors.
 """
@@ -23,7 +24,7 @@ from . import _binding as _b
 from ._binding import CP_BF16, CP_F32, CpError  # noqa: F401
 
 __all__ = ["cp_zigzag_index", "cp_zigzag_gather", "cp_zigzag_scatter", "cp_attn_fwd",
-           "cp_attn_fwd_noalloc",
+           "cp_attn_fwd_noalloc", "cp_attn_fwd_gqa", "cp_attn_bwd_gqa",
            "cp_lse_merge", "cp_attn_bwd", "cp_workspace_status", "cp_set_wait_limit",
            "cp_plan_pairs", "cp_profile_begin", "cp_profile_end", "Workspace",
            "attention_host", "CpError"]
@@ -134,9 +135,26 @@ def cp_attn_fwd(q, k, v, cu_seqlens, P: int, prefix_len: int, softmax_scale: flo
     """Context-parallel causal attention forward; returns ``(out, lse)`` with
     out ``[T,H,d]`` (q's dtype) and lse ``[H,T]`` fp32 (natural log).  With
     ``residual=True`` (bf16 only) it returns ``(out, lse, out_lo)``, where
-    out_lo holds the bf16 rounding remainder of out, for :func:`cp_attn_bwd`."""
+    out_lo holds the bf16 rounding remainder of out, for :func:`cp_attn_bwd`.
+    ``k``/``v`` with fewer heads than ``q`` go to :func:`cp_attn_fwd_gqa`."""
+    return _attn_fwd(q, k, v, cu_seqlens, P, prefix_len, softmax_scale, out, lse, workspace,
+                     residual, out_lo, k.shape[1] != q.shape[1])
+
+
+def cp_attn_fwd_gqa(q, k, v, cu_seqlens, P: int, prefix_len: int, softmax_scale: float,
+                    out=None, lse=None, workspace: Optional[Workspace] = None,
+                    residual: bool = False, out_lo=None):
+    """:func:`cp_attn_fwd` with grouped KV heads: ``k``/``v`` are
+    ``[T,H_kv,d]`` and query head h reads KV head ``h // (H / H_kv)``."""
+    return _attn_fwd(q, k, v, cu_seqlens, P, prefix_len, softmax_scale, out, lse, workspace,
+                     residual, out_lo, True)
+
+
+def _attn_fwd(q, k, v, cu_seqlens, P, prefix_len, softmax_scale, out, lse, workspace, residual,
+              out_lo, gqa):
     _need_cuda(q, k, v, out, lse, out_lo)
     T, H, d = q.shape
+    Hkv = k.shape[1]
     dt = _dt(q)
     if out is None:
         out = torch.empty_like(q)
@@ -147,15 +165,24 @@ def cp_attn_fwd(q, k, v, cu_seqlens, P: int, prefix_len: int, softmax_scale: flo
     cu = _b.cu_array(cu_seqlens)
     n = len(cu_seqlens) - 1
     L = _b.lib()
-    nbytes = L.cp_attn_fwd_workspace_size(dt, T, H, d, cu, n, P, prefix_len)
+    if gqa:
+        nbytes = L.cp_attn_fwd_workspace_size_gqa(dt, T, H, Hkv, d, cu, n, P, prefix_len)
+
+        def run(ws_ptr, ws_bytes):
+            return L.cp_attn_fwd_gqa(_ptr(q), _ptr(k), _ptr(v), dt, T, H, Hkv, d, cu, n, P,
+                                     prefix_len, float(softmax_scale), _ptr(out), _ptr(lse),
+                                     _ptr(out_lo), ws_ptr, ws_bytes, _stream(q.device))
+    else:
+        nbytes = L.cp_attn_fwd_workspace_size(dt, T, H, d, cu, n, P, prefix_len)
+
+        def run(ws_ptr, ws_bytes):
+            return L.cp_attn_fwd(_ptr(q), _ptr(k), _ptr(v), dt, T, H, d, cu, n, P, prefix_len,
+                                 float(softmax_scale), _ptr(out), _ptr(lse), _ptr(out_lo),
+                                 ws_ptr, ws_bytes, _stream(q.device))
     if nbytes == 0:  # invalid arguments: let the library name the problem
-        _b.check(L.cp_attn_fwd(_ptr(q), _ptr(k), _ptr(v), dt, T, H, d, cu, n, P, prefix_len,
-                               float(softmax_scale), _ptr(out), _ptr(lse), _ptr(out_lo), None, 0,
-                               _stream(q.device)))
+        _b.check(run(None, 0))
     ws = _ws(workspace, q.device, nbytes, "fwd")
-    _b.check(L.cp_attn_fwd(_ptr(q), _ptr(k), _ptr(v), dt, T, H, d, cu, n, P, prefix_len,
-                           float(softmax_scale), _ptr(out), _ptr(lse), _ptr(out_lo),
-                           ctypes.c_void_p(ws.ptr()), ws.nbytes(), _stream(q.device)))
+    _b.check(run(ctypes.c_void_p(ws.ptr()), ws.nbytes()))
     if residual:
         return out, lse, out_lo
     return out, lse
@@ -199,35 +226,62 @@ def cp_lse_merge(part_out: torch.Tensor, part_lse: torch.Tensor, out_dtype=torch
 def cp_attn_bwd(q, k, v, out, lse, dout, cu_seqlens, P: int, prefix_len: int,
                 softmax_scale: float, per_rank_prefix: bool = False,
                 workspace: Optional[Workspace] = None, grads=None, out_lo=None):
-    """Backward; returns ``(dq, dk, dv)`` fp32 ``[T,H,d]`` and, with
-    ``per_rank_prefix``, the per-rank prefix gradients
-    ``[2, P+1, n*prefix_len, H, d]`` (slot P: prefix queries' own term).
-    ``out_lo``: the remainder returned by ``cp_attn_fwd(..., residual=True)``."""
+    """Backward; returns ``(dq, dk, dv)`` fp32 (dq ``[T,H,d]``, dk/dv shaped
+    like k) and, with ``per_rank_prefix``, the per-rank prefix gradients
+    ``[2, P+1, n*prefix_len, H_kv, d]`` (slot P: prefix queries' own term).
+    ``out_lo``: the remainder returned by ``cp_attn_fwd(..., residual=True)``.
+    ``k``/``v`` with fewer heads than ``q`` go to :func:`cp_attn_bwd_gqa`."""
+    return _attn_bwd(q, k, v, out, lse, dout, cu_seqlens, P, prefix_len, softmax_scale,
+                     per_rank_prefix, workspace, grads, out_lo, k.shape[1] != q.shape[1])
+
+
+def cp_attn_bwd_gqa(q, k, v, out, lse, dout, cu_seqlens, P: int, prefix_len: int,
+                    softmax_scale: float, per_rank_prefix: bool = False,
+                    workspace: Optional[Workspace] = None, grads=None, out_lo=None):
+    """:func:`cp_attn_bwd` with grouped KV heads: dk/dv ``[T,H_kv,d]`` sum the
+    contributions of each KV head's query heads."""
+    return _attn_bwd(q, k, v, out, lse, dout, cu_seqlens, P, prefix_len, softmax_scale,
+                     per_rank_prefix, workspace, grads, out_lo, True)
+
+
+def _attn_bwd(q, k, v, out, lse, dout, cu_seqlens, P, prefix_len, softmax_scale,
+              per_rank_prefix, workspace, grads, out_lo, gqa):
     _need_cuda(q, k, v, out, lse, dout, out_lo)
     T, H, d = q.shape
+    Hkv = k.shape[1]
     dt = _dt(q)
     if grads is None:
-        grads = tuple(torch.empty((T, H, d), dtype=torch.float32, device=q.device)
-                      for _ in range(3))
+        grads = (torch.empty((T, H, d), dtype=torch.float32, device=q.device),
+                 torch.empty((T, Hkv, d), dtype=torch.float32, device=q.device),
+                 torch.empty((T, Hkv, d), dtype=torch.float32, device=q.device))
     dq, dk, dv = grads
     n = len(cu_seqlens) - 1
     pgrad = None
     if per_rank_prefix:
-        pgrad = torch.empty((2, P + 1, n * prefix_len, H, d), dtype=torch.float32,
+        pgrad = torch.empty((2, P + 1, n * prefix_len, Hkv, d), dtype=torch.float32,
                             device=q.device)
     cu = _b.cu_array(cu_seqlens)
     L = _b.lib()
-    nbytes = L.cp_attn_bwd_workspace_size(dt, T, H, d, cu, n, P, prefix_len)
+    if gqa:
+        nbytes = L.cp_attn_bwd_workspace_size_gqa(dt, T, H, Hkv, d, cu, n, P, prefix_len)
+
+        def run(ws_ptr, ws_bytes):
+            return L.cp_attn_bwd_gqa(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(out_lo),
+                                     _ptr(lse), _ptr(dout), dt, T, H, Hkv, d, cu, n, P,
+                                     prefix_len, float(softmax_scale), _ptr(dq), _ptr(dk),
+                                     _ptr(dv), _ptr(pgrad), ws_ptr, ws_bytes, _stream(q.device))
+    else:
+        nbytes = L.cp_attn_bwd_workspace_size(dt, T, H, d, cu, n, P, prefix_len)
+
+        def run(ws_ptr, ws_bytes):
+            return L.cp_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(out_lo), _ptr(lse),
+                                 _ptr(dout), dt, T, H, d, cu, n, P, prefix_len,
+                                 float(softmax_scale), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(pgrad),
+                                 ws_ptr, ws_bytes, _stream(q.device))
     if nbytes == 0:  # invalid arguments: let the library name the problem
-        _b.check(L.cp_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(out_lo), _ptr(lse),
-                               _ptr(dout), dt, T, H, d, cu, n, P, prefix_len,
-                               float(softmax_scale), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(pgrad),
-                               None, 0, _stream(q.device)))
+        _b.check(run(None, 0))
     ws = _ws(workspace, q.device, nbytes, "bwd")
-    _b.check(L.cp_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(out_lo), _ptr(lse),
-                           _ptr(dout), dt, T, H, d, cu, n, P, prefix_len, float(softmax_scale),
-                           _ptr(dq), _ptr(dk), _ptr(dv), _ptr(pgrad), ctypes.c_void_p(ws.ptr()),
-                           ws.nbytes(), _stream(q.device)))
+    _b.check(run(ctypes.c_void_p(ws.ptr()), ws.nbytes()))
     if per_rank_prefix:
         return dq, dk, dv, pgrad
     return dq, dk, dv

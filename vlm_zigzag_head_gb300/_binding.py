@@ -42,6 +42,23 @@ SIGNATURES = {
                                            ctypes.c_int, ctypes.c_int, c_i32p, ctypes.c_int,
                                            ctypes.c_int, ctypes.c_int, ctypes.c_float, c_vp, c_vp,
                                            c_vp, c_vp]),
+    "cp_attn_fwd_workspace_size_gqa": (ctypes.c_size_t, [ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                                         ctypes.c_int, ctypes.c_int, c_i32p,
+                                                         ctypes.c_int, ctypes.c_int,
+                                                         ctypes.c_int]),
+    "cp_attn_fwd_gqa": (ctypes.c_int, [c_vp, c_vp, c_vp, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                       ctypes.c_int, ctypes.c_int, c_i32p, ctypes.c_int,
+                                       ctypes.c_int, ctypes.c_int, ctypes.c_float, c_vp, c_vp,
+                                       c_vp, c_vp, ctypes.c_size_t, c_vp]),
+    "cp_attn_bwd_workspace_size_gqa": (ctypes.c_size_t, [ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                                         ctypes.c_int, ctypes.c_int, c_i32p,
+                                                         ctypes.c_int, ctypes.c_int,
+                                                         ctypes.c_int]),
+    "cp_attn_bwd_gqa": (ctypes.c_int, [c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, ctypes.c_int,
+                                       ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                       c_i32p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                       ctypes.c_float, c_vp, c_vp, c_vp, c_vp, c_vp,
+                                       ctypes.c_size_t, c_vp]),
     "cp_lse_merge": (ctypes.c_int, [ctypes.c_int, c_vp, c_vp, ctypes.c_int, ctypes.c_int,
                                     ctypes.c_int, c_vp, ctypes.c_int, c_vp, c_vp]),
     "cp_attn_bwd_workspace_size": (ctypes.c_size_t, [ctypes.c_int, ctypes.c_int, ctypes.c_int,

@@ -172,15 +172,18 @@ struct FwdWs {
          total = 0;
 };
 
-FwdWs fwd_layout(const PlanSet& ps, int H, int d, size_t elem) {
+FwdWs fwd_layout(const PlanSet& ps, int H, int Hkv, int d, size_t elem) {
   FwdWs w;
   size_t o = 0;
   w.status = o; o += kStatusBytes;
   w.items = o; o = align_up(o + ps.fwd.items.size() * sizeof(FwdItem), 256);
   w.samples = o; o = align_up(o + ps.samples.size() * sizeof(int32_t), 256);
   w.idx = o; o = align_up(o + (size_t)ps.pb.text_rows * sizeof(int32_t), 256);
-  const size_t tb = (size_t)ps.pb.text_rows * H * d * elem;
-  for (int i = 0; i < 3; ++i) { w.qkv[i] = o; o = align_up(o + tb, 256); }
+  // rank-local q [rows][H][d]; k, v [rows][Hkv][d]
+  for (int i = 0; i < 3; ++i) {
+    w.qkv[i] = o;
+    o = align_up(o + (size_t)ps.pb.text_rows * (i == 0 ? H : Hkv) * d * elem, 256);
+  }
   w.o_run = o; o = align_up(o + (size_t)ps.pb.text_rows * H * d * sizeof(float), 256);
   w.lse_run = o; o = align_up(o + (size_t)ps.pb.text_rows * H * sizeof(float), 256);
   w.total = o;
@@ -193,7 +196,7 @@ struct BwdWs {
 
 inline int64_t ld_pitch(int64_t T) { return (T + 3) / 4 * 4; }
 
-BwdWs bwd_layout(const PlanSet& ps, int H, int d, bool simt, bool own_slots) {
+BwdWs bwd_layout(const PlanSet& ps, int H, int Hkv, int d, bool simt, bool own_slots) {
   BwdWs w;
   const Problem& pb = ps.pb;
   size_t o = 0;
@@ -208,16 +211,19 @@ BwdWs bwd_layout(const PlanSet& ps, int H, int d, bool simt, bool own_slots) {
   o = align_up(o + 2 * (size_t)ld_pitch(pb.T) * H * sizeof(float), 256);
   w.slots = o;
   if (own_slots)
-    o = align_up(o + 2ull * (pb.P + 1) * pb.n_seqs * pb.N * H * d * sizeof(float), 256);
+    o = align_up(o + 2ull * (pb.P + 1) * pb.n_seqs * pb.N * Hkv * d * sizeof(float), 256);
   w.total = o;
   return w;
 }
 
 cp_status_t check_common(const void* const* ptrs, int n_ptrs, cp_dtype_t dt, int T, int H,
-                         int d, const int32_t* cu, int n_seqs, int P, int N, float scale) {
+                         int Hkv, int d, const int32_t* cu, int n_seqs, int P, int N,
+                         float scale) {
   if (dt != CP_F32 && dt != CP_BF16) return fail(CP_ERR_DTYPE, "dtype must be CP_F32 or CP_BF16");
   if (T < 0 || H < 1 || n_seqs < 1 || P < 1 || N < 0)
     return fail(CP_ERR_INVALID_ARG, "T >= 0, H >= 1, n_seqs >= 1, P >= 1, prefix_len >= 0");
+  if (Hkv < 1 || H % Hkv != 0)
+    return fail(CP_ERR_SHAPE, "H must be a positive multiple of H_kv");
   if (!cu) return fail(CP_ERR_INVALID_ARG, "cu_seqlens is NULL");
   if (d != 64 && d != 128) return fail(CP_ERR_SHAPE, "head_dim must be 64 or 128");
   if (!std::isfinite(scale)) return fail(CP_ERR_INVALID_ARG, "softmax_scale must be finite");
@@ -371,20 +377,33 @@ cp_status_t cp_zigzag_scatter(const void* src, void* dst, size_t row_bytes, cons
   return CP_OK;
 }
 
+size_t cp_attn_fwd_workspace_size_gqa(cp_dtype_t dt, int T, int H, int Hkv, int d,
+                                      const int32_t* cu, int n_seqs, int P, int N) {
+  std::shared_ptr<PlanSet> ps;
+  if (!cu || H < 1 || Hkv < 1 || H % Hkv != 0 || (dt != CP_F32 && dt != CP_BF16)) return 0;
+  if (get_plans(cu, n_seqs, N, P, T, H, d, &ps) != CP_OK) return 0;
+  return fwd_layout(*ps, H, Hkv, d, dt == CP_BF16 ? 2 : 4).total;
+}
+
 size_t cp_attn_fwd_workspace_size(cp_dtype_t dt, int T, int H, int d, const int32_t* cu,
                                   int n_seqs, int P, int N) {
-  std::shared_ptr<PlanSet> ps;
-  if (!cu || H < 1 || (dt != CP_F32 && dt != CP_BF16)) return 0;
-  if (get_plans(cu, n_seqs, N, P, T, H, d, &ps) != CP_OK) return 0;
-  return fwd_layout(*ps, H, d, dt == CP_BF16 ? 2 : 4).total;
+  return cp_attn_fwd_workspace_size_gqa(dt, T, H, H, d, cu, n_seqs, P, N);
 }
 
 cp_status_t cp_attn_fwd(const void* q, const void* k, const void* v, cp_dtype_t dt, int T, int H,
                         int d, const int32_t* cu, int n_seqs, int P, int N, float scale,
                         void* out, float* lse, void* out_lo, void* ws, size_t ws_bytes,
                         void* stream) {
+  return cp_attn_fwd_gqa(q, k, v, dt, T, H, H, d, cu, n_seqs, P, N, scale, out, lse, out_lo, ws,
+                         ws_bytes, stream);
+}
+
+cp_status_t cp_attn_fwd_gqa(const void* q, const void* k, const void* v, cp_dtype_t dt, int T,
+                            int H, int Hkv, int d, const int32_t* cu, int n_seqs, int P, int N,
+                            float scale, void* out, float* lse, void* out_lo, void* ws,
+                            size_t ws_bytes, void* stream) {
   const void* ptrs[5] = {q, k, v, out, lse};
-  cp_status_t s = check_common(ptrs, 5, dt, T, H, d, cu, n_seqs, P, N, scale);
+  cp_status_t s = check_common(ptrs, 5, dt, T, H, Hkv, d, cu, n_seqs, P, N, scale);
   if (s != CP_OK) return s;
   if (out_lo && dt != CP_BF16) return fail(CP_ERR_DTYPE, "out_lo is for bf16 outputs only");
   if (out_lo && !aligned16(out_lo)) return fail(CP_ERR_ALIGNMENT, "out_lo alignment");
@@ -396,7 +415,7 @@ cp_status_t cp_attn_fwd(const void* q, const void* k, const void* v, cp_dtype_t 
   const bool tc = bf16 && use_tc_path();
   if (tc && (s = check_device_for_bf16()) != CP_OK) return s;
   const size_t elem = bf16 ? 2 : 4;
-  const FwdWs L = fwd_layout(*ps, H, d, elem);
+  const FwdWs L = fwd_layout(*ps, H, Hkv, d, elem);
   if (!ws || ws_bytes < L.total)
     return fail(CP_ERR_WORKSPACE, "workspace smaller than cp_attn_fwd_workspace_size()");
   if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0)
@@ -422,9 +441,18 @@ cp_status_t cp_attn_fwd(const void* q, const void* k, const void* v, cp_dtype_t 
   void* dst[3] = {w + L.qkv[0], w + L.qkv[1], w + L.qkv[2]};
   {
     ProfScope ps_(1, st);
-    CP_CUDA(launch_gather_rows(src, dst, 3, (size_t)H * d * elem, idx, (int)pb.text_rows, false,
-                               st),
-            "zigzag gather");
+    if (Hkv == H) {
+      CP_CUDA(launch_gather_rows(src, dst, 3, (size_t)H * d * elem, idx, (int)pb.text_rows,
+                                 false, st),
+              "zigzag gather");
+    } else {  // q rows and the narrower k / v rows
+      CP_CUDA(launch_gather_rows(src, dst, 1, (size_t)H * d * elem, idx, (int)pb.text_rows,
+                                 false, st),
+              "zigzag gather");
+      CP_CUDA(launch_gather_rows(src + 1, dst + 1, 2, (size_t)Hkv * d * elem, idx,
+                                 (int)pb.text_rows, false, st),
+              "zigzag gather");
+    }
   }
   const FwdItem* items = reinterpret_cast<const FwdItem*>(w + L.items);
   float* o_run = reinterpret_cast<float*>(w + L.o_run);
@@ -434,14 +462,15 @@ cp_status_t cp_attn_fwd(const void* q, const void* k, const void* v, cp_dtype_t 
     const char* terr = nullptr;
     const int64_t PR = pb.text_rows;
     bool ok = make_tmap_thd(&a.tm_q_text, dst[0], PR, H, d, 128, &terr) &&
-              make_tmap_thd(&a.tm_k_text, dst[1], PR, H, d, 128, &terr) &&
-              make_tmap_thd(&a.tm_v_text, dst[2], PR, H, d, 128, &terr) &&
+              make_tmap_thd(&a.tm_k_text, dst[1], PR, Hkv, d, 128, &terr) &&
+              make_tmap_thd(&a.tm_v_text, dst[2], PR, Hkv, d, 128, &terr) &&
               make_tmap_thd(&a.tm_q_nat, q, T, H, d, 128, &terr) &&
-              make_tmap_thd(&a.tm_k_nat, k, T, H, d, 128, &terr) &&
-              make_tmap_thd(&a.tm_v_nat, v, T, H, d, 128, &terr);
+              make_tmap_thd(&a.tm_k_nat, k, T, Hkv, d, 128, &terr) &&
+              make_tmap_thd(&a.tm_v_nat, v, T, Hkv, d, 128, &terr);
     if (!ok) return fail(CP_ERR_CUDA, std::string("tensor map: ") + (terr ? terr : "?"));
-    a.H = H; a.d = d;
+    a.H = H; a.Hkv = Hkv; a.d = d;
     a.scale_log2 = scale * 1.4426950408889634f;
+    a.split_p = scale > kPrecisionSplitScale ? 1 : 0;
     a.o_run = o_run; a.lse_run = lse_run; a.run_rows = PR;
     a.out = out; a.lse = lse; a.T = T; a.out_lo = out_lo;
     a.status = reinterpret_cast<int32_t*>(w + L.status);
@@ -457,7 +486,7 @@ cp_status_t cp_attn_fwd(const void* q, const void* k, const void* v, cp_dtype_t 
   SimtFwdArgs a;
   a.q_text = dst[0]; a.k_text = dst[1]; a.v_text = dst[2];
   a.q_nat = q; a.k_nat = k; a.v_nat = v;
-  a.H = H; a.d = d; a.scale = scale;
+  a.H = H; a.Hkv = Hkv; a.d = d; a.scale = scale;
   a.o_run = o_run; a.lse_run = lse_run; a.run_rows = pb.text_rows;
   a.out = out; a.lse = lse; a.T = T;
   for (int step = 0; step < P; ++step) {
@@ -486,13 +515,18 @@ cp_status_t cp_lse_merge(int n_parts, const float* part_out, const float* part_l
   return CP_OK;
 }
 
-size_t cp_attn_bwd_workspace_size(cp_dtype_t dt, int T, int H, int d, const int32_t* cu,
-                                  int n_seqs, int P, int N) {
+size_t cp_attn_bwd_workspace_size_gqa(cp_dtype_t dt, int T, int H, int Hkv, int d,
+                                      const int32_t* cu, int n_seqs, int P, int N) {
   std::shared_ptr<PlanSet> ps;
-  if (!cu || H < 1 || (dt != CP_F32 && dt != CP_BF16)) return 0;
+  if (!cu || H < 1 || Hkv < 1 || H % Hkv != 0 || (dt != CP_F32 && dt != CP_BF16)) return 0;
   if (get_plans(cu, n_seqs, N, P, T, H, d, &ps) != CP_OK) return 0;
   const bool simt = !(dt == CP_BF16 && use_tc_path() && d == 128);
-  return bwd_layout(*ps, H, d, simt, true).total;
+  return bwd_layout(*ps, H, Hkv, d, simt, true).total;
+}
+
+size_t cp_attn_bwd_workspace_size(cp_dtype_t dt, int T, int H, int d, const int32_t* cu,
+                                  int n_seqs, int P, int N) {
+  return cp_attn_bwd_workspace_size_gqa(dt, T, H, H, d, cu, n_seqs, P, N);
 }
 
 cp_status_t cp_attn_bwd(const void* q, const void* k, const void* v, const void* out,
@@ -501,8 +535,17 @@ cp_status_t cp_attn_bwd(const void* q, const void* k, const void* v, const void*
                         const int32_t* cu, int n_seqs, int P, int N, float scale, float* dq,
                         float* dk, float* dv, float* pgrad, void* ws, size_t ws_bytes,
                         void* stream) {
+  return cp_attn_bwd_gqa(q, k, v, out, out_lo, lse, dout, dt, T, H, H, d, cu, n_seqs, P, N,
+                         scale, dq, dk, dv, pgrad, ws, ws_bytes, stream);
+}
+
+cp_status_t cp_attn_bwd_gqa(const void* q, const void* k, const void* v, const void* out,
+                            const void* out_lo, const float* lse, const void* dout,
+                            cp_dtype_t dt, int T, int H, int Hkv, int d, const int32_t* cu,
+                            int n_seqs, int P, int N, float scale, float* dq, float* dk,
+                            float* dv, float* pgrad, void* ws, size_t ws_bytes, void* stream) {
   const void* ptrs[9] = {q, k, v, out, lse, dout, dq, dk, dv};
-  cp_status_t s = check_common(ptrs, 9, dt, T, H, d, cu, n_seqs, P, N, scale);
+  cp_status_t s = check_common(ptrs, 9, dt, T, H, Hkv, d, cu, n_seqs, P, N, scale);
   if (s != CP_OK) return s;
   if (pgrad && !aligned16(pgrad)) return fail(CP_ERR_ALIGNMENT, "prefix_grad_per_rank alignment");
   if (out_lo && dt != CP_BF16) return fail(CP_ERR_DTYPE, "out_lo is for bf16 outputs only");
@@ -515,7 +558,7 @@ cp_status_t cp_attn_bwd(const void* q, const void* k, const void* v, const void*
   // the tensor-core backward is built for head_dim 128; head_dim 64 runs on CUDA cores
   const bool tc = bf16 && use_tc_path() && d == 128;
   if (tc && (s = check_device_for_bf16()) != CP_OK) return s;
-  const BwdWs L = bwd_layout(*ps, H, d, !tc, pgrad == nullptr);
+  const BwdWs L = bwd_layout(*ps, H, Hkv, d, !tc, pgrad == nullptr);
   if (!ws || ws_bytes < L.total)
     return fail(CP_ERR_WORKSPACE, "workspace smaller than cp_attn_bwd_workspace_size()");
   if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0)
@@ -526,7 +569,7 @@ cp_status_t cp_attn_bwd(const void* q, const void* k, const void* v, const void*
   const int64_t pre_rows = (int64_t)n_seqs * N;
   float* slots = pgrad ? pgrad : reinterpret_cast<float*>(w + L.slots);
   float* pre_k = slots;
-  float* pre_v = slots + (size_t)(P + 1) * pre_rows * H * d;
+  float* pre_v = slots + (size_t)(P + 1) * pre_rows * Hkv * d;
   float* Dd = reinterpret_cast<float*>(w + L.D);
   float* lse2 = reinterpret_cast<float*>(w + L.lse2);
   CP_CUDA(cudaMemsetAsync(w + L.status, 0, kStatusBytes, st), "clear status");
@@ -546,13 +589,13 @@ cp_status_t cp_attn_bwd(const void* q, const void* k, const void* v, const void*
     TcBwdArgs a;
     const char* terr = nullptr;
     bool ok = make_tmap_thd(&a.tm_q, q, T, H, d, kBwdTileQ, &terr) &&
-              make_tmap_thd(&a.tm_k, k, T, H, d, kBwdTileK, &terr) &&
-              make_tmap_thd(&a.tm_v, v, T, H, d, kBwdTileK, &terr) &&
+              make_tmap_thd(&a.tm_k, k, T, Hkv, d, kBwdTileK, &terr) &&
+              make_tmap_thd(&a.tm_v, v, T, Hkv, d, kBwdTileK, &terr) &&
               make_tmap_thd(&a.tm_do, dout, T, H, d, kBwdTileQ, &terr) &&
               make_tmap_ld(&a.tm_ld, lse2, pitch, H, kBwdTileQ + 4, &terr) &&
               make_tmap_f32_thd(&a.tm_dq, dq, T, H, d, 16, &terr);
     if (!ok) return fail(CP_ERR_CUDA, std::string("tensor map: ") + (terr ? terr : "?"));
-    a.H = H; a.d = d; a.scale = scale; a.scale_log2 = scale * 1.4426950408889634f;
+    a.H = H; a.Hkv = Hkv; a.d = d; a.scale = scale; a.scale_log2 = scale * 1.4426950408889634f;
     a.T = T;
     a.dq = dq; a.dk = dk; a.dv = dv;
     a.pre_k = pre_k; a.pre_v = pre_v; a.pre_rows = pre_rows;
@@ -571,7 +614,7 @@ cp_status_t cp_attn_bwd(const void* q, const void* k, const void* v, const void*
     const FwdItem* qitems = reinterpret_cast<const FwdItem*>(w + L.qitems);
     SimtBwdArgs a;
     a.q = q; a.k = k; a.v = v; a.dout = dout; a.D = Dd; a.lse2 = lse2; a.pitch = pitch;
-    a.H = H; a.d = d; a.scale = scale; a.T = T;
+    a.H = H; a.Hkv = Hkv; a.d = d; a.scale = scale; a.T = T;
     a.dq = dq; a.dk = dk; a.dv = dv; a.pre_k = pre_k; a.pre_v = pre_v; a.pre_rows = pre_rows;
     for (int step = 0; step < P; ++step) {
       a.q_items = qitems + ps->fwd_nat.step_begin[step];
@@ -587,7 +630,7 @@ cp_status_t cp_attn_bwd(const void* q, const void* k, const void* v, const void*
     // the AllReduce of the replicated prefix gradient: fixed-order sum of slots
     ProfScope ps_(5, st);
     CP_CUDA(launch_prefix_reduce(pre_k, pre_v, P + 1, reinterpret_cast<const int32_t*>(w + L.cu),
-                                 n_seqs, N, H, d, dk, dv, st),
+                                 n_seqs, N, Hkv, d, dk, dv, st),
             "prefix gradient sum");
   }
   return CP_OK;

@@ -54,6 +54,7 @@ __global__ void __launch_bounds__(kSimtQ) simt_fwd_kernel(SimtFwdArgs a) {
   if (t == 0) it = a.items[blockIdx.x];
   __syncthreads();
   const int H = a.H;
+  const int Hkv = a.Hkv, hk = h / (H / Hkv);   // the KV head this query head reads
   const T* qsrc = static_cast<const T*>(it.q_src == SRC_TEXT ? a.q_text : a.q_nat);
   for (int x = t; x < kSimtQ * D; x += kSimtQ) {
     const int row = x / D, e = x - row * D;
@@ -75,7 +76,7 @@ __global__ void __launch_bounds__(kSimtQ) simt_fwd_kernel(SimtFwdArgs a) {
       for (int x = t; x < kSimtKT * D; x += kSimtQ) {
         const int u = x / D, e = x - u * D;
         const bool in = u0 + u < nkeys;
-        const long long g = ((long long)(s.row0 + u0 + u) * H + h) * D + e;
+        const long long g = ((long long)(s.row0 + u0 + u) * Hkv + hk) * D + e;
         Ks[x] = in ? ld_f(ksrc + g) : 0.f;
         Vs[x] = in ? ld_f(vsrc + g) : 0.f;
       }
@@ -158,6 +159,7 @@ __global__ void __launch_bounds__(kSimtQ) simt_bwd_dq_kernel(SimtBwdArgs a, int 
   if (t == 0) it = a.q_items[first_item + blockIdx.x];
   __syncthreads();
   const int H = a.H;
+  const int Hkv = a.Hkv, hk = h / (H / Hkv);   // the KV head this query head reads
   const T* q = static_cast<const T*>(a.q);
   const T* k = static_cast<const T*>(a.k);
   const T* v = static_cast<const T*>(a.v);
@@ -184,7 +186,7 @@ __global__ void __launch_bounds__(kSimtQ) simt_bwd_dq_kernel(SimtBwdArgs a, int 
       for (int x = t; x < kSimtKT * D; x += kSimtQ) {
         const int u = x / D, e = x - u * D;
         const bool in = u0 + u < nkeys;
-        const long long g = ((long long)(s.row0 + u0 + u) * H + h) * D + e;
+        const long long g = ((long long)(s.row0 + u0 + u) * Hkv + hk) * D + e;
         Ks[x] = in ? ld_f(k + g) : 0.f;
         Vs[x] = in ? ld_f(v + g) : 0.f;
       }
@@ -233,12 +235,12 @@ __global__ void __launch_bounds__(2 * kBwdTileK) simt_bwd_dkdv_kernel(SimtBwdArg
   float* Ls = dOs + kSimtQT * D;             // [kSimtQT]
   float* Dsm = Ls + kSimtQT;                 // [kSimtQT]
   __shared__ BwdItem it;
-  const int h = blockIdx.y;
+  const int hk = blockIdx.y;                 // KV head; its query heads are hk*G .. hk*G+G-1
   const int tid = threadIdx.x;
   const int u = tid >> 1, half = tid & 1;
   if (tid == 0) it = a.k_items[first_item + blockIdx.x];
   __syncthreads();
-  const int H = a.H;
+  const int H = a.H, Hkv = a.Hkv, G = H / Hkv;
   const T* q = static_cast<const T*>(a.q);
   const T* k = static_cast<const T*>(a.k);
   const T* v = static_cast<const T*>(a.v);
@@ -246,7 +248,7 @@ __global__ void __launch_bounds__(2 * kBwdTileK) simt_bwd_dkdv_kernel(SimtBwdArg
   for (int x = tid; x < kBwdTileK * D; x += 2 * kBwdTileK) {
     const int row = x / D, e = x - row * D;
     const bool in = row < it.k_len;
-    const long long g = ((long long)(it.k_row0 + row) * H + h) * D + e;
+    const long long g = ((long long)(it.k_row0 + row) * Hkv + hk) * D + e;
     Ks[row * (D + 1) + e] = in ? ld_f(k + g) : 0.f;
     Vs[row * (D + 1) + e] = in ? ld_f(v + g) : 0.f;
   }
@@ -254,43 +256,46 @@ __global__ void __launch_bounds__(2 * kBwdTileK) simt_bwd_dkdv_kernel(SimtBwdArg
 #pragma unroll
   for (int e = 0; e < HD; ++e) dk[e] = dv[e] = 0.f;
   const bool valid = u < it.k_len;
-  for (int sg = 0; sg < it.nseg; ++sg) {
-    const Seg s = it.seg[sg];
-    const int t_begin = s.causal ? (s.delta < 0 ? -s.delta : 0) : 0;
-    for (int t0 = t_begin; t0 < s.len; t0 += kSimtQT) {
-      __syncthreads();
-      for (int x = tid; x < kSimtQT * D; x += 2 * kBwdTileK) {
-        const int row = x / D, e = x - row * D;
-        const bool in = t0 + row < s.len;
-        const long long g = ((long long)(s.row0 + t0 + row) * H + h) * D + e;
-        Qs[x] = in ? ld_f(q + g) : 0.f;
-        dOs[x] = in ? ld_f(dout + g) : 0.f;
-      }
-      for (int x = tid; x < kSimtQT; x += 2 * kBwdTileK) {
-        const bool in = t0 + x < s.len;
-        const long long g = (long long)h * a.pitch + s.row0 + t0 + x;
-        Ls[x] = in ? a.lse2[g] : 0.f;
-        Dsm[x] = in ? a.D[g] : 0.f;
-      }
-      __syncthreads();
-      for (int tq = 0; tq < kSimtQT; ++tq) {
-        const int tt = t0 + tq;
-        float pk = 0.f, pv = 0.f;
-#pragma unroll 8
-        for (int e = 0; e < HD; ++e) {
-          pk += Qs[tq * D + half * HD + e] * Ks[u * (D + 1) + half * HD + e];
-          pv += dOs[tq * D + half * HD + e] * Vs[u * (D + 1) + half * HD + e];
+  for (int gi = 0; gi < G; ++gi) {
+    const int h = hk * G + gi;
+    for (int sg = 0; sg < it.nseg; ++sg) {
+      const Seg s = it.seg[sg];
+      const int t_begin = s.causal ? (s.delta < 0 ? -s.delta : 0) : 0;
+      for (int t0 = t_begin; t0 < s.len; t0 += kSimtQT) {
+        __syncthreads();
+        for (int x = tid; x < kSimtQT * D; x += 2 * kBwdTileK) {
+          const int row = x / D, e = x - row * D;
+          const bool in = t0 + row < s.len;
+          const long long g = ((long long)(s.row0 + t0 + row) * H + h) * D + e;
+          Qs[x] = in ? ld_f(q + g) : 0.f;
+          dOs[x] = in ? ld_f(dout + g) : 0.f;
         }
-        pk += __shfl_xor_sync(0xffffffffu, pk, 1);
-        pv += __shfl_xor_sync(0xffffffffu, pv, 1);
-        const bool vis = valid && tt < s.len && (!s.causal || u <= tt + s.delta);
-        if (!vis) continue;
-        const float p = exp2f(pk * a.scale * kLog2e - Ls[tq]);
-        const float ds = p * (pv - Dsm[tq]) * a.scale;
+        for (int x = tid; x < kSimtQT; x += 2 * kBwdTileK) {
+          const bool in = t0 + x < s.len;
+          const long long g = (long long)h * a.pitch + s.row0 + t0 + x;
+          Ls[x] = in ? a.lse2[g] : 0.f;
+          Dsm[x] = in ? a.D[g] : 0.f;
+        }
+        __syncthreads();
+        for (int tq = 0; tq < kSimtQT; ++tq) {
+          const int tt = t0 + tq;
+          float pk = 0.f, pv = 0.f;
+#pragma unroll 8
+          for (int e = 0; e < HD; ++e) {
+            pk += Qs[tq * D + half * HD + e] * Ks[u * (D + 1) + half * HD + e];
+            pv += dOs[tq * D + half * HD + e] * Vs[u * (D + 1) + half * HD + e];
+          }
+          pk += __shfl_xor_sync(0xffffffffu, pk, 1);
+          pv += __shfl_xor_sync(0xffffffffu, pv, 1);
+          const bool vis = valid && tt < s.len && (!s.causal || u <= tt + s.delta);
+          if (!vis) continue;
+          const float p = exp2f(pk * a.scale * kLog2e - Ls[tq]);
+          const float ds = p * (pv - Dsm[tq]) * a.scale;
 #pragma unroll
-        for (int e = 0; e < HD; ++e) {
-          dv[e] += p * dOs[tq * D + half * HD + e];
-          dk[e] += ds * Qs[tq * D + half * HD + e];
+          for (int e = 0; e < HD; ++e) {
+            dv[e] += p * dOs[tq * D + half * HD + e];
+            dk[e] += ds * Qs[tq * D + half * HD + e];
+          }
         }
       }
     }
@@ -298,12 +303,12 @@ __global__ void __launch_bounds__(2 * kBwdTileK) simt_bwd_dkdv_kernel(SimtBwdArg
   if (!valid) return;
   float *pk, *pv;
   if (it.dk_mode == DK_TEXT) {
-    pk = a.dk + ((long long)(it.k_row0 + u) * H + h) * D + half * HD;
-    pv = a.dv + ((long long)(it.k_row0 + u) * H + h) * D + half * HD;
+    pk = a.dk + ((long long)(it.k_row0 + u) * Hkv + hk) * D + half * HD;
+    pv = a.dv + ((long long)(it.k_row0 + u) * Hkv + hk) * D + half * HD;
   } else {
     const long long row = (long long)it.slot * a.pre_rows + it.dk_row0 + u;
-    pk = a.pre_k + (row * H + h) * D + half * HD;
-    pv = a.pre_v + (row * H + h) * D + half * HD;
+    pk = a.pre_k + (row * Hkv + hk) * D + half * HD;
+    pv = a.pre_v + (row * Hkv + hk) * D + half * HD;
   }
   if (it.flags & F_FIRST) {
 #pragma unroll
@@ -343,7 +348,7 @@ cudaError_t dkdv_t(const SimtBwdArgs& a, cudaStream_t st) {
       sizeof(float) * (2 * kBwdTileK * (D + 1) + 2 * kSimtQT * D + 2 * kSimtQT);
   cudaError_t e = set_smem(simt_bwd_dkdv_kernel<T, D>, sm);
   if (e != cudaSuccess) return e;
-  simt_bwd_dkdv_kernel<T, D><<<dim3(a.n_k_items, a.H), 2 * kBwdTileK, sm, st>>>(a, 0);
+  simt_bwd_dkdv_kernel<T, D><<<dim3(a.n_k_items, a.Hkv), 2 * kBwdTileK, sm, st>>>(a, 0);
   return cudaGetLastError();
 }
 

@@ -41,6 +41,7 @@ struct SimtFwdArgs {
   const void* q_nat; const void* k_nat; const void* v_nat;     // SRC_NAT tensors
   const FwdItem* items; int n_items;
   int H, d; float scale;
+  int Hkv;                                          // KV heads (query head h reads h / (H / Hkv))
   float* o_run; float* lse_run; int64_t run_rows;   // [H][run_rows][d], [H][run_rows]
   void* out; float* lse; int64_t T;                 // natural order
 };
@@ -50,10 +51,11 @@ struct SimtBwdArgs {
   const void* q; const void* k; const void* v; const void* dout;  // natural order
   const float* D; const float* lse2; int64_t pitch;               // [H][pitch]
   int H, d; float scale; int64_t T;
+  int Hkv;                                 // KV heads; dK/dV sum each group's query heads
   const FwdItem* q_items; int n_q_items;   // dQ pass (natural-order forward plan)
   const BwdItem* k_items; int n_k_items;   // dK/dV pass
   float* dq; float* dk; float* dv;
-  float* pre_k; float* pre_v; int64_t pre_rows;   // [P+1][pre_rows][H][d]
+  float* pre_k; float* pre_v; int64_t pre_rows;   // [P+1][pre_rows][Hkv][d]
 };
 cudaError_t launch_simt_bwd_dq(const SimtBwdArgs& a, bool bf16, cudaStream_t st);
 cudaError_t launch_simt_bwd_dkdv(const SimtBwdArgs& a, bool bf16, cudaStream_t st);

@@ -158,8 +158,9 @@ extern "C" cp_status_t cp_attn_fwd_noalloc(const void* q, const void* k, const v
                     make_tmap_thd(&a.tm_k_nat, k, T, H, d, 128, &terr) &&
                     make_tmap_thd(&a.tm_v_nat, v, T, H, d, 128, &terr);
     if (!ok) return fail(CP_ERR_CUDA, std::string("tensor map: ") + (terr ? terr : "?"));
-    a.H = H; a.d = d;
+    a.H = H; a.Hkv = H; a.d = d;
     a.scale_log2 = scale * 1.4426950408889634f;
+    a.split_p = scale > kPrecisionSplitScale ? 1 : 0;
     a.o_run = orun; a.lse_run = lrun; a.run_rows = PR;
     a.out = out; a.lse = lse; a.T = T; a.out_lo = out_lo;
     a.status = reinterpret_cast<int32_t*>(w + o_status);
@@ -174,7 +175,7 @@ extern "C" cp_status_t cp_attn_fwd_noalloc(const void* q, const void* k, const v
   SimtFwdArgs a;
   a.q_text = dst[0]; a.k_text = dst[1]; a.v_text = dst[2];
   a.q_nat = q; a.k_nat = k; a.v_nat = v;
-  a.H = H; a.d = d; a.scale = scale;
+  a.H = H; a.Hkv = H; a.d = d; a.scale = scale;
   a.o_run = orun; a.lse_run = lrun; a.run_rows = pb.text_rows;
   a.out = out; a.lse = lse; a.T = T;
   for (int step = 0; step < P; ++step) {

@@ -8,6 +8,12 @@
 
 namespace cpattn {
 
+// Softmax scales above this make dQ = scale * dS K large enough that one bf16
+// rounding of a probability-sized operand (P in the forward's PV product, dS
+// in the backward's dQ product) shows in dQ; both kernels then carry that
+// operand as a bf16 hi + lo pair.
+constexpr float kPrecisionSplitScale = 0.25f;
+
 // 3-D tensor map over a bf16 [rows][H][d] tensor, box {64, 1, rows_per_box},
 // 128-byte swizzle.  Returns false (and a message) if encoding fails.
 bool make_tmap_thd(CUtensorMap* map, const void* base, int64_t rows, int H, int d,
@@ -26,7 +32,9 @@ struct TcFwdArgs {
   CUtensorMap tm_q_nat, tm_k_nat, tm_v_nat;     // natural order (prefix rows)
   const FwdItem* items;
   int n_items, H, d;
+  int Hkv;                    // KV heads; query head h reads KV head h / (H / Hkv)
   float scale_log2;           // softmax scale * log2(e)
+  int split_p;                // P enters PV as bf16 hi + lo (softmax scale > kPrecisionSplitScale)
   float* o_run; float* lse_run; int64_t run_rows;
   void* out; float* lse; int64_t T;
   void* out_lo;               // nullable: bf16 remainder o - bf16(o)
@@ -41,6 +49,7 @@ struct TcBwdArgs {
   CUtensorMap tm_dq;                     // dq fp32 [T][H][d], box {d, 1, 16}: reduce-add target
   const BwdItem* items;
   int n_items, H, d;
+  int Hkv;                    // KV heads; one CTA per (key tile, KV head) walks its H / Hkv query heads
   float scale, scale_log2;
   int64_t T;
   float* dq; float* dk; float* dv;

@@ -1,7 +1,8 @@
 // Ring-step attention backward on 5th-generation tensor cores (sm_103a).
 //
-// One CTA owns one key tile (128 keys, one head) of a ring step and walks the
-// query runs that met those keys at that step (page
+// One CTA owns one key tile (128 keys of one KV head) of a ring step and walks
+// the query runs that met those keys at that step, for every query head that
+// reads this KV head (one head without grouped KV heads) (page
 // "context-parallel-multimodal" §4.2: each rank differentiates its queries
 // against the KV it saw; the KV owner receives dK/dV; the replicated prefix
 // gets one gradient per rank).  Per 64-row query tile, with the final lse:
@@ -54,7 +55,6 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0, kColDP = 64, kColDQ0 = 128, kColDQ1 = 192, kColDK = 256,
                    kColDV = 384;
 constexpr long long kDrainLimit = 1LL << 24;
-constexpr float kSplitScale = 0.25f;  // softmax scales above this use the dS hi + lo split
 
 template <bool kSplit>
 struct Lay {
@@ -134,7 +134,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
   Bars* bars = reinterpret_cast<Bars*>(smem + L::kBars);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int item_idx = blockIdx.x % a.n_items;
-  const int h = blockIdx.x / a.n_items;
+  const int hk = blockIdx.x / a.n_items;   // KV head; its query heads are hk*G .. hk*G+G-1
+  const int G = a.H / a.Hkv;
   BwdItem& it = *reinterpret_cast<BwdItem*>(smem + L::kItem);
   if (warp == 0)  // the work item, copied once into shared memory (128 bytes)
     reinterpret_cast<uint32_t*>(&it)[lane] =
@@ -175,24 +176,25 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
   const uint32_t tmem = bars->tmem_base;
 
   const int nseg = it.nseg;
-  int n_qt = 0;
+  int n_qt = 0;   // query tiles of one query head
   for (int s = 0; s < nseg; ++s) n_qt += run_qtiles(it.seg[s]);
-  // Every role walks the query tiles in the same order.  Concurrent CTAs are
-  // neighbouring key tiles of one head that meet the same queries in the same
-  // order, so the Q / dO tiles they load are shared through L2 (a rotated
-  // order per CTA measured slower).
-  const int rot = 0;
+  // Every role walks the same G * n_qt query tiles in the same order: query
+  // head hk*G + j / n_qt, tile j % n_qt.  dK / dV of the KV head accumulate
+  // over all of them.  Concurrent CTAs are neighbouring key tiles that meet
+  // the same queries in the same order, so the Q / dO tiles they load are
+  // shared through L2 (a rotated order per CTA measured slower).
+  const int n_all = G * n_qt;
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     int issued = 0;
     bool kv_issued = false;
-    if (n_qt > 0) {
+    if (n_all > 0) {
       if (lane == 0) {
         mbar_expect_tx(&bars->kv_full, 4 * L::kKVBox);
         for (int b = 0; b < 2; ++b) {
-          tma_load_3d(&a.tm_k, &bars->kv_full, smem + L::kK + b * L::kKVBox, b * 64, h, it.k_row0);
-          tma_load_3d(&a.tm_v, &bars->kv_full, smem + L::kV + b * L::kKVBox, b * 64, h, it.k_row0);
+          tma_load_3d(&a.tm_k, &bars->kv_full, smem + L::kK + b * L::kKVBox, b * 64, hk, it.k_row0);
+          tma_load_3d(&a.tm_v, &bars->kv_full, smem + L::kV + b * L::kKVBox, b * 64, hk, it.k_row0);
         }
       }
       kv_issued = true;
@@ -200,11 +202,12 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
     // decisions are taken by lane 0 and broadcast: the warp never diverges
     // around the __syncwarp below
     bool go = true;
-    for (int j = 0; go && j < n_qt; ++j) {
+    int jt = 0, hq = hk * G;   // tile j: tile jt of query head hq
+    for (int j = 0; go && j < n_all; ++j, jt = jt + 1 == n_qt ? 0 : jt + 1, hq += jt == 0) {
       {
         Seg sg;
         int q0, t;
-        tile_of(it, (j + rot) % n_qt, sg, q0, t);
+        tile_of(it, jt, sg, q0, t);
         const int st = j % kStages;
         int w_ok = 1;
         if (lane == 0) {
@@ -222,11 +225,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
           mbar_expect_tx(&bars->qdo_full[st], 4 * L::kQBox + L::kLdBytes);
           for (int b = 0; b < 2; ++b) {
             tma_load_3d(&a.tm_q, &bars->qdo_full[st], smem + L::kQ + (st * 2 + b) * L::kQBox,
-                        b * 64, h, grow);
+                        b * 64, hq, grow);
             tma_load_3d(&a.tm_do, &bars->qdo_full[st], smem + L::kDO + (st * 2 + b) * L::kQBox,
-                        b * 64, h, grow);
+                        b * 64, hq, grow);
           }
-          tma_load_3d(&a.tm_ld, &bars->qdo_full[st], smem + L::kLd + st * 1024, grow & ~3, h, 0);
+          tma_load_3d(&a.tm_ld, &bars->qdo_full[st], smem + L::kLd + st * 1024, grow & ~3, hq, 0);
         }
         issued = j + 1;
       }
@@ -248,7 +251,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
       constexpr uint32_t idesc_kv = idesc_bf16(kBK, kD, 0, 1);     // B (Q, dO) MN-major
       constexpr uint32_t idesc_dq = idesc_bf16(kD, kBQ, 1, 1);     // A (K^T), B (dS^T) MN-major
       const uint32_t k_addr = smem_u32(smem + L::kK), v_addr = smem_u32(smem + L::kV);
-      bool ok = n_qt == 0 || mbar_wait(&bars->kv_full, 0, lim, abort);
+      bool ok = n_all == 0 || mbar_wait(&bars->kv_full, 0, lim, abort);
       auto issue_grads = [&](int i) -> bool {
         const int st = i % kStages, b = i & 1;
         if (!mbar_wait(&bars->ps_full, i & 1, lim, abort)) return false;
@@ -282,7 +285,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
         mma_commit(&bars->dq_full[b]);
         return true;
       };
-      for (int i = 0; ok && i < n_qt; ++i) {
+      for (int i = 0; ok && i < n_all; ++i) {
         const int st = i % kStages;
         if (!mbar_wait(&bars->qdo_full[st], (i / kStages) & 1, lim, abort) ||
             (i >= 1 && !mbar_wait(&bars->sdp_empty, (i - 1) & 1, lim, abort))) {
@@ -307,8 +310,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
           break;
         }
       }
-      if (ok && n_qt > 0 && !issue_grads(n_qt - 1)) ok = false;
-      if (ok && n_qt > 0) mma_commit(&bars->dkv_done);
+      if (ok && n_all > 0 && !issue_grads(n_all - 1)) ok = false;
+      if (ok && n_all > 0) mma_commit(&bars->dkv_done);
       if (!ok) {
         record_timeout(a.status, abort, 12);
         mma_commit(&bars->drain);
@@ -328,14 +331,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
     constexpr int N = L::kNumStg;
     bool ok = true;
     int k = 0;                                   // round counter
-    for (int j = 0; ok && j < n_qt; ++j) {
-      Seg sgd;
-      int q0d, td;
-      tile_of(it, (j + rot) % n_qt, sgd, q0d, td);
+    for (int j = 0; ok && j < n_all; ++j) {
       const int b = j & 1;
       if (!mbar_wait(&bars->dq_full[b], (j >> 1) & 1, lim, abort)) { ok = false; break; }
       tc_fence_after();
-      const int grow = sgd.row0 + q0d + td * kBQ;  // natural row of the tile's first query
       // the whole dQ^T tile (64 query columns) into registers first, so its
       // TMEM buffer is free for the next dQ product before any staging
       uint32_t r[2][32];
@@ -372,11 +371,12 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
       constexpr int N = L::kNumStg;
       bool ok = true;
       int k = 0;
-      for (int j = 0; ok && j < n_qt; ++j) {
+      int jt = 0, hq = hk * G;   // tile j: tile jt of query head hq
+      for (int j = 0; ok && j < n_all; ++j, jt = jt + 1 == n_qt ? 0 : jt + 1, hq += jt == 0) {
         Seg sgd;
         int q0d, td;
-        tile_of(it, (j + rot) % n_qt, sgd, q0d, td);
-        const int grow = sgd.row0 + q0d + td * kBQ;
+        tile_of(it, jt, sgd, q0d, td);
+        const int grow = sgd.row0 + q0d + td * kBQ;   // natural row of the tile's first query
         for (int r4 = 0; r4 < 4; ++r4, ++k) {
           const int sb = k % N;
           if (!mbar_wait(&bars->stg_full[sb], (k / N) & 1, lim, abort)) {
@@ -385,7 +385,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
           }
           // rows past the run carry exact zeros (P = 0 there); rows past T are
           // clipped by the tensor map
-          tma_reduce_add_3d(&a.tm_dq, smem + L::kStg + sb * L::kStgBytes, 0, h,
+          tma_reduce_add_3d(&a.tm_dq, smem + L::kStg + sb * L::kStgBytes, 0, hq,
                             grow + r4 * L::kStgRows);
           bulk_commit();
           // free this round's buffer as soon as the reduce has read it, so the
@@ -407,10 +407,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
     const float sl2 = a.scale_log2;
     const bool key_ok = u < it.k_len;
     bool ok = true;
-    for (int i = 0; ok && i < n_qt; ++i) {
+    for (int i = 0, jt = 0; ok && i < n_all; ++i, jt = jt + 1 == n_qt ? 0 : jt + 1) {
       Seg sg;
       int q0, t;
-      tile_of(it, (i + rot) % n_qt, sg, q0, t);
+      tile_of(it, jt, sg, q0, t);
       const int st = i % kStages;
       if (!mbar_wait(&bars->sdp_full, i & 1, lim, abort) ||
           !mbar_wait(&bars->qdo_full[st], (i / kStages) & 1, lim, abort)) {
@@ -511,7 +511,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
       if (lane == 0) mbar_arrive(&bars->ps_full);
     }
     // ------------------------------------------------------------ dK / dV epilogue
-    if (ok && n_qt > 0 && !mbar_wait(&bars->dkv_done, 0, lim, abort)) ok = false;
+    if (ok && n_all > 0 && !mbar_wait(&bars->dkv_done, 0, lim, abort)) ok = false;
     if (!ok) {
       record_timeout(a.status, abort, 13);
     } else {
@@ -519,10 +519,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
       // warpgroup 0 writes dK (scaled), warpgroup 1 writes dV
       float* dst;
       if (it.dk_mode == DK_TEXT) {
-        dst = (g == 0 ? a.dk : a.dv) + ((long long)(it.k_row0 + u) * a.H + h) * kD;
+        dst = (g == 0 ? a.dk : a.dv) + ((long long)(it.k_row0 + u) * a.Hkv + hk) * kD;
       } else {
         const long long row = (long long)it.slot * a.pre_rows + it.dk_row0 + u;
-        dst = (g == 0 ? a.pre_k : a.pre_v) + (row * a.H + h) * kD;
+        dst = (g == 0 ? a.pre_k : a.pre_v) + (row * a.Hkv + hk) * kD;
       }
       const bool first = (it.flags & F_FIRST) != 0;
       const float mul = g == 0 ? a.scale : 1.f;
@@ -530,7 +530,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
 #pragma unroll 1
       for (int c = 0; c < kD / 32; ++c) {
         uint32_t r[32];
-        if (n_qt > 0) {
+        if (n_all > 0) {
           tmem_ld32(tmem + lane_off + col + c * 32, r);
           tmem_ld_wait();
           reg_fence32(r);
@@ -567,7 +567,7 @@ cudaError_t launch_split(const TcBwdArgs& a, cudaStream_t st) {
   cudaError_t e = cudaFuncSetAttribute(tc_bwd_kernel<kSplit>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  const long long blocks = (long long)a.n_items * a.H;
+  const long long blocks = (long long)a.n_items * a.Hkv;
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   tc_bwd_kernel<kSplit><<<(unsigned)blocks, kThreads, smem, st>>>(a);
   return cudaGetLastError();
@@ -579,8 +579,8 @@ cudaError_t launch_tc_bwd(const TcBwdArgs& a, cudaStream_t st) {
   if (a.n_items == 0) return cudaSuccess;
   if (a.d != kD) return cudaErrorNotSupported;
   // The dQ error from one bf16 rounding of dS grows with the softmax scale
-  // (dQ = scale * dS K).  Above kSplitScale the remainder term is added.
-  return a.scale > kSplitScale ? launch_split<true>(a, st) : launch_split<false>(a, st);
+  // (dQ = scale * dS K).  Above kPrecisionSplitScale the remainder term is added.
+  return a.scale > kPrecisionSplitScale ? launch_split<true>(a, st) : launch_split<false>(a, st);
 }
 
 }  // namespace cpattn

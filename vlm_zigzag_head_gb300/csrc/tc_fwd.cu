@@ -22,7 +22,11 @@
 //
 // TMEM (512 columns): S_A [0,128), S_B [128,256), O_A [256, 256 + D),
 // O_B [384, 384 + D).  P (bf16 pairs, 64 columns) overwrites the first half of
-// its S buffer and is the A operand of PV, read straight from TMEM.  Shared
+// its S buffer and is the A operand of PV, read straight from TMEM.  For
+// softmax scales above kPrecisionSplitScale the bf16 remainder p - bf16(p)
+// fills the second half and enters O through a second PV product: the
+// backward's D = dO . O then carries O to about 16 bits, which keeps large
+// dQ rows (few visible keys, scale 1) inside the bf16 tolerance.  Shared
 // memory: Q_A, Q_B, two K and two V stages (128 x D each) in the 128-byte
 // swizzled layout TMA writes, 1024-byte aligned.
 #include <cuda_bf16.h>
@@ -88,7 +92,7 @@ __device__ __forceinline__ void record_timeout(int32_t* status, volatile int* ab
   *abort = 1;
 }
 
-template <int D>
+template <int D, bool kSplitP>
 __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_constant__ TcFwdArgs a) {
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte aligned base, derived from the shared array itself so that the
@@ -99,6 +103,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int item_idx = blockIdx.x % a.n_items;
   const int h = blockIdx.x / a.n_items;
+  const int hk = h / (a.H / a.Hkv);   // the KV head of query head h (grouped-query attention)
   const FwdItem& it = a.items[item_idx];
   volatile int* abort = &bars->abort;
   const long long lim = a.wait_limit;
@@ -171,7 +176,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
           uint8_t* dst = smem + (is_k ? L::kK : L::kV) + st * L::kTile;
           mbar_expect_tx(full, L::kTile);
           for (int b = 0; b < D / 64; ++b)
-            tma_load_3d(m, full, dst + b * L::kBox, b * 64, h, sg.row0 + t * kBN);
+            tma_load_3d(m, full, dst + b * L::kBox, b * 64, hk, sg.row0 + t * kBN);
           issued = j + 1;
         }
         if (*abort) break;
@@ -221,6 +226,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
           const uint64_t bd = sdesc_sw128(v_addr + kk * 16 * 128, L::kBox, 1024);
           mma_bf16_ts(tmem + col_o(x), tmem + col_s(x) + kk * 8, bd, idesc_pv,
                       (j > 0 || kk > 0) ? 1u : 0u);
+          if constexpr (kSplitP)   // the bf16 remainder of P, in S columns [64, 128)
+            mma_bf16_ts(tmem + col_o(x), tmem + col_s(x) + 64 + kk * 8, bd, idesc_pv, 1u);
         }
         mma_commit(&bars->o_done[x]);
         if (x == 1) mma_commit(&bars->v_empty[st]);
@@ -326,28 +333,53 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
         float sp[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) sp[i] = 0.f;
-        uint32_t pk[2][32];
-        if (whole) {
+        if constexpr (kSplitP) {
+          // P (bf16 pairs) over S columns [0, 64) and its bf16 remainder over
+          // [64, 128), written one half row (64 keys) at a time
 #pragma unroll
-          for (int i = 0; i < kBN; i += 2) {
-            const float p0 = ex2(fmaf(__uint_as_float(r[i / 32][i % 32]), sl2, -mu));
-            const float p1 = ex2(fmaf(__uint_as_float(r[i / 32][i % 32 + 1]), sl2, -mu));
-            sp[(i >> 1) & 7] += p0 + p1;
-            pk[i / 64][(i / 2) % 32] = pack_bf16x2(p0, p1);
+          for (int hh = 0; hh < 2; ++hh) {
+            uint32_t pk[32], pl[32];
+#pragma unroll
+            for (int i = hh * 64; i < hh * 64 + 64; i += 2) {
+              float p0 = ex2(fmaf(__uint_as_float(r[i / 32][i % 32]), sl2, -mu));
+              float p1 = ex2(fmaf(__uint_as_float(r[i / 32][i % 32 + 1]), sl2, -mu));
+              if (!whole) {
+                if (i >= vis) p0 = 0.f;
+                if (i + 1 >= vis) p1 = 0.f;
+              }
+              sp[(i >> 1) & 7] += p0 + p1;
+              pk[(i / 2) % 32] = pack_bf16x2(p0, p1);
+              const float h0 = __bfloat162float(__float2bfloat16_rn(p0));
+              const float h1 = __bfloat162float(__float2bfloat16_rn(p1));
+              pl[(i / 2) % 32] = pack_bf16x2(p0 - h0, p1 - h1);
+            }
+            tmem_st32(s_col + hh * 32, pk);
+            tmem_st32(s_col + 64 + hh * 32, pl);
           }
         } else {
+          uint32_t pk[2][32];
+          if (whole) {
 #pragma unroll
-          for (int i = 0; i < kBN; i += 2) {
-            float p0 = ex2(fmaf(__uint_as_float(r[i / 32][i % 32]), sl2, -mu));
-            float p1 = ex2(fmaf(__uint_as_float(r[i / 32][i % 32 + 1]), sl2, -mu));
-            if (i >= vis) p0 = 0.f;
-            if (i + 1 >= vis) p1 = 0.f;
-            sp[(i >> 1) & 7] += p0 + p1;
-            pk[i / 64][(i / 2) % 32] = pack_bf16x2(p0, p1);
+            for (int i = 0; i < kBN; i += 2) {
+              const float p0 = ex2(fmaf(__uint_as_float(r[i / 32][i % 32]), sl2, -mu));
+              const float p1 = ex2(fmaf(__uint_as_float(r[i / 32][i % 32 + 1]), sl2, -mu));
+              sp[(i >> 1) & 7] += p0 + p1;
+              pk[i / 64][(i / 2) % 32] = pack_bf16x2(p0, p1);
+            }
+          } else {
+#pragma unroll
+            for (int i = 0; i < kBN; i += 2) {
+              float p0 = ex2(fmaf(__uint_as_float(r[i / 32][i % 32]), sl2, -mu));
+              float p1 = ex2(fmaf(__uint_as_float(r[i / 32][i % 32 + 1]), sl2, -mu));
+              if (i >= vis) p0 = 0.f;
+              if (i + 1 >= vis) p1 = 0.f;
+              sp[(i >> 1) & 7] += p0 + p1;
+              pk[i / 64][(i / 2) % 32] = pack_bf16x2(p0, p1);
+            }
           }
+          tmem_st32(s_col, pk[0]);
+          tmem_st32(s_col + 32, pk[1]);
         }
-        tmem_st32(s_col, pk[0]);
-        tmem_st32(s_col + 32, pk[1]);
         l += ((sp[0] + sp[1]) + (sp[2] + sp[3])) + ((sp[4] + sp[5]) + (sp[6] + sp[7]));
         tmem_st_wait();
         tc_fence_before();
@@ -448,15 +480,15 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
   }
 }
 
-template <int D>
+template <int D, bool kSplitP>
 cudaError_t launch_d(const TcFwdArgs& a, cudaStream_t st) {
   const int smem = Smem<D>::kAlloc;
-  cudaError_t e = cudaFuncSetAttribute(tc_fwd_kernel<D>,
+  cudaError_t e = cudaFuncSetAttribute(tc_fwd_kernel<D, kSplitP>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const long long blocks = (long long)a.n_items * a.H;
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  tc_fwd_kernel<D><<<(unsigned)blocks, kThreads, smem, st>>>(a);
+  tc_fwd_kernel<D, kSplitP><<<(unsigned)blocks, kThreads, smem, st>>>(a);
   return cudaGetLastError();
 }
 
@@ -464,7 +496,8 @@ cudaError_t launch_d(const TcFwdArgs& a, cudaStream_t st) {
 
 cudaError_t launch_tc_fwd(const TcFwdArgs& a, cudaStream_t st) {
   if (a.n_items == 0) return cudaSuccess;
-  return a.d == 64 ? launch_d<64>(a, st) : launch_d<128>(a, st);
+  if (a.split_p) return a.d == 64 ? launch_d<64, true>(a, st) : launch_d<128, true>(a, st);
+  return a.d == 64 ? launch_d<64, false>(a, st) : launch_d<128, false>(a, st);
 }
 
 }  // namespace cpattn
