@@ -39,7 +39,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # backward ring-step kernel, mean over the 8 launches of one step, from one ncu
 # capture of this kernel on the named workload.  Set an entry to None when the
 # kernel changes until it is captured again.
-MEASURED_TRAFFIC = {"long": 14.47e9}
+MEASURED_TRAFFIC = {"long": 14.48e9}
 
 
 def causal_pairs(w) -> int:
@@ -186,7 +186,10 @@ def run_cuda(args, w, rank, world, dist):
     out = torch.empty_like(qd)
     out_lo = torch.empty_like(qd)
     lse = torch.empty((H, T), dtype=torch.float32, device=dev)
-    grads = tuple(torch.empty((T, H, d), dtype=torch.float32, device=dev) for _ in range(3))
+    Hkv = kd.shape[1]
+    grads = (torch.empty((T, H, d), dtype=torch.float32, device=dev),
+             torch.empty((T, Hkv, d), dtype=torch.float32, device=dev),
+             torch.empty((T, Hkv, d), dtype=torch.float32, device=dev))
     ws_f, ws_b = cp.Workspace(dev), cp.Workspace(dev)
 
     def step():
@@ -263,7 +266,8 @@ def run_cuda(args, w, rank, world, dist):
                 "achieved": ach, "peak": peak_sus, "unit": "TFLOP/s", "frac": ach / peak_sus,
                 "peak_source": "%s bf16_tflops_sustained" % peak_src,
                 "traffic": (args.traffic if args.traffic is not None
-                            else MEASURED_TRAFFIC.get(w.name)), "launch_ms": avg,
+                            else MEASURED_TRAFFIC.get(w.name) if w.kv_heads == w.H else None),
+                "launch_ms": avg,
                 "flops_per_launch": bwd_launch_flops}
     kernels = {}
     for k, (kms, n) in prof.items():
@@ -301,7 +305,8 @@ def run_cuda(args, w, rank, world, dist):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic",
             "config": {"workload": w.name, "text_len": W.text_lengths(w), "prefix_len": N,
-                       "P": P, "heads": H, "head_dim": d, "n_seqs": w.n_seqs,
+                       "P": P, "heads": H, "kv_heads": w.kv_heads, "head_dim": d,
+                       "n_seqs": w.n_seqs,
                        "parallelism": "replicas" if world > 1 else "single",
                        "l2": "inputs larger than L2 (no flush)"},
             "pct_of_bf16_peak": 100.0 * (value / world) / peak_sus,
@@ -330,13 +335,15 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="cuda", choices=["cuda", "reference"])
     ap.add_argument("--workload", default="long", choices=sorted(W.WORKLOADS))
+    ap.add_argument("--kv-heads", type=int, default=0,
+                    help="KV heads for grouped-query attention (default: as many as query heads)")
     ap.add_argument("--oracle-queries", type=int, default=32768)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--traffic", type=float, default=None,
                     help="DRAM bytes per launch of the dominant kernel from an ncu capture")
     args = ap.parse_args()
-    w = W.get(args.workload)
+    w = W.get(args.workload, H_kv=args.kv_heads) if args.kv_heads else W.get(args.workload)
     if w.dtype != "bf16" or not w.backward:
         raise SystemExit("bench workloads are the bf16 forward+backward ones")
     world = int(os.environ.get("WORLD_SIZE", "1"))

@@ -45,6 +45,11 @@ class Workload:
     q_prescaled: bool = False
     packed_range: Optional[tuple] = None   # (lo, hi) inclusive for drawn text lengths
     round_to: int = 0                      # round drawn lengths up to this multiple
+    H_kv: int = 0                          # KV heads (grouped-query attention); 0: H
+
+    @property
+    def kv_heads(self) -> int:
+        return self.H_kv or self.H
 
 
 WORKLOADS = {
@@ -118,10 +123,11 @@ def make_inputs(w: Workload, with_dout: Optional[bool] = None) -> Inputs:
         lo, hi = w.packed_range
         torch.randint(lo, hi + 1, (w.n_seqs,), generator=g)
     shape = (T, w.H, w.d)
+    kv_shape = (T, w.kv_heads, w.d)
     dt = torch_dtype(w)
     q = torch.randn(shape, generator=g, dtype=torch.float32)
-    k = torch.randn(shape, generator=g, dtype=torch.float32)
-    v = torch.randn(shape, generator=g, dtype=torch.float32)
+    k = torch.randn(kv_shape, generator=g, dtype=torch.float32)
+    v = torch.randn(kv_shape, generator=g, dtype=torch.float32)
     if w.q_prescaled:
         q = q * (1.0 / math.sqrt(128.0))
     q, k, v = q.to(dt), k.to(dt), v.to(dt)
