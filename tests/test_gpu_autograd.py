@@ -93,3 +93,25 @@ def test_autograd_refuses_cpu_tensors():
     q = torch.zeros((256, 1, 64), requires_grad=True)
     with pytest.raises(CpError):
         cp_attention(q, q, q, [0, 256], 2)
+
+
+@pytest.mark.gpu
+def test_autograd_grouped_kv_heads():
+    """k / v with fewer heads than q (grouped-query attention): autograd
+    receives dk / dv shaped like k / v, equal to the oracle's group sums."""
+    from vlm_zigzag_head_gb300.autograd import cp_attention
+    P, N, texts, H, H_kv, d = 2, 32, [512, 256], 4, 2, 128
+    cu = _cu(N, texts)
+    g = torch.Generator().manual_seed(19)
+    q = torch.randn((cu[-1], H, d), generator=g).to(torch.bfloat16)
+    k = torch.randn((cu[-1], H_kv, d), generator=g).to(torch.bfloat16)
+    v = torch.randn((cu[-1], H_kv, d), generator=g).to(torch.bfloat16)
+    w = torch.randn((cu[-1], H, d), generator=g).to(torch.bfloat16)
+    qd, kd, vd = (x.to(DEV).requires_grad_(True) for x in (q, k, v))
+    out, _ = cp_attention(qd, kd, vd, cu, P, N)
+    (out.float() * w.to(DEV).float()).sum().backward()
+    torch.cuda.synchronize()
+    g_ref = oracle.causal_attention_bwd(q, k, v, w, cu, d ** -0.5)
+    assert kd.grad.shape == k.shape and vd.grad.shape == v.shape
+    for name, got, want in zip(("dq", "dk", "dv"), (qd.grad, kd.grad, vd.grad), g_ref):
+        assert_close(name, got.cpu(), want, "bf16")

@@ -9,7 +9,7 @@ order (ranks 0..P-1, then the prefix queries' own term) before it returns, so
 the gradients that reach autograd are already the reduced ones.
 
 ``prefix_hook`` gives a caller the quantity the page's hook reduces.  It is
-called during the backward with the per-rank terms ``[2, P+1, n*N, H, d]``
+called during the backward with the per-rank terms ``[2, P+1, n*N, H_kv, d]``
 (dK, dV; slot P is the prefix queries' own term), before autograd receives
 the summed gradients.
 
@@ -70,7 +70,9 @@ def cp_attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
     """Differentiable zigzag context-parallel causal attention over packed
     samples ``[prefix_i ++ text_i]`` (THD layout ``[T, H, d]``, bf16 or fp32,
     on a CUDA device).  Returns ``(out, lse)``; gradients flow to q, k and v.
-    ``softmax_scale`` defaults to ``1/sqrt(d)``."""
+    ``k`` / ``v`` may hold fewer heads than ``q`` (grouped-query attention:
+    query head h reads KV head h // (H / H_kv)).  ``softmax_scale`` defaults
+    to ``1/sqrt(d)``."""
     if softmax_scale is None:
         softmax_scale = q.shape[-1] ** -0.5
     return CPAttention.apply(q, k, v, cu_seqlens, P, prefix_len, softmax_scale, prefix_hook)

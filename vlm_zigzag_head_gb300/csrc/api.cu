@@ -586,6 +586,27 @@ cp_status_t cp_attn_bwd_gqa(const void* q, const void* k, const void* v, const v
   const BwdItem* items = reinterpret_cast<const BwdItem*>(w + L.items);
   if (tc) {
     CP_CUDA(cudaMemsetAsync(dq, 0, (size_t)T * H * d * sizeof(float), st), "clear dq");
+    // With grouped KV heads one CTA walks all G query heads of its KV head.
+    // When that leaves too few CTAs to fill the GPU (under ~4 per SM per
+    // step), the group is shared by kv_split CTAs whose partial dK / dV are
+    // reduce-added into zeroed memory.
+    const int G = H / Hkv;
+    int kv_split = 1;
+    {
+      int dev = 0, sms = 0;
+      CP_CUDA(cudaGetDevice(&dev), "cudaGetDevice");
+      CP_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev), "SM count");
+      const double per_step = (double)ps->bwd.items.size() / P * Hkv;
+      while (G % (2 * kv_split) == 0 && per_step * kv_split < 4.0 * sms) kv_split *= 2;
+    }
+    if (kv_split > 1) {
+      CP_CUDA(cudaMemsetAsync(dk, 0, (size_t)T * Hkv * d * sizeof(float), st), "clear dk");
+      CP_CUDA(cudaMemsetAsync(dv, 0, (size_t)T * Hkv * d * sizeof(float), st), "clear dv");
+      if (N > 0)
+        CP_CUDA(cudaMemsetAsync(slots, 0, 2 * (size_t)(P + 1) * pre_rows * Hkv * d * sizeof(float),
+                                st),
+                "clear prefix slots");
+    }
     TcBwdArgs a;
     const char* terr = nullptr;
     bool ok = make_tmap_thd(&a.tm_q, q, T, H, d, kBwdTileQ, &terr) &&
@@ -595,7 +616,8 @@ cp_status_t cp_attn_bwd_gqa(const void* q, const void* k, const void* v, const v
               make_tmap_ld(&a.tm_ld, lse2, pitch, H, kBwdTileQ + 4, &terr) &&
               make_tmap_f32_thd(&a.tm_dq, dq, T, H, d, 16, &terr);
     if (!ok) return fail(CP_ERR_CUDA, std::string("tensor map: ") + (terr ? terr : "?"));
-    a.H = H; a.Hkv = Hkv; a.d = d; a.scale = scale; a.scale_log2 = scale * 1.4426950408889634f;
+    a.H = H; a.Hkv = Hkv; a.kv_split = kv_split; a.d = d; a.scale = scale;
+    a.scale_log2 = scale * 1.4426950408889634f;
     a.T = T;
     a.dq = dq; a.dk = dk; a.dv = dv;
     a.pre_k = pre_k; a.pre_v = pre_v; a.pre_rows = pre_rows;

@@ -56,6 +56,8 @@ struct TcBwdArgs {
   float* pre_k; float* pre_v; int64_t pre_rows;
   int32_t* status;
   long long wait_limit;
+  int kv_split;               // CTAs sharing one KV head's query heads (divides H / Hkv); > 1:
+                              // dK / dV / prefix slots are reduce-added into zeroed memory
 };
 cudaError_t launch_tc_bwd(const TcBwdArgs& a, cudaStream_t st);
 

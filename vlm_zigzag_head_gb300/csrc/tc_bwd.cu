@@ -124,7 +124,7 @@ __device__ __forceinline__ void record_timeout(int32_t* status, volatile int* ab
   *abort = 1;
 }
 
-template <bool kSplit>
+template <bool kSplit, bool kShared>
 __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_constant__ TcBwdArgs a) {
   using L = Lay<kSplit>;
   extern __shared__ uint8_t smem_raw[];
@@ -134,8 +134,13 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
   Bars* bars = reinterpret_cast<Bars*>(smem + L::kBars);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int item_idx = blockIdx.x % a.n_items;
-  const int hk = blockIdx.x / a.n_items;   // KV head; its query heads are hk*G .. hk*G+G-1
+  // KV head hk; its query heads are hk*G .. hk*G+G-1.  Shared groups
+  // (kv_split > 1): kv_split CTAs take Gs = G / kv_split consecutive query
+  // heads each, and their partial dK / dV meet in global memory by
+  // reduce-adds.
+  const int hk = kShared ? blockIdx.x / a.n_items / a.kv_split : blockIdx.x / a.n_items;
   const int G = a.H / a.Hkv;
+  const int Gs = kShared ? G / a.kv_split : G;   // query heads of this CTA
   BwdItem& it = *reinterpret_cast<BwdItem*>(smem + L::kItem);
   if (warp == 0)  // the work item, copied once into shared memory (128 bytes)
     reinterpret_cast<uint32_t*>(&it)[lane] =
@@ -178,12 +183,12 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
   const int nseg = it.nseg;
   int n_qt = 0;   // query tiles of one query head
   for (int s = 0; s < nseg; ++s) n_qt += run_qtiles(it.seg[s]);
-  // Every role walks the same G * n_qt query tiles in the same order: query
-  // head hk*G + j / n_qt, tile j % n_qt.  dK / dV of the KV head accumulate
+  // Every role walks the same Gs * n_qt query tiles in the same order: the
+  // CTA's first query head + j / n_qt, tile j % n_qt.  dK / dV of the KV head accumulate
   // over all of them.  Concurrent CTAs are neighbouring key tiles that meet
   // the same queries in the same order, so the Q / dO tiles they load are
   // shared through L2 (a rotated order per CTA measured slower).
-  const int n_all = G * n_qt;
+  const int n_all = Gs * n_qt;
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
@@ -202,7 +207,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
     // decisions are taken by lane 0 and broadcast: the warp never diverges
     // around the __syncwarp below
     bool go = true;
-    int jt = 0, hq = hk * G;   // tile j: tile jt of query head hq
+    int jt = 0, hq = hk * G + (kShared ? blockIdx.x / a.n_items % a.kv_split * Gs : 0);
     for (int j = 0; go && j < n_all; ++j, jt = jt + 1 == n_qt ? 0 : jt + 1, hq += jt == 0) {
       {
         Seg sg;
@@ -371,7 +376,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
       constexpr int N = L::kNumStg;
       bool ok = true;
       int k = 0;
-      int jt = 0, hq = hk * G;   // tile j: tile jt of query head hq
+      int jt = 0, hq = hk * G + (kShared ? blockIdx.x / a.n_items % a.kv_split * Gs : 0);
       for (int j = 0; ok && j < n_all; ++j, jt = jt + 1 == n_qt ? 0 : jt + 1, hq += jt == 0) {
         Seg sgd;
         int q0d, td;
@@ -544,6 +549,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
           float4 v = make_float4(__uint_as_float(r[x]) * mul, __uint_as_float(r[x + 1]) * mul,
                                  __uint_as_float(r[x + 2]) * mul, __uint_as_float(r[x + 3]) * mul);
           float4* d4 = reinterpret_cast<float4*>(dst + c * 32 + x);
+          if constexpr (kShared) {    // sub-CTAs of one group meet here (zeroed first)
+            red_add_v4(d4, v);
+            continue;
+          }
           if (!first) {
             const float4 o = *d4;
             v.x += o.x; v.y += o.y; v.z += o.z; v.w += o.w;
@@ -561,15 +570,15 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
   }
 }
 
-template <bool kSplit>
+template <bool kSplit, bool kShared>
 cudaError_t launch_split(const TcBwdArgs& a, cudaStream_t st) {
   constexpr int smem = Lay<kSplit>::kAlloc;
-  cudaError_t e = cudaFuncSetAttribute(tc_bwd_kernel<kSplit>,
+  cudaError_t e = cudaFuncSetAttribute(tc_bwd_kernel<kSplit, kShared>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  const long long blocks = (long long)a.n_items * a.Hkv;
+  const long long blocks = (long long)a.n_items * a.Hkv * a.kv_split;
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  tc_bwd_kernel<kSplit><<<(unsigned)blocks, kThreads, smem, st>>>(a);
+  tc_bwd_kernel<kSplit, kShared><<<(unsigned)blocks, kThreads, smem, st>>>(a);
   return cudaGetLastError();
 }
 
@@ -578,9 +587,12 @@ cudaError_t launch_split(const TcBwdArgs& a, cudaStream_t st) {
 cudaError_t launch_tc_bwd(const TcBwdArgs& a, cudaStream_t st) {
   if (a.n_items == 0) return cudaSuccess;
   if (a.d != kD) return cudaErrorNotSupported;
+  if (a.kv_split < 1 || (a.H / a.Hkv) % a.kv_split != 0) return cudaErrorInvalidValue;
   // The dQ error from one bf16 rounding of dS grows with the softmax scale
   // (dQ = scale * dS K).  Above kPrecisionSplitScale the remainder term is added.
-  return a.scale > kPrecisionSplitScale ? launch_split<true>(a, st) : launch_split<false>(a, st);
+  const bool split = a.scale > kPrecisionSplitScale;
+  if (a.kv_split > 1) return split ? launch_split<true, true>(a, st) : launch_split<false, true>(a, st);
+  return split ? launch_split<true, false>(a, st) : launch_split<false, false>(a, st);
 }
 
 }  // namespace cpattn
