@@ -143,6 +143,14 @@ def oracle_sample(w, n_queries: int = 8192):
     return dt, flops, desc
 
 
+def workload_config(w, world) -> dict:
+    """The `config` object of both arms' JSON lines."""
+    return {"workload": w.name, "text_len": W.text_lengths(w), "prefix_len": w.prefix_len,
+            "P": w.P, "heads": w.H, "kv_heads": w.kv_heads, "head_dim": w.d,
+            "n_seqs": w.n_seqs, "parallelism": "replicas" if world > 1 else "single",
+            "l2": "inputs larger than L2 (no flush)"}
+
+
 def run_reference(args, w, rank, world):
     if rank != 0:
         return 0
@@ -161,7 +169,7 @@ def run_reference(args, w, rank, world):
         "impl": "reference", "metric": METRIC, "value": val, "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": {"workload": w.name, "sample": desc},
+        "data": "synthetic", "config": dict(workload_config(w, world), sample=desc),
         "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
                          "sample": desc},
         "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
@@ -304,11 +312,7 @@ def run_cuda(args, w, rank, world, dist):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic",
-            "config": {"workload": w.name, "text_len": W.text_lengths(w), "prefix_len": N,
-                       "P": P, "heads": H, "kv_heads": w.kv_heads, "head_dim": d,
-                       "n_seqs": w.n_seqs,
-                       "parallelism": "replicas" if world > 1 else "single",
-                       "l2": "inputs larger than L2 (no flush)"},
+            "config": workload_config(w, world),
             "pct_of_bf16_peak": 100.0 * (value / world) / peak_sus,
             "fwd_tflops": world * f_flops / (fwd_ms / 1e3) / 1e12, "fwd_ms": fwd_ms,
             "bwd_tflops": world * 2.5 * f_flops / (bwd_ms / 1e3) / 1e12, "bwd_ms": bwd_ms,
