@@ -40,6 +40,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # capture of this kernel on the named workload.  Set an entry to None when the
 # kernel changes until it is captured again.
 MEASURED_TRAFFIC = {"long": 14.48e9}
+EX2_PER_CLK_SM = 32.0   # MUFU exp2 results per clock per SM (31.8 measured by a throughput loop)
 
 
 def causal_pairs(w) -> int:
@@ -284,6 +285,26 @@ def run_cuda(args, w, rank, world, dist):
     if fwd_launches:
         avg = fwd_ms_k / fwd_launches
         kernels["tc_fwd_step"]["achieved_tflops"] = fwd_launch_flops / (avg / 1e3) / 1e12
+        # secondary bound: one exp2 per visible pair and head, against the MUFU
+        # rate (32 exp2 per clock per SM on this part) at the maximum SM clock
+        exps = causal_pairs(w) * H / P
+        mufu = EX2_PER_CLK_SM * torch.cuda.get_device_properties(dev).multi_processor_count * \
+            float(peaks.get("sm_max_mhz", 2070.0)) * 1e6
+        kernels["tc_fwd_step"]["exp_per_s"] = exps / (avg / 1e3)
+        kernels["tc_fwd_step"]["exp_frac"] = exps / (avg / 1e3) / mufu
+    # memory kernels: algorithmic bytes per launch against the measured HBM copy rate
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    Hkv = kd.shape[1]
+    text_rows = sum(W.text_lengths(w))
+    mem_bytes = {
+        "zigzag_gather": 2 * text_rows * (H + 2 * Hkv) * d * 2,          # q, k, v rows in and out
+        "bwd_preprocess": T * H * d * 2 * 3 + T * H * 4 * 3,              # out, out_lo, dO; lse in, D, lse2 out
+    }
+    for k, nb in mem_bytes.items():
+        if k in kernels:
+            avg = kernels[k]["ms_total"] / kernels[k]["launches"]
+            kernels[k]["achieved_gbs"] = nb / (avg / 1e3) / 1e9
+            kernels[k]["hbm_frac"] = kernels[k]["achieved_gbs"] / hbm
     gpu_launches = sum(n for _, n in prof.values())
 
     # ---- end to end through the public API with host buffers
