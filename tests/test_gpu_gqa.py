@@ -152,3 +152,41 @@ def test_gqa_large_grid_without_group_split(cp):
     assert_close("dq", got["dq"][:, 0:2], dq, "bf16")
     assert_close("dk", got["dk"][:, 0:1], dk, "bf16")
     assert_close("dv", got["dv"][:, 0:1], dv, "bf16")
+
+
+def test_gqa_long_workload_sampled(cp):
+    """128K tokens, P = 8, 32 query heads over 8 KV heads, at full size.
+    out / lse / dQ on 2048 seeded rows of query heads 0 and 5, and dK / dV of
+    KV head 0 on the last 256 keys (the sum of its 4 query heads' terms), from
+    the oracle's row- and key-sampled forms.  At every key, per KV head,
+    sum_j dV_j equals the sum of dO over the group's query heads, and
+    sum_j dK_j = 0."""
+    from gpu_util import BF16_REL, rel_l2
+    from vlm_zigzag_head_gb300 import workloads as W
+    w = W.get("long", H_kv=8)
+    x = W.make_inputs(w)
+    got = _run(cp, x.q, x.k, x.v, x.dout, x.cu_seqlens, w.P, w.prefix_len, x.scale)
+    G = w.H // w.kv_heads
+    rows = W.sample_rows(x.T, 2048, w.seed).numpy()
+    r_t = torch.as_tensor(rows)
+    for h in (0, 5):
+        o_ref, l_ref, dq_ref = oracle.causal_attention_fwd_rows(
+            x.q[:, h:h + 1], x.k[:, h // G:h // G + 1], x.v[:, h // G:h // G + 1], x.cu_seqlens,
+            x.scale, rows, dout=x.dout[:, h:h + 1])
+        assert_close("out rows h%d" % h, got["out"][r_t][:, h:h + 1], o_ref, "bf16")
+        assert_close("lse rows h%d" % h, got["lse"][h:h + 1][:, r_t], l_ref, "bf16")
+        assert_close("dq rows h%d" % h, got["dq"][r_t][:, h:h + 1], dq_ref, "bf16")
+    keys = np.arange(x.T - 256, x.T)
+    dk_ref = dv_ref = 0
+    for h in range(G):                      # the query heads of KV head 0
+        a, b = oracle.causal_attention_bwd_keys(x.q[:, h:h + 1], x.k[:, 0:1], x.v[:, 0:1],
+                                                x.dout[:, h:h + 1], x.cu_seqlens, x.scale, keys)
+        dk_ref, dv_ref = dk_ref + a, dv_ref + b
+    k_t = torch.as_tensor(keys)
+    assert_close("dk keys", got["dk"][k_t][:, 0:1], dk_ref, "bf16")
+    assert_close("dv keys", got["dv"][k_t][:, 0:1], dv_ref, "bf16")
+    sum_dv = got["dv"].double().sum(0)
+    sum_do = x.dout.double().view(x.T, w.kv_heads, G, w.d).sum(dim=(0, 2))
+    assert rel_l2(sum_dv, sum_do) < BF16_REL
+    sum_dk = got["dk"].double().sum(0)
+    assert float(sum_dk.norm() / got["dk"].double().norm()) < BF16_REL
