@@ -133,7 +133,25 @@ __device__ __forceinline__ float to_f<float>(float x) { return x; }
 template <>
 __device__ __forceinline__ float to_f<__nv_bfloat16>(__nv_bfloat16 x) { return __bfloat162float(x); }
 
-// One warp per (head, token): D = dO . O in fp32, plus the log2-domain lse.
+// D = dO . O in fp32 per (token, head), plus the log2-domain lse.  A row of
+// d elements is read by d * sizeof(T) / 16 lanes with 16-byte loads, so a warp
+// covers 32 / that many rows per pass.  Rows are taken in THD order (all heads
+// of a token, then the next token), so the reads stream through memory; the
+// small D / lse2 writes are the scattered side.
+template <typename T>
+__device__ __forceinline__ void add_dot16(const T* o, const T* o_lo, const T* g, float& acc) {
+  constexpr int kV = 16 / sizeof(T);
+  const uint4 a = *reinterpret_cast<const uint4*>(o);
+  const uint4 c = *reinterpret_cast<const uint4*>(g);
+  uint4 b = make_uint4(0u, 0u, 0u, 0u);
+  if (o_lo) b = *reinterpret_cast<const uint4*>(o_lo);
+  const T* av = reinterpret_cast<const T*>(&a);
+  const T* bv = reinterpret_cast<const T*>(&b);
+  const T* cv = reinterpret_cast<const T*>(&c);
+#pragma unroll
+  for (int i = 0; i < kV; ++i) acc += (to_f(av[i]) + (o_lo ? to_f(bv[i]) : 0.f)) * to_f(cv[i]);
+}
+
 template <typename T>
 __global__ void __launch_bounds__(kThreads) bwd_pre_kernel(const T* __restrict__ o,
                                                            const T* __restrict__ o_lo,
@@ -142,22 +160,22 @@ __global__ void __launch_bounds__(kThreads) bwd_pre_kernel(const T* __restrict__
                                                            int H, int d, float* D, float* lse2,
                                                            long long pitch) {
   const int lane = threadIdx.x & 31;
+  const int lpr = d * (int)sizeof(T) / 16;          // lanes per row: 8, 16 or 32
+  const int rpw = 32 / lpr;                          // rows per warp pass
+  const int seg = lane / lpr, sl = lane - seg * lpr;
   const long long pairs = (long long)Tn * H;
-  for (long long w = (long long)blockIdx.x * (kThreads / 32) + threadIdx.x / 32; w < pairs;
-       w += (long long)gridDim.x * (kThreads / 32)) {
-    const int h = (int)(w / Tn);
-    const long long t = w - (long long)h * Tn;
-    const long long base = (t * H + h) * (long long)d;
+  const long long step = (long long)gridDim.x * (kThreads / 32) * rpw;
+  for (long long base = ((long long)blockIdx.x * (kThreads / 32) + threadIdx.x / 32) * rpw;
+       base < pairs; base += step) {
+    const long long w = base + seg;                  // row: token t = w / H, head h
+    const bool valid = w < pairs;
+    const long long t = valid ? w / H : 0;
+    const int h = valid ? (int)(w - t * H) : 0;
+    const long long off = (t * H + h) * (long long)d + (long long)sl * (16 / sizeof(T));
     float acc = 0.f;
-    if (o_lo) {
-      for (int e = lane; e < d; e += 32)
-        acc += (to_f(o[base + e]) + to_f(o_lo[base + e])) * to_f(dout[base + e]);
-    } else {
-      for (int e = lane; e < d; e += 32) acc += to_f(o[base + e]) * to_f(dout[base + e]);
-    }
-#pragma unroll
-    for (int sh = 16; sh > 0; sh >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, sh);
-    if (lane == 0) {
+    if (valid) add_dot16(o + off, o_lo ? o_lo + off : nullptr, dout + off, acc);
+    for (int sh = lpr >> 1; sh > 0; sh >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, sh);
+    if (valid && sl == 0) {
       D[(long long)h * pitch + t] = acc;
       lse2[(long long)h * pitch + t] = lse[(long long)h * Tn + t] * 1.4426950408889634f;
     }
@@ -243,7 +261,7 @@ cudaError_t launch_bwd_preprocess(const void* out, const void* out_lo, const voi
                                   int64_t pitch, cudaStream_t st) {
   const long long pairs = (long long)T * H;
   if (pairs == 0) return cudaSuccess;
-  const int g = grid_for(pairs, kThreads / 32);
+  const int g = grid_for((pairs + 3) / 4, kThreads / 32);
   if (bf16)
     bwd_pre_kernel<__nv_bfloat16><<<g, kThreads, 0, st>>>(
         static_cast<const __nv_bfloat16*>(out), static_cast<const __nv_bfloat16*>(out_lo),
