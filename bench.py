@@ -144,6 +144,20 @@ def oracle_sample(w, n_queries: int = 8192):
     return dt, flops, desc
 
 
+def max_over_ranks(ms: float, dist, device) -> float:
+    """The slowest rank's time (the job finishes with its last replica)."""
+    if dist is None:
+        return ms
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_value(flops_per_step: float, world: int, steps: int, ms: float) -> float:
+    """TFLOP/s of the whole job: every replica runs the workload once per step."""
+    return world * flops_per_step * steps / (ms / 1e3) / 1e12
+
+
 def workload_config(w, world) -> dict:
     """The `config` object of both arms' JSON lines."""
     return {"workload": w.name, "text_len": W.text_lengths(w), "prefix_len": w.prefix_len,
@@ -233,14 +247,11 @@ def run_cuda(args, w, rank, world, dist):
         barrier()
         prof = cp.cp_profile_end()
     ms = e0.elapsed_time(e1)
-    if dist is not None:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, dist, dev)
     if cp.cp_workspace_status(ws_f) or cp.cp_workspace_status(ws_b):
         raise RuntimeError("a device wait timed out in the timed region")
     ms_step = ms / args.steps
-    value = world * total * args.steps / (ms / 1e3) / 1e12
+    value = whole_job_value(total, world, args.steps, ms)
     peaks, peak_src = load_peaks()
     peak_sus = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
 
