@@ -265,6 +265,7 @@ constexpr int kProfKinds = 8;
 struct ProfRec {
   int kind;
   cudaEvent_t a, b;
+  int count;   // launches between the two events
 };
 std::mutex g_prof_mu;
 std::atomic<bool> g_prof_on{false};
@@ -274,7 +275,8 @@ struct ProfScope {
   int kind;
   cudaStream_t st;
   cudaEvent_t a = nullptr, b = nullptr;
-  ProfScope(int k, cudaStream_t s) : kind(k), st(s) {
+  int count;
+  ProfScope(int k, cudaStream_t s, int n = 1) : kind(k), st(s), count(n) {
     if (!g_prof_on.load()) return;
     if (cudaEventCreate(&a) != cudaSuccess || cudaEventCreate(&b) != cudaSuccess) {
       a = b = nullptr;
@@ -286,7 +288,7 @@ struct ProfScope {
     if (!a) return;
     cudaEventRecord(b, st);
     std::lock_guard<std::mutex> lk(g_prof_mu);
-    g_prof.push_back({kind, a, b});
+    g_prof.push_back({kind, a, b, count});
   }
 };
 
@@ -475,11 +477,19 @@ cp_status_t cp_attn_fwd_gqa(const void* q, const void* k, const void* v, cp_dtyp
     a.out = out; a.lse = lse; a.T = T; a.out_lo = out_lo;
     a.status = reinterpret_cast<int32_t*>(w + L.status);
     a.wait_limit = wait_limit();
+    // Ring steps after the first are programmatic dependents of the one
+    // before: their CTAs fill SMs as the previous step drains and wait for it
+    // only at the merge.  One profiling interval spans the P launches.
+    // (Only a step that directly follows a launched step kernel may be a
+    // dependent: an empty step launches nothing.)
+    ProfScope ps_(2, st, P);
+    bool prev = false;
     for (int step = 0; step < P; ++step) {
       a.items = items + fp.step_begin[step];
       a.n_items = fp.step_begin[step + 1] - fp.step_begin[step];
-      ProfScope ps_(2, st);
+      a.pdl = prev ? 1 : 0;
       CP_CUDA(launch_tc_fwd(a, st), "tensor-core ring step");
+      prev = a.n_items > 0;
     }
     return CP_OK;
   }
@@ -623,11 +633,16 @@ cp_status_t cp_attn_bwd_gqa(const void* q, const void* k, const void* v, const v
     a.pre_k = pre_k; a.pre_v = pre_v; a.pre_rows = pre_rows;
     a.status = reinterpret_cast<int32_t*>(w + L.status);
     a.wait_limit = wait_limit();
+    // as in the forward: later steps overlap the previous step's tail and
+    // wait for it only before the dK / dV epilogue
+    ProfScope ps_(4, st, P);
+    bool prev = false;
     for (int step = 0; step < P; ++step) {
       a.items = items + ps->bwd.step_begin[step];
       a.n_items = ps->bwd.step_begin[step + 1] - ps->bwd.step_begin[step];
-      ProfScope ps_(4, st);
+      a.pdl = prev ? 1 : 0;
       CP_CUDA(launch_tc_bwd(a, st), "tensor-core backward ring step");
+      prev = a.n_items > 0;
     }
   } else {
     CP_CUDA(stager().upload(w + L.qitems, ps->fwd_nat.items.data(),
@@ -696,7 +711,7 @@ cp_status_t cp_profile_end(double* ms, int64_t* launches) {
     if (e != cudaSuccess) st = cuda_fail(e, "profile events");
     if (r.kind >= 0 && r.kind < kProfKinds) {
       if (ms) ms[r.kind] += t;
-      if (launches) launches[r.kind] += 1;
+      if (launches) launches[r.kind] += r.count;
     }
     cudaEventDestroy(r.a);
     cudaEventDestroy(r.b);

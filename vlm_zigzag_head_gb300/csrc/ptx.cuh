@@ -248,6 +248,16 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
   return r;
 }
+// Programmatic dependent launch: let the next kernel of the stream start its
+// CTAs once every CTA of this grid has issued this (or exited) ...
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+// ... and, in that next kernel, wait until the previous grid has completed
+// and its memory operations are visible (returns at once without PDL).
+__device__ __forceinline__ void griddep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
 // Vector fp32 reduce-add into global memory (16-byte aligned address).
 __device__ __forceinline__ void red_add_v4(float4* p, float4 v) {
   asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(v.x), "f"(v.y),

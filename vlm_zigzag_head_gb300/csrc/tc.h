@@ -35,6 +35,7 @@ struct TcFwdArgs {
   int Hkv;                    // KV heads; query head h reads KV head h / (H / Hkv)
   float scale_log2;           // softmax scale * log2(e)
   int split_p;                // P enters PV as bf16 hi + lo (softmax scale > kPrecisionSplitScale)
+  int pdl;                    // launched as a programmatic dependent of the previous ring step
   float* o_run; float* lse_run; int64_t run_rows;
   void* out; float* lse; int64_t T;
   void* out_lo;               // nullable: bf16 remainder o - bf16(o)
@@ -58,6 +59,7 @@ struct TcBwdArgs {
   long long wait_limit;
   int kv_split;               // CTAs sharing one KV head's query heads (divides H / Hkv); > 1:
                               // dK / dV / prefix slots are reduce-added into zeroed memory
+  int pdl;                    // launched as a programmatic dependent of the previous ring step
 };
 cudaError_t launch_tc_bwd(const TcBwdArgs& a, cudaStream_t st);
 

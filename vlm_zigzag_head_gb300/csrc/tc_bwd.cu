@@ -179,6 +179,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
+  // the next ring step's CTAs may take SMs as this step's CTAs finish; they
+  // wait for this grid before their dK / dV epilogue (griddep_wait below)
+  griddep_launch_dependents();
 
   const int nseg = it.nseg;
   int n_qt = 0;   // query tiles of one query head
@@ -517,6 +520,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
     }
     // ------------------------------------------------------------ dK / dV epilogue
     if (ok && n_all > 0 && !mbar_wait(&bars->dkv_done, 0, lim, abort)) ok = false;
+    // dK / dV rows accumulate over ring steps: the previous step's grid must
+    // be complete (a no-op unless launched as a programmatic dependent)
+    griddep_wait();
     if (!ok) {
       record_timeout(a.status, abort, 13);
     } else {
@@ -578,8 +584,17 @@ cudaError_t launch_split(const TcBwdArgs& a, cudaStream_t st) {
   if (e != cudaSuccess) return e;
   const long long blocks = (long long)a.n_items * a.Hkv * a.kv_split;
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  tc_bwd_kernel<kSplit, kShared><<<(unsigned)blocks, kThreads, smem, st>>>(a);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)blocks);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = a.pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, tc_bwd_kernel<kSplit, kShared>, a);
 }
 
 }  // namespace

@@ -133,6 +133,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
+  // the next ring step's CTAs may take SMs as this step's CTAs finish; they
+  // wait for this grid before their merge epilogue (griddep_wait below)
+  griddep_launch_dependents();
   // 384 threads launch with 168 registers each; warpgroup 0 (TMA, MMA) drops
   // to 72 and the two softmax warpgroups rise to 216, enough to hold a whole
   // 128-column S row: 128 * 72 + 256 * 216 = 384 * 168
@@ -390,6 +393,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
     // ------------------------------------------------------------ epilogue
     if (ok && n_tiles > 0 && !mbar_wait(&bars->o_done[x], (n_tiles - 1) & 1, lim, abort))
       ok = false;
+    // the running result was written by the previous ring step: its grid must
+    // be complete (a no-op unless launched as a programmatic dependent)
+    griddep_wait();
     if (!ok) {
       record_timeout(a.status, abort, 5);
     } else {
@@ -488,8 +494,17 @@ cudaError_t launch_d(const TcFwdArgs& a, cudaStream_t st) {
   if (e != cudaSuccess) return e;
   const long long blocks = (long long)a.n_items * a.H;
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  tc_fwd_kernel<D, kSplitP><<<(unsigned)blocks, kThreads, smem, st>>>(a);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)blocks);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = a.pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, tc_fwd_kernel<D, kSplitP>, a);
 }
 
 }  // namespace
