@@ -296,9 +296,11 @@ cp_status_t cp_plan_pairs(const int32_t* cu_seqlens_h, int n_seqs, int prefix_le
 /*
  * cp_profile_begin / cp_profile_end -- instrumentation: between the two calls
  * the library records a pair of CUDA events on the launching stream around
- * every kernel it launches (any thread).  cp_profile_end synchronises those
- * events and returns, per kernel kind, the summed milliseconds and the launch
- * count in ms[8] / launches[8] (either may be NULL):
+ * every kernel it launches (any thread); the P tensor-core ring-step launches
+ * of one call, which overlap one another's tails, share one pair that counts
+ * as P launches.  cp_profile_end synchronises those events and returns, per
+ * kernel kind, the summed milliseconds and the launch count in ms[8] /
+ * launches[8] (either may be NULL):
  *   0 zigzag index   1 zigzag gather   2 tensor-core forward ring step
  *   3 backward preprocess   4 tensor-core backward ring step
  *   5 prefix-gradient sum   6 CUDA-core forward step   7 CUDA-core backward step
