@@ -66,12 +66,13 @@ struct Smem {
 static_assert(Smem<128>::kAlloc <= 227 * 1024, "shared memory budget");
 
 struct Bars {
-  uint64_t q_full;
+  uint64_t q_full, q_empty;   // Q of the CTA's current unit landed / free again
   uint64_t k_full[kStages], k_empty[kStages];
   uint64_t v_full[kStages], v_empty[kStages];
   uint64_t s_full[2];   // per tile: S(j) in TMEM
   uint64_t p_full[2];   // per tile: P(j) in TMEM (4 softmax warps)
   uint64_t o_done[2];   // per tile: PV(j) accumulated
+  uint64_t o_free[2];   // per tile: the epilogue has read O (4 softmax warps)
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
@@ -85,6 +86,13 @@ __device__ __forceinline__ int run_tiles(const Seg& s, int q_len) {
     vis = vis < 0 ? 0 : (vis < s.len ? vis : s.len);
   }
   return (vis + kBN - 1) / kBN;
+}
+
+// KV tiles an item visits over all its key runs.
+__device__ __forceinline__ int item_tiles(const FwdItem& it) {
+  int n = 0;
+  for (int s = 0; s < it.nseg; ++s) n += run_tiles(it.seg[s], it.q_len);
+  return n;
 }
 
 __device__ __forceinline__ void record_timeout(int32_t* status, volatile int* abort, int site) {
@@ -101,15 +109,19 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
   using L = Smem<D>;
   Bars* bars = reinterpret_cast<Bars*>(smem + L::kBars);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int item_idx = blockIdx.x % a.n_items;
-  const int h = blockIdx.x / a.n_items;
-  const int hk = h / (a.H / a.Hkv);   // the KV head of query head h (grouped-query attention)
-  const FwdItem& it = a.items[item_idx];
+  // Persistent CTA: units u = blockIdx.x, blockIdx.x + gridDim.x, ... are
+  // (item u % n_items, query head u / n_items), walked in that order by every
+  // role.  KV tiles are numbered across units, so stage indices and barrier
+  // phases simply continue; so are the units that visit at least one tile
+  // ("tiled units", whose Q is loaded and whose O lives in TMEM).
+  const int n_units = a.n_items * a.H;
+  const int G = a.H / a.Hkv;   // query heads per KV head (grouped-query attention)
   volatile int* abort = &bars->abort;
   const long long lim = a.wait_limit;
 
   if (threadIdx.x == 0) {
     mbar_init(&bars->q_full, 1);
+    mbar_init(&bars->q_empty, 1);
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&bars->k_full[s], 1);
       mbar_init(&bars->k_empty[s], 1);
@@ -120,6 +132,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
       mbar_init(&bars->s_full[x], 1);
       mbar_init(&bars->p_full[x], 4);
       mbar_init(&bars->o_done[x], 1);
+      mbar_init(&bars->o_free[x], 4);
     }
     mbar_init(&bars->drain, 1);
     bars->abort = 0;
@@ -140,62 +153,71 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
   // to 72 and the two softmax warpgroups rise to 216, enough to hold a whole
   // 128-column S row: 128 * 72 + 256 * 216 = 384 * 168
 
-  const int q_len = it.q_len;   // rows of the item (tile A: first 128, tile B: the rest)
-  const int nseg = it.nseg;
-  int n_tiles = 0;
-  for (int s = 0; s < nseg; ++s) n_tiles += run_tiles(it.seg[s], q_len);
 
   if (warp < 4) {
   setmaxnreg_dec<72>();
   if (warp == 0 || warp == 2) {
-    // ------------------------------------------------------------ TMA producers
+    // ------------------------------------------------------------ TMA producers of K, V
     if (lane == 0) {
       const bool is_k = warp == 0;
       int issued = 0;
-      bool q_issued = false;
-      if (is_k && n_tiles > 0) {
+      int j = 0;   // KV tile counter across units
+      for (int u = blockIdx.x; u < n_units && !*abort; u += gridDim.x) {
+        const FwdItem& it = a.items[u % a.n_items];
+        const int hk = (u / a.n_items) / G;
+        for (int s = 0; s < it.nseg && !*abort; ++s) {
+          const Seg sg = it.seg[s];
+          const CUtensorMap* m = is_k ? (sg.src == SRC_TEXT ? &a.tm_k_text : &a.tm_k_nat)
+                                      : (sg.src == SRC_TEXT ? &a.tm_v_text : &a.tm_v_nat);
+          const int nt = run_tiles(sg, it.q_len);
+          for (int t = 0; t < nt; ++t, ++j) {
+            const int st = j % kStages;
+            uint64_t* empty = is_k ? &bars->k_empty[st] : &bars->v_empty[st];
+            uint64_t* full = is_k ? &bars->k_full[st] : &bars->v_full[st];
+            if (j >= kStages && !mbar_wait(empty, ((j / kStages) - 1) & 1, lim, abort)) {
+              record_timeout(a.status, abort, is_k ? 1 : 2);
+              break;
+            }
+            uint8_t* dst = smem + (is_k ? L::kK : L::kV) + st * L::kTile;
+            mbar_expect_tx(full, L::kTile);
+            for (int b = 0; b < D / 64; ++b)
+              tma_load_3d(m, full, dst + b * L::kBox, b * 64, hk, sg.row0 + t * kBN);
+            issued = j + 1;
+          }
+        }
+      }
+      // every load this producer issued must land before the CTA exits
+      // (normally the MMA issuer already waited for them: these return at once)
+      int zero = 0;
+      for (int x = issued - kStages; x < issued; ++x) {
+        if (x < 0) continue;
+        const int st = x % kStages;
+        uint64_t* full = is_k ? &bars->k_full[st] : &bars->v_full[st];
+        mbar_wait(full, (x / kStages) & 1, kDrainLimit, &zero);
+      }
+    }
+  } else if (warp == 3) {
+    // ------------------------------------------------------------ TMA producer of Q
+    // Q of tiled unit n + 1 loads once the products of unit n are done.
+    if (lane == 0) {
+      int n = 0;   // tiled units so far
+      for (int u = blockIdx.x; u < n_units && !*abort; u += gridDim.x) {
+        const FwdItem& it = a.items[u % a.n_items];
+        if (item_tiles(it) == 0) continue;
+        if (n > 0 && !mbar_wait(&bars->q_empty, (n - 1) & 1, lim, abort)) {
+          record_timeout(a.status, abort, 6);
+          break;
+        }
         const CUtensorMap* qm = it.q_src == SRC_TEXT ? &a.tm_q_text : &a.tm_q_nat;
         mbar_expect_tx(&bars->q_full, 2 * L::kTile);
         for (int x = 0; x < 2; ++x)
           for (int b = 0; b < D / 64; ++b)
-            tma_load_3d(qm, &bars->q_full, smem + L::kQ + x * L::kTile + b * L::kBox, b * 64, h,
-                        it.q_row0 + x * kBM);
-        q_issued = true;
+            tma_load_3d(qm, &bars->q_full, smem + L::kQ + x * L::kTile + b * L::kBox, b * 64,
+                        u / a.n_items, it.q_row0 + x * kBM);
+        ++n;
       }
-      int j = 0;
-      for (int s = 0; s < nseg && !*abort; ++s) {
-        const Seg sg = it.seg[s];
-        const CUtensorMap* m = is_k ? (sg.src == SRC_TEXT ? &a.tm_k_text : &a.tm_k_nat)
-                                    : (sg.src == SRC_TEXT ? &a.tm_v_text : &a.tm_v_nat);
-        const int nt = run_tiles(sg, q_len);
-        for (int t = 0; t < nt; ++t, ++j) {
-          const int st = j % kStages;
-          uint64_t* empty = is_k ? &bars->k_empty[st] : &bars->v_empty[st];
-          uint64_t* full = is_k ? &bars->k_full[st] : &bars->v_full[st];
-          if (j >= kStages && !mbar_wait(empty, ((j / kStages) - 1) & 1, lim, abort)) {
-            record_timeout(a.status, abort, is_k ? 1 : 2);
-            break;
-          }
-          uint8_t* dst = smem + (is_k ? L::kK : L::kV) + st * L::kTile;
-          mbar_expect_tx(full, L::kTile);
-          for (int b = 0; b < D / 64; ++b)
-            tma_load_3d(m, full, dst + b * L::kBox, b * 64, hk, sg.row0 + t * kBN);
-          issued = j + 1;
-        }
-        if (*abort) break;
-      }
-      // every load this producer issued must land before the CTA exits
-      // (normally the MMA issuer already waited for them: these return at once)
-      {
-        int zero = 0;
-        if (q_issued) mbar_wait(&bars->q_full, 0, kDrainLimit, &zero);
-        for (int x = issued - kStages; x < issued; ++x) {
-          if (x < 0) continue;
-          const int st = x % kStages;
-          uint64_t* full = is_k ? &bars->k_full[st] : &bars->v_full[st];
-          mbar_wait(full, (x / kStages) & 1, kDrainLimit, &zero);
-        }
-      }
+      int zero = 0;
+      if (n > 0) mbar_wait(&bars->q_full, (n - 1) & 1, kDrainLimit, &zero);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
@@ -203,8 +225,6 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
       constexpr uint32_t idesc_qk = idesc_bf16(kBM, kBN, 0, 0);
       constexpr uint32_t idesc_pv = idesc_bf16(kBM, D, 0, 1);
       const uint32_t q_addr = smem_u32(smem + L::kQ);
-      bool ok = n_tiles == 0 || mbar_wait(&bars->q_full, 0, lim, abort);
-      if (!ok) record_timeout(a.status, abort, 3);
       // S_x(j) = Q_x K_j^T into tile x's S buffer
       auto issue_s = [&](int x, int j) {
         const uint32_t k_addr = smem_u32(smem + L::kK + (j % kStages) * L::kTile);
@@ -217,18 +237,21 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
         }
         mma_commit(&bars->s_full[x]);
       };
-      // O_x += P_x(j) V_j, P from TMEM (keys 16kk.. 16kk+15: columns 8kk .. 8kk+7)
-      auto issue_pv = [&](int x, int j) -> bool {
+      // O_x += P_x(j) V_j, P from TMEM (keys 16kk.. 16kk+15: columns 8kk .. 8kk+7);
+      // `first`: the unit's first tile, which overwrites O (after the previous
+      // unit's epilogue has read it: o_free of tiled unit n - 1)
+      auto issue_pv = [&](int x, int j, bool first, int n) -> bool {
         const int st = j % kStages;
         if (!mbar_wait(&bars->p_full[x], j & 1, lim, abort)) return false;
         if (x == 0 && !mbar_wait(&bars->v_full[st], (j / kStages) & 1, lim, abort)) return false;
+        if (first && n > 0 && !mbar_wait(&bars->o_free[x], (n - 1) & 1, lim, abort)) return false;
         tc_fence_after();
         const uint32_t v_addr = smem_u32(smem + L::kV + st * L::kTile);
 #pragma unroll
         for (int kk = 0; kk < kBN / 16; ++kk) {
           const uint64_t bd = sdesc_sw128(v_addr + kk * 16 * 128, L::kBox, 1024);
           mma_bf16_ts(tmem + col_o(x), tmem + col_s(x) + kk * 8, bd, idesc_pv,
-                      (j > 0 || kk > 0) ? 1u : 0u);
+                      (!first || kk > 0) ? 1u : 0u);
           if constexpr (kSplitP)   // the bf16 remainder of P, in S columns [64, 128)
             mma_bf16_ts(tmem + col_o(x), tmem + col_s(x) + 64 + kk * 8, bd, idesc_pv, 1u);
         }
@@ -236,20 +259,33 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
         if (x == 1) mma_commit(&bars->v_empty[st]);
         return true;
       };
-      for (int j = 0; ok && j < n_tiles; ++j) {
-        const int st = j % kStages;
-        if (!mbar_wait(&bars->k_full[st], (j / kStages) & 1, lim, abort)) {
-          ok = false;
-          break;
+      bool ok = true;
+      int j = 0;   // KV tile counter across units
+      int n = 0;   // tiled units so far
+      for (int u = blockIdx.x; ok && u < n_units; u += gridDim.x) {
+        const int n_tiles = item_tiles(a.items[u % a.n_items]);
+        if (n_tiles == 0) continue;
+        if (!mbar_wait(&bars->q_full, n & 1, lim, abort)) { ok = false; break; }
+        const int j0 = j;
+        for (int jj = 0; jj < n_tiles; ++jj, ++j) {
+          const int st = j % kStages;
+          if (!mbar_wait(&bars->k_full[st], (j / kStages) & 1, lim, abort)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          if (jj >= 1 && !issue_pv(0, j - 1, j - 1 == j0, n)) { ok = false; break; }
+          issue_s(0, j);
+          if (jj >= 1 && !issue_pv(1, j - 1, j - 1 == j0, n)) { ok = false; break; }
+          issue_s(1, j);
+          mma_commit(&bars->k_empty[st]);
         }
-        tc_fence_after();
-        if (j >= 1 && !issue_pv(0, j - 1)) { ok = false; break; }
-        issue_s(0, j);
-        if (j >= 1 && !issue_pv(1, j - 1)) { ok = false; break; }
-        issue_s(1, j);
-        mma_commit(&bars->k_empty[st]);
+        if (ok && !(issue_pv(0, j - 1, j - 1 == j0, n) && issue_pv(1, j - 1, j - 1 == j0, n)))
+          ok = false;
+        if (!ok) break;
+        mma_commit(&bars->q_empty);   // every product of this unit that reads Q is done
+        ++n;
       }
-      if (ok && n_tiles > 0 && !(issue_pv(0, n_tiles - 1) && issue_pv(1, n_tiles - 1))) ok = false;
       if (!ok) {
         record_timeout(a.status, abort, 4);
         // drain: nothing issued by this thread may still be running at exit
@@ -268,10 +304,17 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     const uint32_t s_col = tmem + lane_off + col_s(x);
     const float sl2 = a.scale_log2;
+    bool ok = true;
+    int j = 0;   // KV tile counter across units
+    for (int u = blockIdx.x; ok && u < n_units; u += gridDim.x) {
+    const FwdItem& it = a.items[u % a.n_items];
+    const int h = u / a.n_items;
+    const int q_len = it.q_len;   // rows of the item (tile A: first 128, tile B: the rest)
+    const int nseg = it.nseg;
+    const int n_tiles = item_tiles(it);
+    const int j0 = j;
     float m = -INFINITY;   // running max of scaled scores (log2 units), may lag
     float l = 0.f;
-    bool ok = true;
-    int j = 0;
     for (int s = 0; ok && s < nseg; ++s) {
       const Seg sg = it.seg[s];
       const int nt = run_tiles(sg, q_len);
@@ -314,7 +357,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
             l *= alpha;
             m = m_new;
           }
-          if (j > 0) {  // O holds PV of earlier tiles (complete: PV_x(j-1) precedes S_x(j))
+          if (j > j0) {  // O holds PV of earlier tiles (complete: PV_x(j-1) precedes S_x(j))
             if (!mbar_wait(&bars->o_done[x], (j - 1) & 1, lim, abort)) { ok = false; break; }
             tc_fence_after();
 #pragma unroll 1
@@ -391,14 +434,16 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
       }
     }
     // ------------------------------------------------------------ epilogue
-    if (ok && n_tiles > 0 && !mbar_wait(&bars->o_done[x], (n_tiles - 1) & 1, lim, abort))
+    if (ok && n_tiles > 0 && !mbar_wait(&bars->o_done[x], (j - 1) & 1, lim, abort))
       ok = false;
     // the running result was written by the previous ring step: its grid must
     // be complete (a no-op unless launched as a programmatic dependent)
     griddep_wait();
     if (!ok) {
       record_timeout(a.status, abort, 5);
-    } else {
+      break;
+    }
+    {
       tc_fence_after();
       const bool valid = tq < q_len;
       float lse_s = l > 0.f ? (m + __log2f(l)) * 0.6931471805599453f : -INFINITY;
@@ -426,9 +471,14 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
 #pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {
         uint32_t r[32];
-        tmem_ld32(tmem + lane_off + col_o(x) + c * 32, r);
-        tmem_ld_wait();
-        reg_fence32(r);
+        if (n_tiles > 0) {
+          tmem_ld32(tmem + lane_off + col_o(x) + c * 32, r);
+          tmem_ld_wait();
+          reg_fence32(r);
+        } else {   // no key visible: O was never written for this unit
+#pragma unroll
+          for (int i = 0; i < 32; ++i) r[i] = 0u;
+        }
         if (!valid) continue;
         float o[32];
 #pragma unroll
@@ -477,6 +527,12 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
         else a.lse_run[rrow] = lse_s;
       }
     }
+    if (n_tiles > 0) {   // O of this unit is read: the next unit's first PV may overwrite it
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->o_free[x]);
+    }
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -492,8 +548,16 @@ cudaError_t launch_d(const TcFwdArgs& a, cudaStream_t st) {
   cudaError_t e = cudaFuncSetAttribute(tc_fwd_kernel<D, kSplitP>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  const long long blocks = (long long)a.n_items * a.H;
-  if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  // persistent: one CTA per SM walks units gridDim.x apart
+  int dev = 0, sms = 0;
+  e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  const long long units = (long long)a.n_items * a.H;
+  if (units > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  // with few units per SM (under 4), one CTA per unit: a static share of
+  // units per CTA would leave some CTAs a whole unit behind the others
+  const long long blocks = units < 4LL * sms ? units : sms;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)blocks);
   cfg.blockDim = dim3(kThreads);
