@@ -280,10 +280,14 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
           issue_s(1, j);
           mma_commit(&bars->k_empty[st]);
         }
-        if (ok && !(issue_pv(0, j - 1, j - 1 == j0, n) && issue_pv(1, j - 1, j - 1 == j0, n)))
-          ok = false;
         if (!ok) break;
-        mma_commit(&bars->q_empty);   // every product of this unit that reads Q is done
+        // the unit's S products, the only readers of Q, are all issued: the
+        // next unit's Q may load while the last PV products run
+        mma_commit(&bars->q_empty);
+        if (!(issue_pv(0, j - 1, j - 1 == j0, n) && issue_pv(1, j - 1, j - 1 == j0, n))) {
+          ok = false;
+          break;
+        }
         ++n;
       }
       if (!ok) {
