@@ -1,11 +1,13 @@
 // Ring-step attention forward on 5th-generation tensor cores (sm_103a).
 //
-// One CTA computes one work item of a ring step for one head: up to 256 query
-// rows, taken as two 128-row tiles A and B, against the key runs the step
-// gives them (page "context-parallel-multimodal": §1.1 zigzag chunks, §1 ring
-// order, §4.1 replicated prefix in step 0), with an online softmax over the
-// KV tiles and a fused log-sum-exp merge into the fp32 running result (or the
-// final write in natural order).  Both tiles share every K / V tile.
+// A unit is one work item of a ring step for one head: up to 256 query rows,
+// taken as two 128-row tiles A and B, against the key runs the step gives
+// them (page "context-parallel-multimodal": §1.1 zigzag chunks, §1 ring order,
+// §4.1 replicated prefix in step 0), with an online softmax over the KV tiles
+// and a fused log-sum-exp merge into the fp32 running result (or the final
+// write in natural order).  Both tiles share every K / V tile.  The kernel is
+// persistent: a CTA walks units gridDim.x apart, with its barrier phases and
+// K / V stages continuing from one unit to the next.
 //
 // The two tiles ping-pong: the tensor core computes one tile's products while
 // the other tile's softmax runs.  Issue order for KV tile j >= 1:
@@ -13,10 +15,10 @@
 // (S_A(j) overwrites the TMEM that holds P_A(j-1), so PV_A(j-1) goes first).
 //
 // Warp roles (384 threads; TMEM lane quarter of warp w is w % 4):
-//   warp 0       TMA producer of Q (both tiles) and K
+//   warp 0       TMA producer of K
 //   warp 1       TMEM allocation; lane 0 issues every tcgen05.mma
 //   warp 2       TMA producer of V
-//   warp 3       idle
+//   warp 3       TMA producer of Q (both tiles of a unit)
 //   warps 4..7   softmax + epilogue of tile A; thread = query row = TMEM lane
 //   warps 8..11  softmax + epilogue of tile B
 //
