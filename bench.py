@@ -277,7 +277,6 @@ def run_cuda(args, w, rank, world, dist):
     bwd_ms_k, bwd_launches = prof["tc_bwd_step"]
     fwd_ms_k, fwd_launches = prof["tc_fwd_step"]
     bwd_launch_flops = 2.5 * f_flops / P
-    fwd_launch_flops = f_flops / P
     roof = None
     if bwd_launches:
         avg = bwd_ms_k / bwd_launches
@@ -294,11 +293,13 @@ def run_cuda(args, w, rank, world, dist):
         if n:
             kernels[k] = {"launches": n, "ms_total": kms, "share": kms / max(ms, 1e-9)}
     if fwd_launches:
-        avg = fwd_ms_k / fwd_launches
-        kernels["tc_fwd_step"]["achieved_tflops"] = fwd_launch_flops / (avg / 1e3) / 1e12
+        # one forward call is one all-steps launch (P ring-step launches under
+        # CPATTN_FWD_PER_STEP=1): rate over the kernel time of a whole call
+        avg = fwd_ms_k / args.steps
+        kernels["tc_fwd_step"]["achieved_tflops"] = f_flops / (avg / 1e3) / 1e12
         # secondary bound: one exp2 per visible pair and head, against the MUFU
         # rate (32 exp2 per clock per SM on this part) at the maximum SM clock
-        exps = causal_pairs(w) * H / P
+        exps = causal_pairs(w) * H
         mufu = EX2_PER_CLK_SM * torch.cuda.get_device_properties(dev).multi_processor_count * \
             float(peaks.get("sm_max_mhz", 2070.0)) * 1e6
         kernels["tc_fwd_step"]["exp_per_s"] = exps / (avg / 1e3)

@@ -120,12 +120,17 @@ cp_status_t cp_zigzag_scatter(const void* src, void* dst, size_t row_bytes, cons
  * CP-VLM page §1.1 (zigzag split), §1 (Ring Attention), §4.1 (replicated
  * prefix), §5.3 (cu_seqlens).
  *
- * The text rows of q, k, v are gathered into rank-local order (the split),
- * then for ring step s = 0..P-1 one kernel computes, for every simulated rank
- * r, the partial attention of its queries over the KV of rank (r-s) mod P
- * (step 0: [replicated prefix, own chunks]) and merges it by log-sum-exp into
- * an fp32 running result; the last contributing step writes out/lse in
- * natural order.  Prefix query rows attend causally to their own prefix once.
+ * The text rows of q, k, v are gathered into rank-local order (the split).
+ * At ring step s = 0..P-1 every simulated rank r meets the KV of rank
+ * (r-s) mod P (step 0: [replicated prefix, own chunks]), and the per-step
+ * partial results are merged by log-sum-exp; out/lse are written in natural
+ * order.  Prefix query rows attend causally to their own prefix once.  On the
+ * tensor-core path one persistent kernel walks, per query tile, the KV tiles
+ * of every ring step in ring order, so the merge is its online softmax and no
+ * partial result leaves the chip.  CP_F32 (and CP_BF16 under
+ * CPATTN_FWD_PER_STEP=1) launch one kernel per ring step that merges into an
+ * fp32 running result in the workspace; the last contributing step writes
+ * out/lse.
  *
  *   q, k, v    [T][H][d], dtype dt (CP_BF16: tensor-core path, fp32
  *              accumulation; CP_F32: fp32 CUDA-core path)
@@ -285,9 +290,11 @@ cp_status_t cp_workspace_status(const void* workspace, void* stream);
  * the backward work lists cover (prefix-query pairs are part of step 0) and
  * the number of work items.  Forward figures are those of the 256-query items
  * of the tensor-core kernel; the 128-query items of the CUDA-core kernel are
- * checked to cover the same pairs.  Any output may be NULL.  Needs no GPU.
- * Errors: CP_ERR_INVALID_ARG, CP_ERR_SHAPE, CP_ERR_UNSUPPORTED (the two
- * forward work lists disagree: an internal error).
+ * checked to cover the same pairs, and the all-steps items of the default
+ * tensor-core forward (every ring step of one query tile in one item) to
+ * cover their sum.  Any output may be NULL.  Needs no GPU.
+ * Errors: CP_ERR_INVALID_ARG, CP_ERR_SHAPE, CP_ERR_UNSUPPORTED (the forward
+ * work lists disagree: an internal error).
  */
 cp_status_t cp_plan_pairs(const int32_t* cu_seqlens_h, int n_seqs, int prefix_len, int P,
                           int64_t* fwd_pairs, int64_t* bwd_pairs, int64_t* fwd_items,
@@ -296,12 +303,13 @@ cp_status_t cp_plan_pairs(const int32_t* cu_seqlens_h, int n_seqs, int prefix_le
 /*
  * cp_profile_begin / cp_profile_end -- instrumentation: between the two calls
  * the library records a pair of CUDA events on the launching stream around
- * every kernel it launches (any thread); the P tensor-core ring-step launches
- * of one call, which overlap one another's tails, share one pair that counts
- * as P launches.  cp_profile_end synchronises those events and returns, per
+ * every kernel it launches (any thread).  The tensor-core forward is one
+ * launch covering all ring steps; with CPATTN_FWD_PER_STEP=1 in the
+ * environment it is P ring-step launches, which overlap one another's tails
+ * and share one pair that counts as P launches.  cp_profile_end synchronises those events and returns, per
  * kernel kind, the summed milliseconds and the launch count in ms[8] /
  * launches[8] (either may be NULL):
- *   0 zigzag index   1 zigzag gather   2 tensor-core forward ring step
+ *   0 zigzag index   1 zigzag gather   2 tensor-core forward (ring steps)
  *   3 backward preprocess   4 tensor-core backward ring step
  *   5 prefix-gradient sum   6 CUDA-core forward step   7 CUDA-core backward step
  * Errors: CP_ERR_CUDA.

@@ -3,6 +3,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <cstdio>
@@ -109,14 +110,41 @@ Stager& stager() {
 // ---------------------------------------------------------------------------
 // plan cache (plans depend only on cu_seqlens, prefix_len and P)
 // ---------------------------------------------------------------------------
+// Unit lists of the persistent all-steps forward for one (heads, grid):
+// `packed` holds the units, then cta_off (grid + 1 entries).
+struct UnitLists {
+  int H = 0, grid = 0;
+  size_t n_units = 0;
+  std::vector<int32_t> packed;
+};
+
 struct PlanSet {
   Problem pb;
   FwdPlan fwd;       // text rows in rank-local order, 128-row items (CUDA cores)
   FwdPlan fwd2;      // text rows in rank-local order, 256-row items (tensor cores)
+  FusedFwdPlan fused;  // fwd2 with all ring steps of a query tile in one item
   FwdPlan fwd_nat;   // text rows in natural order (fp32 dQ pass)
   BwdPlan bwd;
   std::vector<int32_t> samples;  // [n][4]: t0, c, off, ord0 (index kernel)
+  std::mutex ul_mu;
+  std::vector<std::shared_ptr<const UnitLists>> ul;  // recent unit lists
 };
+
+std::shared_ptr<const UnitLists> unit_lists(PlanSet& ps, int H, int grid) {
+  std::lock_guard<std::mutex> lk(ps.ul_mu);
+  for (const auto& p : ps.ul)
+    if (p->H == H && p->grid == grid) return p;
+  auto u = std::make_shared<UnitLists>();
+  u->H = H;
+  u->grid = grid;
+  std::vector<int32_t> cta_off;
+  plan_unit_lists(ps.fused.items, H, grid, &u->packed, &cta_off);
+  u->n_units = u->packed.size();
+  u->packed.insert(u->packed.end(), cta_off.begin(), cta_off.end());
+  ps.ul.push_back(u);
+  if (ps.ul.size() > 4) ps.ul.erase(ps.ul.begin());
+  return u;
+}
 
 struct PlanCache {
   std::mutex mu;
@@ -147,6 +175,7 @@ cp_status_t get_plans(const int32_t* cu, int n_seqs, int N, int P, int T, int H,
   ps->pb = pb;
   plan_forward(pb, true, &ps->fwd);
   plan_forward(pb, true, &ps->fwd2, kFwdPairQ);
+  plan_forward_fused(ps->fwd2, P, &ps->fused);
   plan_forward(pb, false, &ps->fwd_nat);
   plan_backward(pb, &ps->bwd);
   int64_t ord = 0;
@@ -168,15 +197,19 @@ cp_status_t get_plans(const int32_t* cu, int n_seqs, int N, int P, int T, int H,
 // workspace layouts
 // ---------------------------------------------------------------------------
 struct FwdWs {
-  size_t status = 0, items = 0, samples = 0, idx = 0, qkv[3] = {0, 0, 0}, o_run = 0, lse_run = 0,
-         total = 0;
+  size_t status = 0, items = 0, runs = 0, units = 0, samples = 0, idx = 0, qkv[3] = {0, 0, 0},
+         o_run = 0, lse_run = 0, total = 0;
 };
 
 FwdWs fwd_layout(const PlanSet& ps, int H, int Hkv, int d, size_t elem) {
   FwdWs w;
   size_t o = 0;
   w.status = o; o += kStatusBytes;
-  w.items = o; o = align_up(o + ps.fwd.items.size() * sizeof(FwdItem), 256);
+  w.items = o;
+  o = align_up(o + std::max(ps.fwd.items.size(), ps.fused.items.size()) * sizeof(FwdItem), 256);
+  w.runs = o; o = align_up(o + ps.fused.runs.size() * sizeof(Seg), 256);
+  // unit lists: units, then cta_off (at most units + 1 entries)
+  w.units = o; o = align_up(o + (2 * ps.fused.items.size() * H + 1) * sizeof(int32_t), 256);
   w.samples = o; o = align_up(o + ps.samples.size() * sizeof(int32_t), 256);
   w.idx = o; o = align_up(o + (size_t)ps.pb.text_rows * sizeof(int32_t), 256);
   // rank-local q [rows][H][d]; k, v [rows][Hkv][d]
@@ -242,6 +275,17 @@ cp_status_t check_device_for_bf16() {
   if (major != 10 || minor != 3)
     return fail(CP_ERR_UNSUPPORTED, "the bf16 path is built for sm_103a (compute capability 10.3)");
   return CP_OK;
+}
+
+// The tensor-core forward runs all ring steps in one launch unless
+// CPATTN_FWD_PER_STEP=1 asks for one launch per ring step with the fp32
+// running result in between (the same arithmetic, merged in another order).
+bool use_fused_forward() {
+  static int v = [] {
+    const char* e = getenv("CPATTN_FWD_PER_STEP");
+    return (e && e[0] == '1') ? 0 : 1;
+  }();
+  return v != 0;
 }
 
 bool use_tc_path() {
@@ -427,8 +471,18 @@ cp_status_t cp_attn_fwd_gqa(const void* q, const void* k, const void* v, cp_dtyp
   const Problem& pb = ps->pb;
   CP_CUDA(cudaMemsetAsync(w + L.status, 0, kStatusBytes, st), "clear status");
   const FwdPlan& fp = tc ? ps->fwd2 : ps->fwd;  // items of 256 (tensor cores) / 128 rows
-  CP_CUDA(stager().upload(w + L.items, fp.items.data(), fp.items.size() * sizeof(FwdItem), st),
-          "upload work list");
+  const bool fused = tc && use_fused_forward();
+  if (fused) {
+    CP_CUDA(stager().upload(w + L.items, ps->fused.items.data(),
+                            ps->fused.items.size() * sizeof(FwdItem), st),
+            "upload work list");
+    CP_CUDA(stager().upload(w + L.runs, ps->fused.runs.data(),
+                            ps->fused.runs.size() * sizeof(Seg), st),
+            "upload key runs");
+  } else {
+    CP_CUDA(stager().upload(w + L.items, fp.items.data(), fp.items.size() * sizeof(FwdItem), st),
+            "upload work list");
+  }
   CP_CUDA(stager().upload(w + L.samples, ps->samples.data(), ps->samples.size() * 4, st),
           "upload sample table");
   int32_t* idx = reinterpret_cast<int32_t*>(w + L.idx);
@@ -477,6 +531,33 @@ cp_status_t cp_attn_fwd_gqa(const void* q, const void* k, const void* v, cp_dtyp
     a.out = out; a.lse = lse; a.T = T; a.out_lo = out_lo;
     a.status = reinterpret_cast<int32_t*>(w + L.status);
     a.wait_limit = wait_limit();
+    a.runs = nullptr;
+    a.units = nullptr;
+    a.cta_off = nullptr;
+    a.n_ctas = 0;
+    if (fused) {  // every ring step of every query tile in one persistent launch
+      a.items = items;
+      a.n_items = (int)ps->fused.items.size();
+      a.runs = reinterpret_cast<const Seg*>(w + L.runs);
+      a.pdl = 0;
+      int dev = 0, sms = 0;
+      CP_CUDA(cudaGetDevice(&dev), "cudaGetDevice");
+      CP_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev), "SM count");
+      const long long units = (long long)a.n_items * H;
+      const long long grid = fwd_grid(units, sms);
+      if (grid < units) {  // persistent CTAs: equal shares of work, head by head
+        std::shared_ptr<const UnitLists> ul = unit_lists(*ps, H, (int)grid);
+        CP_CUDA(stager().upload(w + L.units, ul->packed.data(),
+                                ul->packed.size() * sizeof(int32_t), st),
+                "upload unit lists");
+        a.units = reinterpret_cast<const int32_t*>(w + L.units);
+        a.cta_off = a.units + ul->n_units;
+        a.n_ctas = (int)grid;
+      }
+      ProfScope ps_(2, st);
+      CP_CUDA(launch_tc_fwd(a, st), "tensor-core forward (all ring steps)");
+      return CP_OK;
+    }
     // Ring steps after the first are programmatic dependents of the one
     // before: their CTAs fill SMs as the previous step drains and wait for it
     // only at the merge.  One profiling interval spans the P launches.
@@ -727,25 +808,36 @@ cp_status_t cp_plan_pairs(const int32_t* cu, int n_seqs, int N, int P, int64_t* 
   std::string err = make_problem(cu, n_seqs, N, P, -1, &pb);
   if (!err.empty()) return fail(CP_ERR_SHAPE, err);
   // forward: the 256-row items of the tensor-core kernel, checked against the
-  // 128-row items of the CUDA-core kernel (both must cover the same pairs)
+  // 128-row items of the CUDA-core kernel (both must cover the same pairs),
+  // and the all-steps items against the sum over the ring steps
   FwdPlan f, f1;
+  FusedFwdPlan fu;
   BwdPlan b;
   plan_forward(pb, true, &f, kFwdPairQ);
   plan_forward(pb, true, &f1, kFwdTileQ);
+  plan_forward_fused(f, P, &fu);
   plan_backward(pb, &b);
-  auto fwd_step_pairs = [](const FwdPlan& fp_, int s) {
+  auto run_pairs = [](const Seg& sg, int q_len) {
+    int64_t n = 0;
+    for (int t = 0; t < q_len; ++t)
+      n += sg.causal ? std::min<int64_t>(sg.len, std::max<int64_t>(0, t + sg.delta + 1)) : sg.len;
+    return n;
+  };
+  auto fwd_step_pairs = [&](const FwdPlan& fp_, int s) {
     int64_t n = 0;
     for (int x = fp_.step_begin[s]; x < fp_.step_begin[s + 1]; ++x) {
       const FwdItem& it = fp_.items[x];
-      for (int t = 0; t < it.q_len; ++t)
-        for (int g = 0; g < it.nseg; ++g) {
-          const Seg& sg = it.seg[g];
-          n += sg.causal ? std::min<int64_t>(sg.len, std::max<int64_t>(0, t + sg.delta + 1))
-                         : sg.len;
-        }
+      for (int g = 0; g < it.nseg; ++g) n += run_pairs(it.seg[g], it.q_len);
     }
     return n;
   };
+  int64_t fused_pairs = 0, step_sum = 0;
+  for (const FwdItem& it : fu.items) {
+    if (it.flags != (F_FIRST | F_FINAL) || it.run_row0 < 0 ||
+        it.run_row0 + it.nseg > (int64_t)fu.runs.size())
+      return fail(CP_ERR_UNSUPPORTED, "all-steps forward item with a bad run range");
+    for (int g = 0; g < it.nseg; ++g) fused_pairs += run_pairs(fu.runs[it.run_row0 + g], it.q_len);
+  }
   for (int s = 0; s < P; ++s) {
     int64_t fp = fwd_step_pairs(f, s), bp = 0;
     if (fp != fwd_step_pairs(f1, s))
@@ -760,11 +852,14 @@ cp_status_t cp_plan_pairs(const int32_t* cu, int n_seqs, int N, int P, int64_t* 
           bp += vis;
         }
     }
+    step_sum += fp;
     if (fwd_pairs) fwd_pairs[s] = fp;
     if (bwd_pairs) bwd_pairs[s] = bp;
     if (fwd_items) fwd_items[s] = f.step_begin[s + 1] - f.step_begin[s];
     if (bwd_items) bwd_items[s] = b.step_begin[s + 1] - b.step_begin[s];
   }
+  if (fused_pairs != step_sum)
+    return fail(CP_ERR_UNSUPPORTED, "all-steps forward items disagree with the ring steps");
   return CP_OK;
 }
 

@@ -159,6 +159,10 @@ extern "C" cp_status_t cp_attn_fwd_noalloc(const void* q, const void* k, const v
                     make_tmap_thd(&a.tm_v_nat, v, T, H, d, 128, &terr);
     if (!ok) return fail(CP_ERR_CUDA, std::string("tensor map: ") + (terr ? terr : "?"));
     a.H = H; a.Hkv = H; a.d = d; a.pdl = 0;
+    a.runs = nullptr;  // one ring step per launch (fp32 running result in the scratch)
+    a.units = nullptr;
+    a.cta_off = nullptr;
+    a.n_ctas = 0;
     a.scale_log2 = scale * 1.4426950408889634f;
     a.split_p = scale > kPrecisionSplitScale ? 1 : 0;
     a.o_run = orun; a.lse_run = lrun; a.run_rows = PR;

@@ -3,6 +3,8 @@
 
 #include <algorithm>
 #include <cstdio>
+#include <map>
+#include <queue>
 
 namespace cpattn {
 
@@ -185,6 +187,68 @@ void plan_forward(const Problem& pb, bool text_perm, FwdPlan* plan, int tile_q) 
                      [](const FwdItem& a, const FwdItem& b) { return a.n_tiles > b.n_tiles; });
     plan->items.insert(plan->items.end(), step.begin(), step.end());
     plan->step_begin.push_back((int32_t)plan->items.size());
+  }
+}
+
+void plan_forward_fused(const FwdPlan& per_step, int P, FusedFwdPlan* out) {
+  // group the per-step items by query tile, keeping ring-step order
+  struct Acc {
+    FwdItem head;
+    std::vector<Seg> segs;
+  };
+  std::vector<Acc> acc;
+  std::map<std::pair<int32_t, int32_t>, size_t> where;  // (q_src, q_row0) -> acc index
+  for (int s = 0; s < P; ++s) {
+    for (int x = per_step.step_begin[s]; x < per_step.step_begin[s + 1]; ++x) {
+      const FwdItem& it = per_step.items[x];
+      const auto key = std::make_pair(it.q_src, it.q_row0);
+      auto f = where.find(key);
+      if (f == where.end()) {
+        f = where.emplace(key, acc.size()).first;
+        acc.push_back({it, {}});
+      }
+      for (int g = 0; g < it.nseg; ++g) acc[f->second].segs.push_back(it.seg[g]);
+    }
+  }
+  out->items.clear();
+  out->runs.clear();
+  for (Acc& a : acc) {
+    FwdItem it = a.head;
+    it.nseg = (int32_t)a.segs.size();
+    it.run_row0 = (int32_t)out->runs.size();
+    it.flags = F_FIRST | F_FINAL;
+    int64_t tiles = 0;
+    for (const Seg& sg : a.segs) tiles += cdiv(fwd_visible(sg, it.q_len), kFwdTileK);
+    it.n_tiles = (int32_t)tiles;
+    out->runs.insert(out->runs.end(), a.segs.begin(), a.segs.end());
+    out->items.push_back(it);
+  }
+  std::stable_sort(out->items.begin(), out->items.end(),
+                   [](const FwdItem& a, const FwdItem& b) { return a.n_tiles > b.n_tiles; });
+}
+
+void plan_unit_lists(const std::vector<FwdItem>& items, int H, int grid,
+                     std::vector<int32_t>* units, std::vector<int32_t>* cta_off) {
+  constexpr int64_t kUnitCost = 2;  // Q load and epilogue, in KV-tile equivalents
+  const int n = (int)items.size();
+  std::vector<std::vector<int32_t>> lists(grid);
+  using Load = std::pair<int64_t, int>;  // (work so far, CTA): least work first, then lowest CTA
+  std::priority_queue<Load, std::vector<Load>, std::greater<Load>> pq;
+  for (int b = 0; b < grid; ++b) pq.push({0, b});
+  for (int h = 0; h < H; ++h) {
+    for (int x = 0; x < n; ++x) {
+      Load e = pq.top();
+      pq.pop();
+      lists[e.second].push_back(x + n * h);
+      e.first += items[x].n_tiles + kUnitCost;
+      pq.push(e);
+    }
+  }
+  units->clear();
+  cta_off->assign(1, 0);
+  for (const auto& l : lists) {
+    units->insert(units->end(), l.begin(), l.end());
+    cta_off->push_back((int32_t)units->size());
   }
 }
 

@@ -85,6 +85,34 @@ struct BwdPlan {
   std::vector<int32_t> step_begin;
 };
 
+// All ring steps fused per query tile: each item lists, in ring-step order,
+// every key run its query tile meets over steps 0..P-1 (the runs of the
+// per-step items of the same tile, concatenated).  An online softmax over
+// those runs is the log-sum-exp merge of the per-step partials, taken one KV
+// tile at a time.  Items: nseg = number of runs, run_row0 = index of the first
+// run in `runs`, flags = F_FIRST | F_FINAL (no fp32 running result).
+struct FusedFwdPlan {
+  std::vector<FwdItem> items;
+  std::vector<Seg> runs;
+};
+void plan_forward_fused(const FwdPlan& per_step, int P, FusedFwdPlan* out);
+
+// CTAs of a tensor-core forward launch over `units` (item, head) units: one
+// per unit below four units per SM, else one persistent CTA per SM.
+inline long long fwd_grid(long long units, int sms) { return units < 4LL * sms ? units : sms; }
+
+// Unit lists of a persistent forward launch with `grid` CTAs: CTA b walks
+// units[cta_off[b] .. cta_off[b + 1]), each entry item + n_items * head.
+// Units are taken head by head, items heaviest first (the plan's order), and
+// each goes to the CTA with the least work so far (n_tiles plus a fixed cost
+// per unit), as a dynamic scheduler would hand them out.  Every CTA's total
+// then stays within one unit of the mean, and at any moment the CTAs work on
+// one or two heads, whose K / V stay in L2.  (A plain round robin over
+// (item, head) can give a CTA a much heavier share when n_items and grid
+// share a stride.)
+void plan_unit_lists(const std::vector<FwdItem>& items, int H, int grid,
+                     std::vector<int32_t>* units, std::vector<int32_t>* cta_off);
+
 // text_perm = true: text rows address the rank-local (gathered) buffer;
 // false: they address natural order (used by the fp32 dQ pass).  tile_q:
 // query rows per item (kFwdTileQ, or kFwdPairQ for the tensor-core kernel,

@@ -31,6 +31,12 @@ struct TcFwdArgs {
   CUtensorMap tm_q_text, tm_k_text, tm_v_text;  // rank-local (gathered) text rows
   CUtensorMap tm_q_nat, tm_k_nat, tm_v_nat;     // natural order (prefix rows)
   const FwdItem* items;
+  const Seg* runs;            // non-null: all ring steps in one launch; item key runs are
+                              // runs[run_row0 .. run_row0 + nseg) (no running result)
+  const int32_t* units;       // nullable: CTA b walks units[cta_off[b] .. cta_off[b + 1]),
+  const int32_t* cta_off;     // entries item + n_items * head (a permutation of all units)
+  int n_ctas;                 // grid size when units != null (cta_off has n_ctas + 1 entries);
+                              // null units: CTA b walks b, b + grid, ...  (grid chosen here)
   int n_items, H, d;
   int Hkv;                    // KV heads; query head h reads KV head h / (H / Hkv)
   float scale_log2;           // softmax scale * log2(e)

@@ -1,13 +1,19 @@
 // Ring-step attention forward on 5th-generation tensor cores (sm_103a).
 //
-// A unit is one work item of a ring step for one head: up to 256 query rows,
-// taken as two 128-row tiles A and B, against the key runs the step gives
-// them (page "context-parallel-multimodal": §1.1 zigzag chunks, §1 ring order,
-// §4.1 replicated prefix in step 0), with an online softmax over the KV tiles
-// and a fused log-sum-exp merge into the fp32 running result (or the final
-// write in natural order).  Both tiles share every K / V tile.  The kernel is
-// persistent: a CTA walks units gridDim.x apart, with its barrier phases and
-// K / V stages continuing from one unit to the next.
+// A unit is one work item for one head: up to 256 query rows, taken as two
+// 128-row tiles A and B, against a list of key runs (page
+// "context-parallel-multimodal": §1.1 zigzag chunks, §1 ring order, §4.1
+// replicated prefix in step 0), with an online softmax over the KV tiles.
+// Two modes:
+//   all steps in one launch (runs != null): the item's runs are those of
+//     every ring step in ring order, so the online softmax itself is the
+//     log-sum-exp merge of the per-step partials, and the epilogue writes
+//     bf16 out and lse in natural order;
+//   one ring step per launch: the epilogue merges into the fp32 running
+//     result (or makes the final write at the query chunk's last step).
+// Both tiles share every K / V tile.  The kernel is persistent: a CTA walks
+// units gridDim.x apart, with its barrier phases and K / V stages continuing
+// from one unit to the next.
 //
 // The two tiles ping-pong: the tensor core computes one tile's products while
 // the other tile's softmax runs.  Issue order for KV tile j >= 1:
@@ -90,10 +96,33 @@ __device__ __forceinline__ int run_tiles(const Seg& s, int q_len) {
   return (vis + kBN - 1) / kBN;
 }
 
+// Key run s of an item: held in the item (one ring step per launch), or in
+// the run list of the all-steps launch, where the item's runs are the runs of
+// every ring step in ring order.
+__device__ __forceinline__ Seg item_seg(const TcFwdArgs& a, const FwdItem& it, int s) {
+  return a.runs != nullptr ? a.runs[it.run_row0 + s] : it.seg[s];
+}
+
+// The units this CTA walks, in order: without a unit table, u = blockIdx.x,
+// blockIdx.x + gridDim.x, ... < n_units; with one, the table entries
+// cta_off[blockIdx.x] .. cta_off[blockIdx.x + 1] - 1, where the host gave
+// every CTA an equal share of work.  unit_id maps a position to the unit,
+// item + n_items * query head.
+struct UnitRange {
+  int begin, end, step;
+};
+__device__ __forceinline__ UnitRange cta_units(const TcFwdArgs& a) {
+  if (a.units != nullptr) return {a.cta_off[blockIdx.x], a.cta_off[blockIdx.x + 1], 1};
+  return {(int)blockIdx.x, a.n_items * a.H, (int)gridDim.x};
+}
+__device__ __forceinline__ int unit_id(const TcFwdArgs& a, int u) {
+  return a.units != nullptr ? a.units[u] : u;
+}
+
 // KV tiles an item visits over all its key runs.
-__device__ __forceinline__ int item_tiles(const FwdItem& it) {
+__device__ __forceinline__ int item_tiles(const TcFwdArgs& a, const FwdItem& it) {
   int n = 0;
-  for (int s = 0; s < it.nseg; ++s) n += run_tiles(it.seg[s], it.q_len);
+  for (int s = 0; s < it.nseg; ++s) n += run_tiles(item_seg(a, it, s), it.q_len);
   return n;
 }
 
@@ -111,12 +140,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
   using L = Smem<D>;
   Bars* bars = reinterpret_cast<Bars*>(smem + L::kBars);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // Persistent CTA: units u = blockIdx.x, blockIdx.x + gridDim.x, ... are
-  // (item u % n_items, query head u / n_items), walked in that order by every
-  // role.  KV tiles are numbered across units, so stage indices and barrier
+  // Persistent CTA: every role walks the CTA's units (cta_units) in the same
+  // order.  KV tiles are numbered across units, so stage indices and barrier
   // phases simply continue; so are the units that visit at least one tile
   // ("tiled units", whose Q is loaded and whose O lives in TMEM).
-  const int n_units = a.n_items * a.H;
   const int G = a.H / a.Hkv;   // query heads per KV head (grouped-query attention)
   volatile int* abort = &bars->abort;
   const long long lim = a.wait_limit;
@@ -164,11 +191,13 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
       const bool is_k = warp == 0;
       int issued = 0;
       int j = 0;   // KV tile counter across units
-      for (int u = blockIdx.x; u < n_units && !*abort; u += gridDim.x) {
-        const FwdItem& it = a.items[u % a.n_items];
-        const int hk = (u / a.n_items) / G;
+      const UnitRange ur = cta_units(a);
+      for (int u = ur.begin; u < ur.end && !*abort; u += ur.step) {
+        const int uid = unit_id(a, u);
+        const FwdItem& it = a.items[uid % a.n_items];
+        const int hk = (uid / a.n_items) / G;
         for (int s = 0; s < it.nseg && !*abort; ++s) {
-          const Seg sg = it.seg[s];
+          const Seg sg = item_seg(a, it, s);
           const CUtensorMap* m = is_k ? (sg.src == SRC_TEXT ? &a.tm_k_text : &a.tm_k_nat)
                                       : (sg.src == SRC_TEXT ? &a.tm_v_text : &a.tm_v_nat);
           const int nt = run_tiles(sg, it.q_len);
@@ -203,9 +232,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
     // Q of tiled unit n + 1 loads once the products of unit n are done.
     if (lane == 0) {
       int n = 0;   // tiled units so far
-      for (int u = blockIdx.x; u < n_units && !*abort; u += gridDim.x) {
-        const FwdItem& it = a.items[u % a.n_items];
-        if (item_tiles(it) == 0) continue;
+      const UnitRange ur = cta_units(a);
+      for (int u = ur.begin; u < ur.end && !*abort; u += ur.step) {
+        const int uid = unit_id(a, u);
+        const FwdItem& it = a.items[uid % a.n_items];
+        if (item_tiles(a, it) == 0) continue;
         if (n > 0 && !mbar_wait(&bars->q_empty, (n - 1) & 1, lim, abort)) {
           record_timeout(a.status, abort, 6);
           break;
@@ -215,7 +246,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
         for (int x = 0; x < 2; ++x)
           for (int b = 0; b < D / 64; ++b)
             tma_load_3d(qm, &bars->q_full, smem + L::kQ + x * L::kTile + b * L::kBox, b * 64,
-                        u / a.n_items, it.q_row0 + x * kBM);
+                        uid / a.n_items, it.q_row0 + x * kBM);
         ++n;
       }
       int zero = 0;
@@ -264,8 +295,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
       bool ok = true;
       int j = 0;   // KV tile counter across units
       int n = 0;   // tiled units so far
-      for (int u = blockIdx.x; ok && u < n_units; u += gridDim.x) {
-        const int n_tiles = item_tiles(a.items[u % a.n_items]);
+      const UnitRange ur = cta_units(a);
+      for (int u = ur.begin; ok && u < ur.end; u += ur.step) {
+        const int n_tiles = item_tiles(a, a.items[unit_id(a, u) % a.n_items]);
         if (n_tiles == 0) continue;
         if (!mbar_wait(&bars->q_full, n & 1, lim, abort)) { ok = false; break; }
         const int j0 = j;
@@ -312,17 +344,19 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
     const float sl2 = a.scale_log2;
     bool ok = true;
     int j = 0;   // KV tile counter across units
-    for (int u = blockIdx.x; ok && u < n_units; u += gridDim.x) {
-    const FwdItem& it = a.items[u % a.n_items];
-    const int h = u / a.n_items;
+    const UnitRange ur = cta_units(a);
+    for (int u = ur.begin; ok && u < ur.end; u += ur.step) {
+    const int uid = unit_id(a, u);
+    const FwdItem& it = a.items[uid % a.n_items];
+    const int h = uid / a.n_items;
     const int q_len = it.q_len;   // rows of the item (tile A: first 128, tile B: the rest)
     const int nseg = it.nseg;
-    const int n_tiles = item_tiles(it);
+    const int n_tiles = item_tiles(a, it);
     const int j0 = j;
     float m = -INFINITY;   // running max of scaled scores (log2 units), may lag
     float l = 0.f;
     for (int s = 0; ok && s < nseg; ++s) {
-      const Seg sg = it.seg[s];
+      const Seg sg = item_seg(a, it, s);
       const int nt = run_tiles(sg, q_len);
       // key u of the run is visible to this row iff u < lim_u
       const int lim_u = sg.causal ? min(sg.len, tq + sg.delta + 1) : sg.len;
@@ -456,7 +490,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
       const float inv = l > 0.f ? 1.f / l : 0.f;
       const int flags = it.flags;
       const long long rrow =
-          it.run_row0 >= 0 ? (long long)h * a.run_rows + it.run_row0 + tq : 0;
+          it.run_row0 >= 0 && a.runs == nullptr ? (long long)h * a.run_rows + it.run_row0 + tq : 0;
       float ca = 0.f, cb = 1.f;
       if (valid && !(flags & F_FIRST)) {
         const float lr = a.lse_run[rrow];
@@ -563,7 +597,8 @@ cudaError_t launch_d(const TcFwdArgs& a, cudaStream_t st) {
   if (units > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   // with few units per SM (under 4), one CTA per unit: a static share of
   // units per CTA would leave some CTAs a whole unit behind the others
-  const long long blocks = units < 4LL * sms ? units : sms;
+  const long long blocks = a.units != nullptr ? a.n_ctas : fwd_grid(units, sms);
+  if (blocks < 1) return cudaErrorInvalidConfiguration;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)blocks);
   cfg.blockDim = dim3(kThreads);
