@@ -301,6 +301,27 @@ cp_status_t cp_plan_pairs(const int32_t* cu_seqlens_h, int n_seqs, int prefix_le
                           int64_t* bwd_items);
 
 /*
+ * cp_plan_unit_lists -- host-only view of how the default tensor-core forward
+ * (all ring steps in one persistent launch) hands its units to `grid` CTAs.
+ * An item is one 256-query tile with the key runs of every ring step (CP-VLM
+ * page §1 ring order, §1.1 zigzag chunks, §4.1 prefix); a unit is an
+ * (item, query head) pair, numbered item + n_items * head.
+ *
+ *   n_items   out: number of items (may be NULL)
+ *   tiles     [n_items] or NULL: KV tiles each item visits (its cost)
+ *   units     [n_items * H] or NULL: the units, CTA by CTA
+ *   cta_off   [grid + 1] or NULL: CTA b walks units[cta_off[b] .. cta_off[b+1])
+ *
+ * Call once with NULL arrays to learn n_items.  The library applies these
+ * lists when a launch has at least four units per SM, with grid = the SM
+ * count; below that it launches one CTA per unit.  Needs no GPU.
+ * Errors: CP_ERR_INVALID_ARG (H < 1, grid < 1, bad counts), CP_ERR_SHAPE.
+ */
+cp_status_t cp_plan_unit_lists(const int32_t* cu_seqlens_h, int n_seqs, int prefix_len, int P,
+                               int H, int grid, int64_t* n_items, int32_t* tiles,
+                               int32_t* units, int32_t* cta_off);
+
+/*
  * cp_profile_begin / cp_profile_end -- instrumentation: between the two calls
  * the library records a pair of CUDA events on the launching stream around
  * every kernel it launches (any thread).  The tensor-core forward is one

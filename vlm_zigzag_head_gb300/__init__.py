@@ -10,7 +10,8 @@ Functions keep the names of the C entry points:
 * :func:`cp_zigzag_index`, :func:`cp_zigzag_gather`, :func:`cp_zigzag_scatter`
 * :func:`cp_attn_fwd`, :func:`cp_lse_merge`, :func:`cp_attn_bwd`
 * :func:`cp_attn_fwd_gqa`, :func:`cp_attn_bwd_gqa` -- grouped KV heads
-* :func:`cp_workspace_status`, :func:`cp_set_wait_limit`, :func:`cp_plan_pairs`
+* :func:`cp_workspace_status`, :func:`cp_set_wait_limit`, :func:`cp_plan_pairs`,
+  :func:`cp_plan_unit_lists`
 * :func:`attention_host` -- end-to-end call on host (pinned) tensors.
 """
 from __future__ import annotations
@@ -26,7 +27,7 @@ from ._binding import CP_BF16, CP_F32, CpError  # noqa: F401
 __all__ = ["cp_zigzag_index", "cp_zigzag_gather", "cp_zigzag_scatter", "cp_attn_fwd",
            "cp_attn_fwd_noalloc", "cp_attn_fwd_gqa", "cp_attn_bwd_gqa",
            "cp_lse_merge", "cp_attn_bwd", "cp_workspace_status", "cp_set_wait_limit",
-           "cp_plan_pairs", "cp_profile_begin", "cp_profile_end", "Workspace",
+           "cp_plan_pairs", "cp_plan_unit_lists", "cp_profile_begin", "cp_profile_end", "Workspace",
            "attention_host", "CpError"]
 
 
@@ -325,6 +326,24 @@ def cp_plan_pairs(cu_seqlens, prefix_len: int, P: int):
     cu = _b.cu_array(cu_seqlens)
     _b.check(_b.lib().cp_plan_pairs(cu, len(cu_seqlens) - 1, prefix_len, P, *arrs))
     return tuple([int(x) for x in a] for a in arrs)
+
+
+def cp_plan_unit_lists(cu_seqlens, prefix_len: int, P: int, H: int, grid: int):
+    """Host-only: the all-steps forward's items and their cost in KV tiles,
+    and the unit lists of a persistent launch over ``grid`` CTAs.  Returns
+    ``(tiles, units, cta_off)`` as int32 numpy arrays; unit = item + n_items * head."""
+    import numpy as np
+    cu = _b.cu_array(cu_seqlens)
+    n = ctypes.c_int64(0)
+    args = (cu, len(cu_seqlens) - 1, prefix_len, P, H, grid)
+    _b.check(_b.lib().cp_plan_unit_lists(*args, ctypes.byref(n), None, None, None))
+    tiles = np.zeros(n.value, np.int32)
+    units = np.zeros(n.value * H, np.int32)
+    off = np.zeros(grid + 1, np.int32)
+    p32 = ctypes.POINTER(ctypes.c_int32)
+    _b.check(_b.lib().cp_plan_unit_lists(*args, ctypes.byref(n), tiles.ctypes.data_as(p32),
+                                         units.ctypes.data_as(p32), off.ctypes.data_as(p32)))
+    return tiles, units, off
 
 
 def attention_host(q, k, v, dout, cu_seqlens, P: int, prefix_len: int, softmax_scale: float,

@@ -72,6 +72,9 @@ SIGNATURES = {
     "cp_workspace_status": (ctypes.c_int, [c_vp, c_vp]),
     "cp_plan_pairs": (ctypes.c_int, [c_i32p, ctypes.c_int, ctypes.c_int, ctypes.c_int, c_i64p,
                                      c_i64p, c_i64p, c_i64p]),
+    "cp_plan_unit_lists": (ctypes.c_int, [c_i32p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                          ctypes.c_int, ctypes.c_int, c_i64p, c_i32p, c_i32p,
+                                          c_i32p]),
     "cp_set_wait_limit": (None, [ctypes.c_longlong]),
     "cp_profile_begin": (None, []),
     "cp_profile_end": (ctypes.c_int, [ctypes.POINTER(ctypes.c_double), c_i64p]),

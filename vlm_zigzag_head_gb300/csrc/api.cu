@@ -863,4 +863,30 @@ cp_status_t cp_plan_pairs(const int32_t* cu, int n_seqs, int N, int P, int64_t* 
   return CP_OK;
 }
 
+cp_status_t cp_plan_unit_lists(const int32_t* cu, int n_seqs, int N, int P, int H, int grid,
+                               int64_t* n_items, int32_t* tiles, int32_t* units,
+                               int32_t* cta_off) {
+  if (!cu || n_seqs < 1 || P < 1 || N < 0 || H < 1 || grid < 1)
+    return fail(CP_ERR_INVALID_ARG, "bad arguments");
+  Problem pb;
+  std::string err = make_problem(cu, n_seqs, N, P, -1, &pb);
+  if (!err.empty()) return fail(CP_ERR_SHAPE, err);
+  FwdPlan f;
+  FusedFwdPlan fu;
+  plan_forward(pb, true, &f, kFwdPairQ);
+  plan_forward_fused(f, P, &fu);
+  if ((int64_t)fu.items.size() * H > 0x7fffffffLL)
+    return fail(CP_ERR_INVALID_ARG, "too many units");
+  if (n_items) *n_items = (int64_t)fu.items.size();
+  if (tiles)
+    for (size_t x = 0; x < fu.items.size(); ++x) tiles[x] = fu.items[x].n_tiles;
+  if (units || cta_off) {
+    std::vector<int32_t> u, off;
+    plan_unit_lists(fu.items, H, grid, &u, &off);
+    if (units) std::copy(u.begin(), u.end(), units);
+    if (cta_off) std::copy(off.begin(), off.end(), cta_off);
+  }
+  return CP_OK;
+}
+
 }  // extern "C"
