@@ -12,8 +12,9 @@
 //   one ring step per launch: the epilogue merges into the fp32 running
 //     result (or makes the final write at the query chunk's last step).
 // Both tiles share every K / V tile.  The kernel is persistent: a CTA walks
-// units gridDim.x apart, with its barrier phases and K / V stages continuing
-// from one unit to the next.
+// its own list of units (dealt by the host so that every CTA gets an equal
+// share of KV tiles), or units gridDim.x apart without a list, with its
+// barrier phases and K / V stages continuing from one unit to the next.
 //
 // The two tiles ping-pong: the tensor core computes one tile's products while
 // the other tile's softmax runs.  Issue order for KV tile j >= 1:
