@@ -41,6 +41,9 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # kernel changes until it is captured again.
 MEASURED_TRAFFIC = {"long": 14.48e9}
 EX2_PER_CLK_SM = 32.0   # MUFU exp2 results per clock per SM (31.8 measured by a throughput loop)
+# every bf16 forward + backward workload of the method; the default line's
+# `value` is the 128K one, the others are reported under `workloads`
+OTHER_WORKLOADS = ("long", "vlm_prefix", "packed_vlm", "text_llm")
 
 
 def causal_pairs(w) -> int:
@@ -142,6 +145,58 @@ def oracle_sample(w, n_queries: int = 8192):
     desc = ("first %d tokens of sample 0, head 0 of the '%s' workload (causal: a complete "
             "slice of its work), oracle forward + backward in fp64" % (n, w.name))
     return dt, flops, desc
+
+
+def time_workload(cp, w, dev, steps: int, warmup: int) -> dict:
+    """Forward, backward and forward+backward rates of one bf16 workload, inputs
+    resident on the device, CUDA events on the launching stream."""
+    x = W.make_inputs(w)
+    stream = torch.cuda.current_stream(dev)
+    qd, kd, vd, dod = (t.to(dev) for t in (x.q, x.k, x.v, x.dout))
+    cu, P, N, scale = x.cu_seqlens, w.P, w.prefix_len, x.scale
+    T, H, d = qd.shape
+    Hkv = kd.shape[1]
+    out, out_lo = torch.empty_like(qd), torch.empty_like(qd)
+    lse = torch.empty((H, T), dtype=torch.float32, device=dev)
+    grads = (torch.empty((T, H, d), dtype=torch.float32, device=dev),
+             torch.empty((T, Hkv, d), dtype=torch.float32, device=dev),
+             torch.empty((T, Hkv, d), dtype=torch.float32, device=dev))
+    ws_f, ws_b = cp.Workspace(dev), cp.Workspace(dev)
+
+    def fwd():
+        cp.cp_attn_fwd(qd, kd, vd, cu, P, N, scale, out=out, lse=lse, workspace=ws_f,
+                       residual=True, out_lo=out_lo)
+
+    def bwd():
+        cp.cp_attn_bwd(qd, kd, vd, out, lse, dod, cu, P, N, scale, workspace=ws_b, grads=grads,
+                       out_lo=out_lo)
+
+    def timed(fn, n):
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(dev)
+        a0.record(stream)
+        for _ in range(n):
+            fn()
+        a1.record(stream)
+        torch.cuda.synchronize(dev)
+        return a0.elapsed_time(a1) / n
+
+    for _ in range(warmup):
+        fwd()
+        bwd()
+    torch.cuda.synchronize(dev)
+    if cp.cp_workspace_status(ws_f) or cp.cp_workspace_status(ws_b):
+        raise RuntimeError("a device wait timed out on workload %s" % w.name)
+    f = fwd_flops(w)
+    fwd_ms = timed(fwd, steps)
+    bwd_ms = timed(bwd, steps)
+    step_ms = timed(lambda: (fwd(), bwd()), steps)
+    if cp.cp_workspace_status(ws_f) or cp.cp_workspace_status(ws_b):
+        raise RuntimeError("a device wait timed out on workload %s" % w.name)
+    return {"fwd_ms": fwd_ms, "bwd_ms": bwd_ms, "ms_per_step": step_ms,
+            "fwd_tflops": f / fwd_ms / 1e9, "bwd_tflops": 2.5 * f / bwd_ms / 1e9,
+            "tflops": 3.5 * f / step_ms / 1e9, "flops_per_step": 3.5 * f,
+            "softmax_scale": x.scale, "steps": steps, "warmup": warmup}
 
 
 def max_over_ranks(ms: float, dist, device) -> float:
@@ -339,6 +394,28 @@ def run_cuda(args, w, rank, world, dist):
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "ms_per_step": e2e_s * 1e3}
 
+    # ---- the other bf16 workloads of the method (parity configs, measured the
+    # same way at fewer steps): fwd, bwd and fwd+bwd rates, and the oracle's
+    # wall time on a bounded slice of each
+    workloads = {w.name: {"fwd_tflops": world * f_flops / (fwd_ms / 1e3) / 1e12,
+                          "bwd_tflops": world * 2.5 * f_flops / (bwd_ms / 1e3) / 1e12,
+                          "tflops": value / world, "ms_per_step": ms_step,
+                          "pct_of_bf16_peak": 100.0 * (value / world) / peak_sus}}
+    if not args.no_workloads:
+        for name in OTHER_WORKLOADS:
+            if name == w.name:
+                continue
+            wl = W.get(name, H_kv=args.kv_heads) if args.kv_heads else W.get(name)
+            r = time_workload(cp, wl, dev, max(3, min(args.steps, 10)), max(3, args.warmup))
+            r["pct_of_bf16_peak"] = 100.0 * r["tflops"] / peak_sus
+            workloads[name] = r
+    if not args.no_cpu_baseline and world == 1 and rank == 0:
+        for name in workloads:
+            wl = W.get(name)
+            dt, fl, desc = oracle_sample(wl, args.workload_oracle_queries)
+            workloads[name]["oracle"] = {"seconds": dt, "tflops": fl / dt / 1e12,
+                                         "cores": os.cpu_count(), "sample": desc}
+
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
@@ -352,6 +429,7 @@ def run_cuda(args, w, rank, world, dist):
             "flops_per_step": total,
             "roofline": roof,
             "kernels": kernels,
+            "workloads": workloads,
             "gpu_launches": gpu_launches,
             "clocks": clk.summary(),
             "e2e": e2e,
@@ -377,6 +455,10 @@ def main():
     ap.add_argument("--oracle-queries", type=int, default=32768)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="skip the other bf16 workloads (reported under 'workloads')")
+    ap.add_argument("--workload-oracle-queries", type=int, default=8192,
+                    help="queries of the oracle slice timed per workload")
     ap.add_argument("--traffic", type=float, default=None,
                     help="DRAM bytes per launch of the dominant kernel from an ncu capture")
     args = ap.parse_args()

@@ -92,10 +92,11 @@ int cp_version(void);
  *     natural order (prefix tokens are not counted).
  *
  * on_device = 0: fwd_idx / inv_idx are host arrays, filled before return
- * (stream unused).  on_device = 1: they are device arrays; the tables are
- * built on the host and copied asynchronously on `stream`.  (Inside
- * cp_attn_fwd the same table is produced by a device kernel.)  Either pointer
- * may be NULL to skip that table.
+ * (stream unused).  on_device = 1: they are device arrays (16-byte aligned),
+ * written asynchronously on `stream` by the device kernel that cp_attn_fwd
+ * runs for its own gather table; the per-sample table travels in the kernel
+ * parameters (one launch per 192 samples), so nothing is allocated or copied.
+ * Either pointer may be NULL to skip that table.
  * Errors: CP_ERR_INVALID_ARG (n_seqs < 1, P < 1, prefix_len < 0, null
  * cu_seqlens), CP_ERR_SHAPE (a text length < 0 or not divisible by 2P).
  */
@@ -168,11 +169,13 @@ cp_status_t cp_attn_fwd(const void* q, const void* k, const void* v, cp_dtype_t 
  * cudaFree or other allocating routine; work lists are copied from ordinary
  * host memory.
  *
- *  - Capacity: the scratch holds the work list, the zigzag table, the
- *    rank-local q/k/v (3 x rows x H x d elements) and the fp32 running result
- *    (rows x H x (d + 1) x 4 bytes), rows = text tokens.  For bf16 and
- *    d = 128 that is about 1.3 KB per (text token, head), so about 50 000
- *    (token, head) pairs, e.g. 4096 tokens with 12 heads.  Larger problems
+ *  - Capacity: for CP_BF16 the scratch holds the work lists of the all-steps
+ *    forward (every ring step of a query tile in one launch, merged on chip),
+ *    the zigzag table and the rank-local q/k/v: 3 x rows x H x d x 2 bytes,
+ *    rows = text tokens.  At d = 128 that is 768 bytes per (text token, head),
+ *    so about 85 000 (token, head) pairs, e.g. 8192 tokens with 10 heads.
+ *    CP_F32 merges its ring steps through an fp32 running result held in the
+ *    scratch as well (about 1.6 KB per pair at d = 128).  Larger problems
  *    return CP_ERR_WORKSPACE with the number of bytes they would need.
  *  - The first call on a device looks up the scratch's device address
  *    (cudaGetSymbolAddress, with that device current); make that first call
@@ -181,8 +184,10 @@ cp_status_t cp_attn_fwd(const void* q, const void* k, const void* v, cp_dtype_t 
  *    status word is cleared at the start of each call and everything else is
  *    written before it is read.  Calls that overlap on the GPU (other streams,
  *    other host threads) race on the scratch: order them on one stream.
- *  - Results equal cp_attn_fwd's (same kernels).  cp_workspace_status does not
- *    apply (there is no caller workspace).
+ *  - Results equal cp_attn_fwd's (same kernels and schedule).  The status
+ *    word is the first thing in the scratch and is cleared at the start of
+ *    each call: cp_workspace_status(NULL, stream) reads it (CP_ERR_TIMEOUT
+ *    when a bounded device wait of the last call gave up).
  * Errors: as cp_attn_fwd, plus CP_ERR_WORKSPACE when the problem exceeds the
  * fixed scratch.
  */
@@ -280,7 +285,9 @@ cp_status_t cp_attn_bwd_gqa(const void* q, const void* k, const void* v, const v
 /*
  * cp_workspace_status -- synchronise `stream` and report whether a kernel of
  * the last cp_attn_fwd / cp_attn_bwd call that used `workspace` gave up on a
- * bounded device wait (CP_ERR_TIMEOUT) or CP_OK.
+ * bounded device wait (CP_ERR_TIMEOUT) or CP_OK.  workspace = NULL: the same
+ * for the last cp_attn_fwd_noalloc call on the current device (its fixed
+ * scratch holds the status word).
  */
 cp_status_t cp_workspace_status(const void* workspace, void* stream);
 

@@ -146,3 +146,20 @@ def test_grouped_kv_arguments(cplib):
     st = L.cp_attn_bwd_gqa(fake, fake, fake, fake, None, fake, fake, 1, 16, 4, 3, 128, cu, 1, 2,
                            0, 1.0, fake, fake, fake, None, fake, 1 << 20, None)
     assert st == 2
+
+
+@pytest.mark.skipif(os.environ.get("CPATTN_FWD_PER_STEP") == "1",
+                    reason="the per-step schedule merges through the running result")
+def test_forward_workspace_is_sized_by_schedule(cplib):
+    """The default bf16 forward merges its ring steps on chip, so its
+    workspace holds the rank-local q/k/v but no fp32 running result; the fp32
+    path merges through one ([rows][H][d] fp32 plus lse) and reserves it."""
+    L = cplib
+    rows, H, d = 4096, 8, 128
+    cu = B.cu_array([0, rows])
+    ws_bf16 = L.cp_attn_fwd_workspace_size(1, rows, H, d, cu, 1, 2, 0)
+    ws_f32 = L.cp_attn_fwd_workspace_size(0, rows, H, d, cu, 1, 2, 0)
+    qkv_bf16, qkv_f32 = 3 * rows * H * d * 2, 3 * rows * H * d * 4
+    running = rows * H * (d + 1) * 4
+    assert qkv_bf16 <= ws_bf16 < qkv_bf16 + running // 4
+    assert ws_f32 >= qkv_f32 + running

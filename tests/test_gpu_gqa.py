@@ -157,7 +157,9 @@ def test_gqa_large_grid_without_group_split(cp):
 def test_gqa_long_workload_sampled(cp):
     """128K tokens, P = 8, 32 query heads over 8 KV heads, at full size.
     out / lse / dQ on 2048 seeded rows of query heads 0 and 5, and dK / dV of
-    KV head 0 on the last 256 keys (the sum of its 4 query heads' terms), from
+    KV head 0 (the sum of its 4 query heads' terms) on the last 64 keys of
+    zigzag chunk 14, which rank 0's chunk-15 queries meet at ring step 7, and
+    on the last 256 keys, from
     the oracle's row- and key-sampled forms.  At every key, per KV head,
     sum_j dV_j equals the sum of dO over the group's query heads, and
     sum_j dK_j = 0."""
@@ -176,7 +178,8 @@ def test_gqa_long_workload_sampled(cp):
         assert_close("out rows h%d" % h, got["out"][r_t][:, h:h + 1], o_ref, "bf16")
         assert_close("lse rows h%d" % h, got["lse"][h:h + 1][:, r_t], l_ref, "bf16")
         assert_close("dq rows h%d" % h, got["dq"][r_t][:, h:h + 1], dq_ref, "bf16")
-    keys = np.arange(x.T - 256, x.T)
+    c = x.T // (2 * w.P)
+    keys = np.concatenate([np.arange(15 * c - 64, 15 * c), np.arange(x.T - 256, x.T)])
     dk_ref = dv_ref = 0
     for h in range(G):                      # the query heads of KV head 0
         a, b = oracle.causal_attention_bwd_keys(x.q[:, h:h + 1], x.k[:, 0:1], x.v[:, 0:1],

@@ -3,8 +3,6 @@
 Small cases are compared element by element over the whole output; the large
 workloads on seeded heads / rows / keys the oracle computes one by one, and
 at full length through identities that hold at any size."""
-import os
-
 import numpy as np
 import pytest
 import torch
@@ -79,7 +77,20 @@ def _check_full(cp, cu, P, N, H, d, dtype, seed, scale, bwd=True, heads=None, q_
 # ---------------------------------------------------------------------------
 # zigzag index / permutation kernels: bit-exact
 # ---------------------------------------------------------------------------
-@pytest.mark.parametrize("P,N,texts", [(2, 0, [256]), (4, 576, [1024, 0, 3072]), (8, 3, [32, 16])])
+def _many_texts(P, n, seed):
+    g = torch.Generator().manual_seed(seed)
+    return [int(x) * 2 * P for x in torch.randint(0, 9, (n,), generator=g)]
+
+
+# The device tables come from the same kernel cp_attn_fwd launches for its
+# gather (sample tables travel in its parameters, 192 samples per launch: the
+# 401-sample case spans three launches).
+INDEX_CASES = [(1, 0, [256]), (2, 0, [256]), (3, 37, [384, 0, 1152]),
+               (4, 576, [1024, 0, 3072]), (8, 3, [32, 16]), (8, 64, [1024, 2048, 0, 512]),
+               (2, 5, _many_texts(2, 401, 3)), (3, 0, [0, 0, 6] + _many_texts(3, 200, 4))]
+
+
+@pytest.mark.parametrize("P,N,texts", INDEX_CASES)
 def test_index_and_permutation_bit_exact(cp, P, N, texts):
     cu = _cu(N, texts)
     fwd, inv = cp.cp_zigzag_index(cu, N, P, device=DEV)
@@ -211,11 +222,20 @@ def test_per_rank_prefix_gradients(cp):
     assert_close("prefix dv", got["dv"][pre], dv[pre], "bf16")
 
 
-@pytest.mark.skipif(os.environ.get("CPATTN_BF16_SIMT") == "1", reason="CUDA-core path too slow")
+def _long_check_keys(T, c):
+    """Keys whose gradients come from several ring steps: the last 64 keys of
+    zigzag chunks 12, 13 and 14 (ranks 3, 2, 1 at P = 8) are met by their own
+    rank at step 0 and by the ranks holding later chunks at steps 5..7; the
+    last 256 keys (chunk 15) only by rank 0 at step 0."""
+    ends = [13 * c, 14 * c, 15 * c]
+    return np.concatenate([np.arange(e - 64, e) for e in ends] + [np.arange(T - 256, T)])
+
+
 def test_bf16_long_workload_sampled(cp):
     """128K tokens, P=8: out/lse/dQ on 4096 seeded query rows (2 heads), dK/dV
-    on the last 256 keys (2 heads), and at every key the identities
-    sum_j dV_j = sum_i dO_i and sum_j dK_j = 0 per head."""
+    at 448 keys (2 heads) that include keys met at ring steps 5..7, and at
+    every key the identities sum_j dV_j = sum_i dO_i and sum_j dK_j = 0 per
+    head."""
     w = W.get("long")
     x = W.make_inputs(w)
     got = _run(cp, x.q, x.k, x.v, x.dout, x.cu_seqlens, w.P, w.prefix_len, x.scale)
@@ -227,7 +247,7 @@ def test_bf16_long_workload_sampled(cp):
     assert_close("out rows", got["out"][r_t][:, heads], o_ref, "bf16")
     assert_close("lse rows", got["lse"][heads][:, r_t], l_ref, "bf16")
     assert_close("dq rows", got["dq"][r_t][:, heads], dq_ref, "bf16")
-    keys = np.arange(x.T - 256, x.T)
+    keys = _long_check_keys(x.T, W.text_lengths(w)[0] // (2 * w.P))
     dk_ref, dv_ref = oracle.causal_attention_bwd_keys(x.q, x.k, x.v, x.dout, x.cu_seqlens,
                                                       x.scale, keys, heads=heads)
     k_t = torch.as_tensor(keys)

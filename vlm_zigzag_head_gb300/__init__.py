@@ -196,7 +196,8 @@ def cp_attn_fwd_noalloc(q, k, v, cu_seqlens, P: int, prefix_len: int, softmax_sc
     :func:`cp_attn_fwd`, but the library's fixed 64 MiB scratch replaces the
     workspace.  Outputs may be passed in (``out``, ``lse``, ``out_lo``) so the
     call allocates nothing; the first call on a device must precede any
-    stream capture; calls that overlap on the GPU race on the shared scratch."""
+    stream capture; calls that overlap on the GPU race on the shared scratch.
+    ``cp_workspace_status()`` (no workspace) reports a device wait that gave up."""
     _need_cuda(q, k, v, out, lse, out_lo)
     T, H, d = q.shape
     dt = _dt(q)
@@ -288,8 +289,15 @@ def _attn_bwd(q, k, v, out, lse, dout, cu_seqlens, P, prefix_len, softmax_scale,
     return dq, dk, dv
 
 
-def cp_workspace_status(workspace: Workspace) -> int:
-    """Synchronise the current stream; 0 or the CP_ERR_TIMEOUT status."""
+def cp_workspace_status(workspace: Optional[Workspace] = None, device=None) -> int:
+    """Synchronise the current stream; 0 or the CP_ERR_TIMEOUT status.  With
+    no workspace it reads the status of :func:`cp_attn_fwd_noalloc`'s fixed
+    scratch on ``device`` (default: the current device)."""
+    if workspace is None:
+        dev = torch.device(device) if device is not None else torch.device(
+            "cuda", torch.cuda.current_device())
+        with torch.cuda.device(dev):
+            return _b.lib().cp_workspace_status(None, _stream(dev))
     st = _b.lib().cp_workspace_status(ctypes.c_void_p(workspace.ptr()),
                                       _stream(workspace.buf.device))
     return st
@@ -346,24 +354,71 @@ def cp_plan_unit_lists(cu_seqlens, prefix_len: int, P: int, H: int, grid: int):
     return tiles, units, off
 
 
+_side = {}
+
+
+def _side_streams(dev):
+    """Two copy streams per device: host-to-device and device-to-host."""
+    key = str(dev)
+    if key not in _side:
+        _side[key] = (torch.cuda.Stream(dev), torch.cuda.Stream(dev))
+    return _side[key]
+
+
 def attention_host(q, k, v, dout, cu_seqlens, P: int, prefix_len: int, softmax_scale: float,
                    device="cuda", host_out=None):
     """End-to-end call on host tensors (pinned for asynchronous copies): copy the
     inputs to ``device``, run forward (and backward when ``dout`` is given),
-    copy results back.  Returns host tensors ``(out, lse[, dq, dk, dv])``."""
+    copy results back.  Returns host tensors ``(out, lse[, dq, dk, dv])``.
+
+    The copies overlap the kernels: q, k, v go up first on a copy stream and
+    the forward starts once they have landed; dO goes up on the same stream
+    while the forward runs; out and lse come down on a second copy stream
+    while the backward runs; the gradients come down after it.  Events order
+    every copy against the kernels that write or read its tensor."""
     dev = torch.device(device)
-    qd, kd, vd = (x.to(dev, non_blocking=True) for x in (q, k, v))
+    comp = torch.cuda.current_stream(dev)
+    up, down = _side_streams(dev)
+    up.wait_stream(comp)            # device memory freed by earlier work on comp
+    with torch.cuda.stream(up):
+        qd, kd, vd = (x.to(dev, non_blocking=True) for x in (q, k, v))
+        ev_qkv = torch.cuda.Event()
+        ev_qkv.record(up)
+        dod = dout.to(dev, non_blocking=True) if dout is not None else None
+        ev_do = torch.cuda.Event()
+        ev_do.record(up)
+    comp.wait_event(ev_qkv)
+    for t in (qd, kd, vd):
+        t.record_stream(comp)
     keep = dout is not None and qd.dtype == torch.bfloat16
     r = cp_attn_fwd(qd, kd, vd, cu_seqlens, P, prefix_len, softmax_scale, residual=keep)
     out, lse = r[0], r[1]
-    res = [out, lse]
-    if dout is not None:
-        dod = dout.to(dev, non_blocking=True)
-        res += list(cp_attn_bwd(qd, kd, vd, out, lse, dod, cu_seqlens, P, prefix_len,
-                                softmax_scale, out_lo=r[2] if keep else None))
+    n_res = 5 if dout is not None else 2
     if host_out is None:
-        host_out = [torch.empty(r.shape, dtype=r.dtype, pin_memory=True) for r in res]
-    for h, r in zip(host_out, res):
-        h.copy_(r, non_blocking=True)
-    torch.cuda.current_stream(dev).synchronize()
-    return tuple(host_out)
+        shapes = [(out.shape, out.dtype), (lse.shape, lse.dtype)]
+        if dout is not None:
+            shapes += [(qd.shape, torch.float32), (kd.shape, torch.float32),
+                       (kd.shape, torch.float32)]
+        host_out = [torch.empty(sh, dtype=dt, pin_memory=True) for sh, dt in shapes]
+    ev_fwd = torch.cuda.Event()
+    ev_fwd.record(comp)
+    down.wait_event(ev_fwd)
+    with torch.cuda.stream(down):
+        for h, t in zip(host_out[:2], (out, lse)):
+            h.copy_(t, non_blocking=True)
+            t.record_stream(down)
+    if dout is not None:
+        comp.wait_event(ev_do)
+        dod.record_stream(comp)
+        grads = cp_attn_bwd(qd, kd, vd, out, lse, dod, cu_seqlens, P, prefix_len, softmax_scale,
+                            out_lo=r[2] if keep else None)
+        ev_bwd = torch.cuda.Event()
+        ev_bwd.record(comp)
+        down.wait_event(ev_bwd)
+        with torch.cuda.stream(down):
+            for h, t in zip(host_out[2:n_res], grads):
+                h.copy_(t, non_blocking=True)
+                t.record_stream(down)
+    down.synchronize()
+    comp.synchronize()
+    return tuple(host_out[:n_res])

@@ -197,11 +197,15 @@ cp_status_t get_plans(const int32_t* cu, int n_seqs, int N, int P, int T, int H,
 // workspace layouts
 // ---------------------------------------------------------------------------
 struct FwdWs {
-  size_t status = 0, items = 0, runs = 0, units = 0, samples = 0, idx = 0, qkv[3] = {0, 0, 0},
+  size_t status = 0, items = 0, runs = 0, units = 0, idx = 0, qkv[3] = {0, 0, 0},
          o_run = 0, lse_run = 0, total = 0;
 };
 
-FwdWs fwd_layout(const PlanSet& ps, int H, int Hkv, int d, size_t elem) {
+// `running`: reserve the fp32 running result (o_run, lse_run) that the
+// per-step schedules merge into (fp32 inputs, or bf16 under
+// CPATTN_FWD_PER_STEP=1).  The default all-steps tensor-core forward keeps its
+// merge on chip and needs none.
+FwdWs fwd_layout(const PlanSet& ps, int H, int Hkv, int d, size_t elem, bool running) {
   FwdWs w;
   size_t o = 0;
   w.status = o; o += kStatusBytes;
@@ -210,15 +214,16 @@ FwdWs fwd_layout(const PlanSet& ps, int H, int Hkv, int d, size_t elem) {
   w.runs = o; o = align_up(o + ps.fused.runs.size() * sizeof(Seg), 256);
   // unit lists: units, then cta_off (at most units + 1 entries)
   w.units = o; o = align_up(o + (2 * ps.fused.items.size() * H + 1) * sizeof(int32_t), 256);
-  w.samples = o; o = align_up(o + ps.samples.size() * sizeof(int32_t), 256);
   w.idx = o; o = align_up(o + (size_t)ps.pb.text_rows * sizeof(int32_t), 256);
   // rank-local q [rows][H][d]; k, v [rows][Hkv][d]
   for (int i = 0; i < 3; ++i) {
     w.qkv[i] = o;
     o = align_up(o + (size_t)ps.pb.text_rows * (i == 0 ? H : Hkv) * d * elem, 256);
   }
-  w.o_run = o; o = align_up(o + (size_t)ps.pb.text_rows * H * d * sizeof(float), 256);
-  w.lse_run = o; o = align_up(o + (size_t)ps.pb.text_rows * H * sizeof(float), 256);
+  w.o_run = o;
+  if (running) o = align_up(o + (size_t)ps.pb.text_rows * H * d * sizeof(float), 256);
+  w.lse_run = o;
+  if (running) o = align_up(o + (size_t)ps.pb.text_rows * H * sizeof(float), 256);
   w.total = o;
   return w;
 }
@@ -288,13 +293,8 @@ bool use_fused_forward() {
   return v != 0;
 }
 
-bool use_tc_path() {
-  static int v = [] {
-    const char* e = getenv("CPATTN_BF16_SIMT");
-    return (e && e[0] == '1') ? 0 : 1;
-  }();
-  return v != 0;
-}
+// The forward of this dtype merges ring steps through the fp32 running result.
+bool fwd_needs_running(cp_dtype_t dt) { return dt != CP_BF16 || !use_fused_forward(); }
 
 long long wait_limit() {
   long long w = g_wait_limit.load();
@@ -339,6 +339,7 @@ struct ProfScope {
 }  // namespace
 
 namespace cpattn {
+cudaError_t noalloc_read_status(int32_t out[2]);   // noalloc.cu
 // Shared with other translation units of the library (the fixed-scratch entry
 // point): the thread-local error message and the device wait bound.
 void set_last_error(const std::string& msg) { g_err = msg; }
@@ -378,12 +379,12 @@ cp_status_t cp_zigzag_index(const int32_t* cu, int n_seqs, int N, int P, int32_t
     if (s != CP_OK) return s;
     if ((fwd_idx && !aligned16(fwd_idx)) || (inv_idx && !aligned16(inv_idx)))
       return fail(CP_ERR_ALIGNMENT, "index tables must be 16-byte aligned");
-    if (ps->pb.text_rows == 0) return CP_OK;
-    std::vector<int32_t> f(ps->pb.text_rows), v(ps->pb.text_rows);
-    zigzag_tables(ps->pb, f.data(), v.data());
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if (fwd_idx) CP_CUDA(stager().upload(fwd_idx, f.data(), f.size() * 4, st), "upload fwd_idx");
-    if (inv_idx) CP_CUDA(stager().upload(inv_idx, v.data(), v.size() * 4, st), "upload inv_idx");
+    if (ps->pb.text_rows == 0 || (!fwd_idx && !inv_idx)) return CP_OK;
+    // the device kernel cp_attn_fwd runs for its own table
+    ProfScope ps_(0, static_cast<cudaStream_t>(stream));
+    CP_CUDA(launch_zigzag_index(ps->samples.data(), n_seqs, P, ps->pb.R, fwd_idx, inv_idx,
+                                static_cast<cudaStream_t>(stream)),
+            "zigzag index kernel");
     return CP_OK;
   }
   Problem pb;
@@ -428,7 +429,7 @@ size_t cp_attn_fwd_workspace_size_gqa(cp_dtype_t dt, int T, int H, int Hkv, int 
   std::shared_ptr<PlanSet> ps;
   if (!cu || H < 1 || Hkv < 1 || H % Hkv != 0 || (dt != CP_F32 && dt != CP_BF16)) return 0;
   if (get_plans(cu, n_seqs, N, P, T, H, d, &ps) != CP_OK) return 0;
-  return fwd_layout(*ps, H, Hkv, d, dt == CP_BF16 ? 2 : 4).total;
+  return fwd_layout(*ps, H, Hkv, d, dt == CP_BF16 ? 2 : 4, fwd_needs_running(dt)).total;
 }
 
 size_t cp_attn_fwd_workspace_size(cp_dtype_t dt, int T, int H, int d, const int32_t* cu,
@@ -458,10 +459,10 @@ cp_status_t cp_attn_fwd_gqa(const void* q, const void* k, const void* v, cp_dtyp
   if (s != CP_OK) return s;
   if (T == 0) return CP_OK;
   const bool bf16 = dt == CP_BF16;
-  const bool tc = bf16 && use_tc_path();
+  const bool tc = bf16;   // bf16: tensor cores; fp32: the CUDA-core parity path
   if (tc && (s = check_device_for_bf16()) != CP_OK) return s;
   const size_t elem = bf16 ? 2 : 4;
-  const FwdWs L = fwd_layout(*ps, H, Hkv, d, elem);
+  const FwdWs L = fwd_layout(*ps, H, Hkv, d, elem, fwd_needs_running(dt));
   if (!ws || ws_bytes < L.total)
     return fail(CP_ERR_WORKSPACE, "workspace smaller than cp_attn_fwd_workspace_size()");
   if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0)
@@ -483,14 +484,11 @@ cp_status_t cp_attn_fwd_gqa(const void* q, const void* k, const void* v, cp_dtyp
     CP_CUDA(stager().upload(w + L.items, fp.items.data(), fp.items.size() * sizeof(FwdItem), st),
             "upload work list");
   }
-  CP_CUDA(stager().upload(w + L.samples, ps->samples.data(), ps->samples.size() * 4, st),
-          "upload sample table");
   int32_t* idx = reinterpret_cast<int32_t*>(w + L.idx);
   // get_batch_on_this_cp_rank: zigzag table, then index_select of q, k, v text rows
   {
     ProfScope ps_(0, st);
-    CP_CUDA(launch_zigzag_index(reinterpret_cast<const int32_t*>(w + L.samples), n_seqs, P, pb.R,
-                                idx, nullptr, st),
+    CP_CUDA(launch_zigzag_index(ps->samples.data(), n_seqs, P, pb.R, idx, nullptr, st),
             "zigzag index kernel");
   }
   const void* src[3] = {q, k, v};
@@ -584,7 +582,7 @@ cp_status_t cp_attn_fwd_gqa(const void* q, const void* k, const void* v, cp_dtyp
     a.items = items + fp.step_begin[step];
     a.n_items = fp.step_begin[step + 1] - fp.step_begin[step];
     ProfScope ps_(6, st);
-    CP_CUDA(launch_simt_fwd(a, bf16, st), "ring step");
+    CP_CUDA(launch_simt_fwd(a, st), "ring step");
   }
   return CP_OK;
 }
@@ -611,7 +609,7 @@ size_t cp_attn_bwd_workspace_size_gqa(cp_dtype_t dt, int T, int H, int Hkv, int 
   std::shared_ptr<PlanSet> ps;
   if (!cu || H < 1 || Hkv < 1 || H % Hkv != 0 || (dt != CP_F32 && dt != CP_BF16)) return 0;
   if (get_plans(cu, n_seqs, N, P, T, H, d, &ps) != CP_OK) return 0;
-  const bool simt = !(dt == CP_BF16 && use_tc_path() && d == 128);
+  const bool simt = dt != CP_BF16;   // fp32: the CUDA-core parity path
   return bwd_layout(*ps, H, Hkv, d, simt, true).total;
 }
 
@@ -646,8 +644,7 @@ cp_status_t cp_attn_bwd_gqa(const void* q, const void* k, const void* v, const v
   if (s != CP_OK) return s;
   if (T == 0) return CP_OK;
   const bool bf16 = dt == CP_BF16;
-  // the tensor-core backward is built for head_dim 128; head_dim 64 runs on CUDA cores
-  const bool tc = bf16 && use_tc_path() && d == 128;
+  const bool tc = bf16;   // bf16: tensor cores (head_dim 64 and 128); fp32: CUDA cores
   if (tc && (s = check_device_for_bf16()) != CP_OK) return s;
   const BwdWs L = bwd_layout(*ps, H, Hkv, d, !tc, pgrad == nullptr);
   if (!ws || ws_bytes < L.total)
@@ -700,12 +697,16 @@ cp_status_t cp_attn_bwd_gqa(const void* q, const void* k, const void* v, const v
     }
     TcBwdArgs a;
     const char* terr = nullptr;
-    bool ok = make_tmap_thd(&a.tm_q, q, T, H, d, kBwdTileQ, &terr) &&
+    // 128-query tiles, or 64-query tiles for head_dim 128 with the dS split
+    const bool q128 = bwd_uses_q128(d, scale);
+    const int tq = bwd_tile_q(d, scale);
+    bool ok = make_tmap_thd(&a.tm_q, q, T, H, d, tq, &terr) &&
               make_tmap_thd(&a.tm_k, k, T, Hkv, d, kBwdTileK, &terr) &&
               make_tmap_thd(&a.tm_v, v, T, Hkv, d, kBwdTileK, &terr) &&
-              make_tmap_thd(&a.tm_do, dout, T, H, d, kBwdTileQ, &terr) &&
-              make_tmap_ld(&a.tm_ld, lse2, pitch, H, kBwdTileQ + 4, &terr) &&
-              make_tmap_f32_thd(&a.tm_dq, dq, T, H, d, 16, &terr);
+              make_tmap_thd(&a.tm_do, dout, T, H, d, tq, &terr) &&
+              make_tmap_ld(&a.tm_ld, lse2, pitch, H, tq + 4, &terr) &&
+              (q128 ? make_tmap_f32_sw128(&a.tm_dq, dq, T, H, d, 32, &terr)
+                    : make_tmap_f32_thd(&a.tm_dq, dq, T, H, d, 16, &terr));
     if (!ok) return fail(CP_ERR_CUDA, std::string("tensor map: ") + (terr ? terr : "?"));
     a.H = H; a.Hkv = Hkv; a.kv_split = kv_split; a.d = d; a.scale = scale;
     a.scale_log2 = scale * 1.4426950408889634f;
@@ -722,7 +723,8 @@ cp_status_t cp_attn_bwd_gqa(const void* q, const void* k, const void* v, const v
       a.items = items + ps->bwd.step_begin[step];
       a.n_items = ps->bwd.step_begin[step + 1] - ps->bwd.step_begin[step];
       a.pdl = prev ? 1 : 0;
-      CP_CUDA(launch_tc_bwd(a, st), "tensor-core backward ring step");
+      CP_CUDA(q128 ? launch_tc_bwd_q128(a, st) : launch_tc_bwd(a, st),
+              "tensor-core backward ring step");
       prev = a.n_items > 0;
     }
   } else {
@@ -740,8 +742,8 @@ cp_status_t cp_attn_bwd_gqa(const void* q, const void* k, const void* v, const v
       a.k_items = items + ps->bwd.step_begin[step];
       a.n_k_items = ps->bwd.step_begin[step + 1] - ps->bwd.step_begin[step];
       ProfScope ps_(7, st);
-      CP_CUDA(launch_simt_bwd_dq(a, bf16, st), "backward dq step");
-      CP_CUDA(launch_simt_bwd_dkdv(a, bf16, st), "backward dk/dv step");
+      CP_CUDA(launch_simt_bwd_dq(a, st), "backward dq step");
+      CP_CUDA(launch_simt_bwd_dkdv(a, st), "backward dk/dv step");
     }
   }
   if (N > 0) {
@@ -755,10 +757,13 @@ cp_status_t cp_attn_bwd_gqa(const void* q, const void* k, const void* v, const v
 }
 
 cp_status_t cp_workspace_status(const void* ws, void* stream) {
-  if (!ws) return fail(CP_ERR_INVALID_ARG, "workspace is NULL");
   CP_CUDA(cudaStreamSynchronize(static_cast<cudaStream_t>(stream)), "stream sync");
   DevStatus h{};
-  CP_CUDA(cudaMemcpy(&h, ws, sizeof(int32_t) * 2, cudaMemcpyDeviceToHost), "read status");
+  if (ws) {
+    CP_CUDA(cudaMemcpy(&h, ws, sizeof(int32_t) * 2, cudaMemcpyDeviceToHost), "read status");
+  } else {  // the fixed scratch of cp_attn_fwd_noalloc on the current device
+    CP_CUDA(noalloc_read_status(&h.timeout), "read the fixed scratch's status");
+  }
   if (h.timeout) {
     char buf[96];
     snprintf(buf, sizeof buf, "a device wait gave up (site %d)", h.where);

@@ -1,5 +1,6 @@
-// CUDA-core attention for fp32 inputs (FFMA, accurate expf/logf): one work
-// item of the ring-step plan per block.  It walks the same work lists as the
+// CUDA-core attention for fp32 inputs (FFMA, accurate expf/logf), the parity
+// path of the fp32 interface (bf16 inputs always run on the tensor cores): one
+// work item of the ring-step plan per block.  It walks the same work lists as the
 // tensor-core kernels: a query tile against runs of keys (forward, dQ), or a
 // key tile against runs of queries (dK, dV).
 #include <cuda_bf16.h>
@@ -354,22 +355,18 @@ cudaError_t dkdv_t(const SimtBwdArgs& a, cudaStream_t st) {
 
 }  // namespace
 
-cudaError_t launch_simt_fwd(const SimtFwdArgs& a, bool bf16, cudaStream_t st) {
+cudaError_t launch_simt_fwd(const SimtFwdArgs& a, cudaStream_t st) {
   if (a.n_items == 0) return cudaSuccess;
-  if (bf16) return a.d == 64 ? fwd_t<__nv_bfloat16, 64>(a, st) : fwd_t<__nv_bfloat16, 128>(a, st);
   return a.d == 64 ? fwd_t<float, 64>(a, st) : fwd_t<float, 128>(a, st);
 }
 
-cudaError_t launch_simt_bwd_dq(const SimtBwdArgs& a, bool bf16, cudaStream_t st) {
+cudaError_t launch_simt_bwd_dq(const SimtBwdArgs& a, cudaStream_t st) {
   if (a.n_q_items == 0) return cudaSuccess;
-  if (bf16) return a.d == 64 ? dq_t<__nv_bfloat16, 64>(a, st) : dq_t<__nv_bfloat16, 128>(a, st);
   return a.d == 64 ? dq_t<float, 64>(a, st) : dq_t<float, 128>(a, st);
 }
 
-cudaError_t launch_simt_bwd_dkdv(const SimtBwdArgs& a, bool bf16, cudaStream_t st) {
+cudaError_t launch_simt_bwd_dkdv(const SimtBwdArgs& a, cudaStream_t st) {
   if (a.n_k_items == 0) return cudaSuccess;
-  if (bf16)
-    return a.d == 64 ? dkdv_t<__nv_bfloat16, 64>(a, st) : dkdv_t<__nv_bfloat16, 128>(a, st);
   return a.d == 64 ? dkdv_t<float, 64>(a, st) : dkdv_t<float, 128>(a, st);
 }
 

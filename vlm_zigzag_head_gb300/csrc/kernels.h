@@ -20,9 +20,20 @@ constexpr size_t kStatusBytes = 256;
 cudaError_t launch_gather_rows(const void* const* src, void* const* dst, int n_tensors,
                                size_t row_bytes, const int32_t* idx, int n_rows, bool scatter,
                                cudaStream_t st);
-cudaError_t launch_zigzag_index(const int32_t* samples_dev /*[n][4]: t0, c, off, ord0*/,
-                                int n_seqs, int P, int64_t R, int32_t* fwd_idx, int32_t* inv_idx,
-                                cudaStream_t st);
+// Zigzag tables on the device.  `samples_host` is a HOST array [n_seqs][4]
+// (first text token, chunk length c, rank-local offset, text ordinal of the
+// first text token); it is passed to the kernel by value, kZigzagBatch
+// samples per launch, so the call needs no device copy of it.
+constexpr int kZigzagBatch = 192;
+struct ZigzagBatch {
+  int n, P;
+  long long R;          // rank-local rows per rank (all samples)
+  long long loc0;       // rank-local row of the batch's first sample
+  long long span;       // rank-local rows the batch covers on each rank
+  int32_t smp[kZigzagBatch][4];
+};
+cudaError_t launch_zigzag_index(const int32_t* samples_host, int n_seqs, int P, int64_t R,
+                                int32_t* fwd_idx, int32_t* inv_idx, cudaStream_t st);
 cudaError_t launch_lse_merge(int n_parts, const float* part_out, const float* part_lse, int rows,
                              int H, int d, void* out, bool out_bf16, float* lse, cudaStream_t st);
 // D[h*pitch + t] = sum_e dO[t][h][e] * O[t][h][e];  lse2[h*pitch + t] = lse[h][t] * log2(e)
@@ -35,7 +46,7 @@ cudaError_t launch_prefix_reduce(const float* slots_k, const float* slots_v, int
                                  const int32_t* cu_dev, int n_seqs, int N, int H, int d,
                                  float* dk, float* dv, cudaStream_t st);
 
-// ---- fp32 / CUDA-core attention (attn_simt.cu) -----------------------------
+// ---- fp32 inputs: CUDA-core attention (attn_simt.cu) -------------------------
 struct SimtFwdArgs {
   const void* q_text; const void* k_text; const void* v_text;  // SRC_TEXT tensors
   const void* q_nat; const void* k_nat; const void* v_nat;     // SRC_NAT tensors
@@ -45,7 +56,7 @@ struct SimtFwdArgs {
   float* o_run; float* lse_run; int64_t run_rows;   // [H][run_rows][d], [H][run_rows]
   void* out; float* lse; int64_t T;                 // natural order
 };
-cudaError_t launch_simt_fwd(const SimtFwdArgs& a, bool bf16, cudaStream_t st);
+cudaError_t launch_simt_fwd(const SimtFwdArgs& a, cudaStream_t st);
 
 struct SimtBwdArgs {
   const void* q; const void* k; const void* v; const void* dout;  // natural order
@@ -57,7 +68,7 @@ struct SimtBwdArgs {
   float* dq; float* dk; float* dv;
   float* pre_k; float* pre_v; int64_t pre_rows;   // [P+1][pre_rows][Hkv][d]
 };
-cudaError_t launch_simt_bwd_dq(const SimtBwdArgs& a, bool bf16, cudaStream_t st);
-cudaError_t launch_simt_bwd_dkdv(const SimtBwdArgs& a, bool bf16, cudaStream_t st);
+cudaError_t launch_simt_bwd_dq(const SimtBwdArgs& a, cudaStream_t st);
+cudaError_t launch_simt_bwd_dkdv(const SimtBwdArgs& a, cudaStream_t st);
 
 }  // namespace cpattn

@@ -56,27 +56,29 @@ __global__ void __launch_bounds__(kThreads) gather_rows_kernel(RowPtrs p, int n_
   }
 }
 
-// Thread per permuted text row k: rank r = k / R; its sample by binary search
-// over the rank-local offsets; then chunk r or 2P-1-r (page §1.1 pairing).
-__global__ void zigzag_index_kernel(const int32_t* __restrict__ smp, int n_seqs, int P,
-                                    long long R, int32_t* fwd_idx, int32_t* inv_idx) {
-  const long long n = R * P;
-  for (long long k = (long long)blockIdx.x * blockDim.x + threadIdx.x; k < n;
-       k += (long long)gridDim.x * blockDim.x) {
-    const int r = (int)(k / R);
-    const long long loc = k - (long long)r * R;
-    int lo = 0, hi = n_seqs - 1;
-    while (lo < hi) {  // last sample whose range [off, off + 2c) contains loc
+// Thread per permuted text row of one batch of samples: rank r, then the
+// sample by binary search over the batch's rank-local offsets, then chunk r
+// or 2P-1-r of that sample (page §1.1 head-tail pairing, §5.3 per sample).
+// The batch's sample table travels in the kernel parameters.
+__global__ void zigzag_index_kernel(const __grid_constant__ ZigzagBatch b, int32_t* fwd_idx,
+                                    int32_t* inv_idx) {
+  const long long n = (long long)b.span * b.P;
+  for (long long m = (long long)blockIdx.x * blockDim.x + threadIdx.x; m < n;
+       m += (long long)gridDim.x * blockDim.x) {
+    const int r = (int)(m / b.span);
+    const long long loc = b.loc0 + (m - (long long)r * b.span);   // rank-local row
+    int lo = 0, hi = b.n - 1;
+    while (lo < hi) {  // last sample of the batch whose range [off, off + 2c) starts at or before loc
       const int mid = (lo + hi + 1) >> 1;
-      if (smp[mid * 4 + 2] <= loc) lo = mid; else hi = mid - 1;
+      if (b.smp[mid][2] <= loc) lo = mid; else hi = mid - 1;
     }
-    while (lo > 0 && smp[lo * 4 + 1] == 0) --lo;  // skip text-less samples
-    const long long t0 = smp[lo * 4 + 0], c = smp[lo * 4 + 1], off = smp[lo * 4 + 2],
-                    ord0 = smp[lo * 4 + 3];
+    while (lo > 0 && b.smp[lo][1] == 0) --lo;  // text-less samples share the next one's offset
+    const long long t0 = b.smp[lo][0], c = b.smp[lo][1], off = b.smp[lo][2], ord0 = b.smp[lo][3];
     const long long within = loc - off;
     const int slot = (int)(within / c);
     const long long t = within - slot * c;
-    const long long ch = slot == 0 ? r : 2 * P - 1 - r;
+    const long long ch = slot == 0 ? r : 2LL * b.P - 1 - r;
+    const long long k = (long long)r * b.R + loc;
     if (fwd_idx) fwd_idx[k] = (int32_t)(t0 + ch * c + t);
     if (inv_idx) inv_idx[ord0 + ch * c + t] = (int32_t)k;
   }
@@ -240,11 +242,27 @@ cudaError_t launch_gather_rows(const void* const* src, void* const* dst, int n_t
 
 cudaError_t launch_zigzag_index(const int32_t* smp, int n_seqs, int P, int64_t R,
                                 int32_t* fwd_idx, int32_t* inv_idx, cudaStream_t st) {
-  const long long n = (long long)R * P;
-  if (n == 0) return cudaSuccess;
-  zigzag_index_kernel<<<grid_for(n, kThreads), kThreads, 0, st>>>(smp, n_seqs, P, R, fwd_idx,
-                                                                   inv_idx);
-  return cudaGetLastError();
+  if (R == 0 || P < 1) return cudaSuccess;
+  // one launch per batch of up to kZigzagBatch samples: each covers, on every
+  // rank, the contiguous rank-local rows of its samples
+  for (int i0 = 0; i0 < n_seqs; i0 += kZigzagBatch) {
+    const int i1 = n_seqs - i0 < kZigzagBatch ? n_seqs : i0 + kZigzagBatch;
+    ZigzagBatch b;
+    b.n = i1 - i0;
+    b.P = P;
+    b.R = R;
+    b.loc0 = smp[i0 * 4 + 2];
+    const long long end = (long long)smp[(i1 - 1) * 4 + 2] + 2LL * smp[(i1 - 1) * 4 + 1];
+    b.span = end - b.loc0;
+    if (b.span == 0) continue;
+    for (int i = i0; i < i1; ++i)
+      for (int f = 0; f < 4; ++f) b.smp[i - i0][f] = smp[i * 4 + f];
+    const long long n = b.span * (long long)P;
+    zigzag_index_kernel<<<grid_for(n, kThreads), kThreads, 0, st>>>(b, fwd_idx, inv_idx);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 cudaError_t launch_lse_merge(int n_parts, const float* po, const float* pl, int rows, int H,

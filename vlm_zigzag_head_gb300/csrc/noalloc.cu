@@ -1,7 +1,8 @@
 // cp_attn_fwd_noalloc: the forward for callers that cannot allocate device
-// memory.  Its scratch (work list, zigzag table, rank-local q/k/v, the fp32
-// running result) lives in one fixed array compiled into this library instead
-// of a caller-supplied workspace.  Host-side uploads are plain copies from the
+// memory.  Its scratch (work lists, zigzag table, rank-local q/k/v, and for
+// fp32 inputs the running result) lives in one fixed array compiled into this
+// library instead of a caller-supplied workspace; its status word is the first
+// thing in that array.  Host-side uploads are plain copies from the
 // plan's own vectors; nothing here calls cudaMalloc, cudaFree, cudaHostAlloc
 // or any other allocating routine.
 #include <cuda.h>
@@ -62,6 +63,15 @@ cp_status_t scratch_address(void** out) {
 
 }  // namespace
 
+namespace cpattn {
+// Status words of the fixed scratch on the current device, read after the
+// caller has synchronised the stream (cp_workspace_status with a NULL
+// workspace).  Reads the symbol directly: no allocation.
+cudaError_t noalloc_read_status(int32_t out[2]) {
+  return cudaMemcpyFromSymbol(out, g_scratch, 2 * sizeof(int32_t), 0, cudaMemcpyDeviceToHost);
+}
+}  // namespace cpattn
+
 extern "C" cp_status_t cp_attn_fwd_noalloc(const void* q, const void* k, const void* v,
                                            cp_dtype_t dt, int T, int H, int d,
                                            const int32_t* cu, int n_seqs, int P, int N,
@@ -84,8 +94,24 @@ extern "C" cp_status_t cp_attn_fwd_noalloc(const void* q, const void* k, const v
   if (!err.empty()) return fail(CP_ERR_SHAPE, err);
   if (T == 0) return CP_OK;
   const bool bf16 = dt == CP_BF16;
+  // bf16: the all-steps tensor-core forward (every ring step of a query tile
+  // in one persistent launch, no fp32 running result); fp32: one CUDA-core
+  // launch per ring step with the running result in the scratch
   FwdPlan plan;
   plan_forward(pb, true, &plan, bf16 ? kFwdPairQ : kFwdTileQ);
+  FusedFwdPlan fused;
+  std::vector<int32_t> units, cta_off;
+  int sms = 0, grid = 0;
+  if (bf16) {
+    plan_forward_fused(plan, P, &fused);
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const long long n_units = (long long)fused.items.size() * H;
+    if (n_units > 0x7fffffffLL) return fail(CP_ERR_INVALID_ARG, "too many work units");
+    grid = (int)fwd_grid(n_units, sms > 0 ? sms : 1);
+    if (grid < n_units) plan_unit_lists(fused.items, H, grid, &units, &cta_off);
+  }
   std::vector<int32_t> samples;
   int64_t ord = 0;
   for (int i = 0; i < n_seqs; ++i) {
@@ -96,13 +122,17 @@ extern "C" cp_status_t cp_attn_fwd_noalloc(const void* q, const void* k, const v
   const size_t elem = bf16 ? 2 : 4;
   size_t o = 0;
   const size_t o_status = o; o += kStatusBytes;
-  const size_t o_items = o; o = up256(o + plan.items.size() * sizeof(FwdItem));
-  const size_t o_samples = o; o = up256(o + samples.size() * sizeof(int32_t));
+  const size_t n_items = bf16 ? fused.items.size() : plan.items.size();
+  const size_t o_items = o; o = up256(o + n_items * sizeof(FwdItem));
+  const size_t o_runs = o; o = up256(o + fused.runs.size() * sizeof(Seg));
+  const size_t o_units = o; o = up256(o + (units.size() + cta_off.size()) * sizeof(int32_t));
   const size_t o_idx = o; o = up256(o + (size_t)pb.text_rows * sizeof(int32_t));
   size_t o_qkv[3];
   for (int i = 0; i < 3; ++i) { o_qkv[i] = o; o = up256(o + (size_t)pb.text_rows * H * d * elem); }
-  const size_t o_run = o; o = up256(o + (size_t)pb.text_rows * H * d * sizeof(float));
-  const size_t o_lrun = o; o = up256(o + (size_t)pb.text_rows * H * sizeof(float));
+  const size_t o_run = o;
+  if (!bf16) o = up256(o + (size_t)pb.text_rows * H * d * sizeof(float));
+  const size_t o_lrun = o;
+  if (!bf16) o = up256(o + (size_t)pb.text_rows * H * sizeof(float));
   if (o > kScratchBytes) {
     char buf[160];
     snprintf(buf, sizeof buf,
@@ -128,25 +158,35 @@ extern "C" cp_status_t cp_attn_fwd_noalloc(const void* q, const void* k, const v
     cudaError_t e_ = (call);                                                             \
     if (e_ != cudaSuccess) return fail(CP_ERR_CUDA, std::string(what) + ": " + cudaGetErrorString(e_)); \
   } while (0)
-  // the status word must start at zero; everything else is written before it is read
+  // The host arrays below are pageable, so each copy returns only once the
+  // source has been read: they may go out of scope when this call returns.
+  // The status word must start at zero; everything else is written before it
+  // is read.
   NA_CUDA(cudaMemsetAsync(w + o_status, 0, kStatusBytes, st), "clear status");
-  NA_CUDA(cudaMemcpyAsync(w + o_items, plan.items.data(), plan.items.size() * sizeof(FwdItem),
+  const void* items_src = bf16 ? (const void*)fused.items.data() : (const void*)plan.items.data();
+  NA_CUDA(cudaMemcpyAsync(w + o_items, items_src, n_items * sizeof(FwdItem),
                           cudaMemcpyHostToDevice, st),
           "upload work list");
-  NA_CUDA(cudaMemcpyAsync(w + o_samples, samples.data(), samples.size() * sizeof(int32_t),
-                          cudaMemcpyHostToDevice, st),
-          "upload sample table");
+  if (!fused.runs.empty())
+    NA_CUDA(cudaMemcpyAsync(w + o_runs, fused.runs.data(), fused.runs.size() * sizeof(Seg),
+                            cudaMemcpyHostToDevice, st),
+            "upload key runs");
+  if (!units.empty()) {
+    NA_CUDA(cudaMemcpyAsync(w + o_units, units.data(), units.size() * sizeof(int32_t),
+                            cudaMemcpyHostToDevice, st),
+            "upload unit lists");
+    NA_CUDA(cudaMemcpyAsync(w + o_units + units.size() * sizeof(int32_t), cta_off.data(),
+                            cta_off.size() * sizeof(int32_t), cudaMemcpyHostToDevice, st),
+            "upload unit list offsets");
+  }
   int32_t* idx = reinterpret_cast<int32_t*>(w + o_idx);
-  NA_CUDA(launch_zigzag_index(reinterpret_cast<const int32_t*>(w + o_samples), n_seqs, P, pb.R,
-                              idx, nullptr, st),
+  NA_CUDA(launch_zigzag_index(samples.data(), n_seqs, P, pb.R, idx, nullptr, st),
           "zigzag index kernel");
   const void* src[3] = {q, k, v};
   void* dst[3] = {w + o_qkv[0], w + o_qkv[1], w + o_qkv[2]};
   NA_CUDA(launch_gather_rows(src, dst, 3, (size_t)H * d * elem, idx, (int)pb.text_rows, false, st),
           "zigzag gather");
   const FwdItem* items = reinterpret_cast<const FwdItem*>(w + o_items);
-  float* orun = reinterpret_cast<float*>(w + o_run);
-  float* lrun = reinterpret_cast<float*>(w + o_lrun);
   if (bf16) {
     TcFwdArgs a;
     const char* terr = nullptr;
@@ -159,33 +199,38 @@ extern "C" cp_status_t cp_attn_fwd_noalloc(const void* q, const void* k, const v
                     make_tmap_thd(&a.tm_v_nat, v, T, H, d, 128, &terr);
     if (!ok) return fail(CP_ERR_CUDA, std::string("tensor map: ") + (terr ? terr : "?"));
     a.H = H; a.Hkv = H; a.d = d; a.pdl = 0;
-    a.runs = nullptr;  // one ring step per launch (fp32 running result in the scratch)
+    a.items = items;
+    a.n_items = (int)fused.items.size();
+    a.runs = reinterpret_cast<const Seg*>(w + o_runs);
     a.units = nullptr;
     a.cta_off = nullptr;
     a.n_ctas = 0;
+    if (!units.empty()) {
+      a.units = reinterpret_cast<const int32_t*>(w + o_units);
+      a.cta_off = a.units + units.size();
+      a.n_ctas = grid;
+    }
     a.scale_log2 = scale * 1.4426950408889634f;
     a.split_p = scale > kPrecisionSplitScale ? 1 : 0;
-    a.o_run = orun; a.lse_run = lrun; a.run_rows = PR;
+    a.o_run = nullptr; a.lse_run = nullptr; a.run_rows = 0;
     a.out = out; a.lse = lse; a.T = T; a.out_lo = out_lo;
     a.status = reinterpret_cast<int32_t*>(w + o_status);
     a.wait_limit = device_wait_limit();
-    for (int step = 0; step < P; ++step) {
-      a.items = items + plan.step_begin[step];
-      a.n_items = plan.step_begin[step + 1] - plan.step_begin[step];
-      NA_CUDA(launch_tc_fwd(a, st), "tensor-core ring step");
-    }
+    NA_CUDA(launch_tc_fwd(a, st), "tensor-core forward (all ring steps)");
     return CP_OK;
   }
   SimtFwdArgs a;
   a.q_text = dst[0]; a.k_text = dst[1]; a.v_text = dst[2];
   a.q_nat = q; a.k_nat = k; a.v_nat = v;
   a.H = H; a.Hkv = H; a.d = d; a.scale = scale;
-  a.o_run = orun; a.lse_run = lrun; a.run_rows = pb.text_rows;
+  a.o_run = reinterpret_cast<float*>(w + o_run);
+  a.lse_run = reinterpret_cast<float*>(w + o_lrun);
+  a.run_rows = pb.text_rows;
   a.out = out; a.lse = lse; a.T = T;
   for (int step = 0; step < P; ++step) {
     a.items = items + plan.step_begin[step];
     a.n_items = plan.step_begin[step + 1] - plan.step_begin[step];
-    NA_CUDA(launch_simt_fwd(a, false, st), "ring step");
+    NA_CUDA(launch_simt_fwd(a, st), "ring step");
   }
 #undef NA_CUDA
   return CP_OK;

@@ -22,6 +22,10 @@ bool make_tmap_thd(CUtensorMap* map, const void* base, int64_t rows, int H, int 
 // swizzle (the dQ reduce-add target of the backward).
 bool make_tmap_f32_thd(CUtensorMap* map, void* base, int64_t rows, int H, int d, int box_rows,
                        const char** err);
+// 3-D tensor map over an fp32 [rows][H][d] tensor, box {32, 1, box_rows} with
+// the 128-byte swizzle (the dQ reduce-add target of the 128-query backward).
+bool make_tmap_f32_sw128(CUtensorMap* map, void* base, int64_t rows, int H, int d, int box_rows,
+                         const char** err);
 // 3-D tensor map over the fp32 planes [2][H][pitch] (lse2, D) of the backward
 // preprocess, box {box_rows, 1, 2}; pitch must be a multiple of 4.
 bool make_tmap_ld(CUtensorMap* map, const void* base, int64_t pitch, int H, int box_rows,
@@ -68,5 +72,15 @@ struct TcBwdArgs {
   int pdl;                    // launched as a programmatic dependent of the previous ring step
 };
 cudaError_t launch_tc_bwd(const TcBwdArgs& a, cudaStream_t st);
+
+// The backward walks 128-query tiles (tc_bwd_q128.cu) except at head_dim 128
+// with the dS precision split, whose second dS buffer does not fit in shared
+// memory beside 128-query tiles; that case walks 64-query tiles (tc_bwd.cu).
+// The tensor maps differ: Q / dO boxes of bwd_tile_q(...) rows, an lse2 / D
+// box of bwd_tile_q(...) + 4 rows, and the dQ target as swizzled 32-column
+// boxes of 32 rows (128-query tiles) or unswizzled d-column boxes of 16 rows.
+inline bool bwd_uses_q128(int d, float scale) { return d == 64 || scale <= kPrecisionSplitScale; }
+inline int bwd_tile_q(int d, float scale) { return bwd_uses_q128(d, scale) ? 128 : 64; }
+cudaError_t launch_tc_bwd_q128(const TcBwdArgs& a, cudaStream_t st);
 
 }  // namespace cpattn

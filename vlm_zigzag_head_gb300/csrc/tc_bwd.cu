@@ -1,4 +1,8 @@
-// Ring-step attention backward on 5th-generation tensor cores (sm_103a).
+// Ring-step attention backward on 5th-generation tensor cores (sm_103a), with
+// 64-query tiles: the form taken at head_dim 128 when the softmax scale is
+// above kPrecisionSplitScale, where dS enters dQ as a bf16 hi + lo pair and the
+// second dS buffer does not fit in shared memory beside 128-query tiles (every
+// other case runs tc_bwd_q128.cu).
 //
 // One CTA owns one key tile (128 keys of one KV head) of a ring step and walks
 // the query runs that met those keys at that step, for every query head that
@@ -604,10 +608,10 @@ cudaError_t launch_tc_bwd(const TcBwdArgs& a, cudaStream_t st) {
   if (a.d != kD) return cudaErrorNotSupported;
   if (a.kv_split < 1 || (a.H / a.Hkv) % a.kv_split != 0) return cudaErrorInvalidValue;
   // The dQ error from one bf16 rounding of dS grows with the softmax scale
-  // (dQ = scale * dS K).  Above kPrecisionSplitScale the remainder term is added.
-  const bool split = a.scale > kPrecisionSplitScale;
-  if (a.kv_split > 1) return split ? launch_split<true, true>(a, st) : launch_split<false, true>(a, st);
-  return split ? launch_split<true, false>(a, st) : launch_split<false, false>(a, st);
+  // (dQ = scale * dS K).  Above kPrecisionSplitScale the remainder term is
+  // added; every other case runs the 128-query kernel (tc_bwd_q128.cu).
+  if (!(a.scale > kPrecisionSplitScale)) return cudaErrorNotSupported;
+  return a.kv_split > 1 ? launch_split<true, true>(a, st) : launch_split<true, false>(a, st);
 }
 
 }  // namespace cpattn

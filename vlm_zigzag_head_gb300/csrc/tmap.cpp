@@ -75,6 +75,28 @@ bool make_tmap_f32_thd(CUtensorMap* map, void* base, int64_t rows, int H, int d,
   return true;
 }
 
+bool make_tmap_f32_sw128(CUtensorMap* map, void* base, int64_t rows, int H, int d, int box_rows,
+                         const char** err) {
+  auto fn = encode_fn();
+  if (!fn) {
+    *err = "cuTensorMapEncodeTiled unavailable";
+    return false;
+  }
+  if (rows < 1) rows = 1;
+  cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)H, (cuuint64_t)rows};
+  cuuint64_t strides[2] = {(cuuint64_t)d * 4, (cuuint64_t)H * d * 4};
+  cuuint32_t box[3] = {32, 1, (cuuint32_t)box_rows};   // 32 fp32 = one 128-byte swizzle row
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    *err = "cuTensorMapEncodeTiled failed (swizzled fp32 rows)";
+    return false;
+  }
+  return true;
+}
+
 bool make_tmap_ld(CUtensorMap* map, const void* base, int64_t pitch, int H, int box_rows,
                   const char** err) {
   auto fn = encode_fn();
