@@ -1,9 +1,11 @@
 """Throughput of zigzag context-parallel causal attention (forward + backward).
 
 One step = one pass of the whole hot path over one batch of synthetic input:
-cp_attn_fwd (zigzag gather, P ring-step kernels with the fused log-sum-exp
-merge) followed by cp_attn_bwd (preprocess, P ring-step kernels, prefix
-gradient sum).  Default workload: "long" -- 131072 text tokens, P = 8
+cp_attn_fwd (zigzag index and gather, one persistent tensor-core launch over
+all P ring steps whose online softmax is the log-sum-exp merge) followed by
+cp_attn_bwd (preprocess, P ring-step tensor-core launches, prefix gradient
+sum).  The other bf16 workloads of the method are measured the same way and
+reported under "workloads".  Default workload: "long" -- 131072 text tokens, P = 8
 simulated ranks, 32 heads, head_dim 128, bf16; inputs are ~1 GiB per tensor,
 far larger than L2, so no flush is needed between steps.
 
@@ -36,9 +38,9 @@ from vlm_zigzag_head_gb300 import workloads as W  # noqa: E402
 METRIC = "CP causal attention TFLOP/s fwd & fwd+bwd, % of GB300 BF16 tensor peak"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) per launch of the
-# backward ring-step kernel, mean over the 8 launches of one step, from one ncu
-# capture of this kernel on the named workload.  Set an entry to None when the
-# kernel changes until it is captured again.
+# backward ring-step kernel, mean over the ring-step launches of one call, from
+# one ncu capture of this kernel on the named workload.  An entry is removed
+# when the kernel changes, until it is captured again.
 MEASURED_TRAFFIC = {"long": 14.48e9}
 EX2_PER_CLK_SM = 32.0   # MUFU exp2 results per clock per SM (31.8 measured by a throughput loop)
 # every bf16 forward + backward workload of the method; the default line's
@@ -336,7 +338,7 @@ def run_cuda(args, w, rank, world, dist):
     if bwd_launches:
         avg = bwd_ms_k / bwd_launches
         ach = bwd_launch_flops / (avg / 1e3) / 1e12
-        roof = {"kernel": "tc_bwd_kernel (backward ring step)", "bound": "tensor",
+        roof = {"kernel": "tc_bwd_q128_kernel (backward ring step)", "bound": "tensor",
                 "achieved": ach, "peak": peak_sus, "unit": "TFLOP/s", "frac": ach / peak_sus,
                 "peak_source": "%s bf16_tflops_sustained" % peak_src,
                 "traffic": (args.traffic if args.traffic is not None
