@@ -39,9 +39,10 @@
 //   warps 4..11  P / dS (two warpgroups, 64 query columns each; thread = key
 //                row), then the dK / dV epilogue
 //   warps 12..15 dQ drain; thread = query row (TMEM lane of dQ)
-// Registers: warpgroup 0 drops to 56, the P / dS warpgroups rise to 136 and
-// the drain warpgroup to 176 (128 * 56 + 256 * 136 + 128 * 176 <= 512 * 128),
-// so a drain thread can hold its whole dQ row and free the TMEM at once.
+// Registers: warpgroup 0 drops to 64 (the least that leaves its MMA and
+// producer code without spills), the P / dS warpgroups rise to 136 and the
+// drain warpgroup to 168 (128 * 64 + 256 * 136 + 128 * 168 <= 512 * 128), so a
+// drain thread can hold its whole dQ row and free the TMEM at once.
 #include <cuda_bf16.h>
 
 #include <type_traits>
@@ -214,7 +215,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int n_all = Gs * n_qt;
 
   if (warp < 4) {
-    setmaxnreg_dec<56>();
+    setmaxnreg_dec<64>();
     if (warp == 0) {
       // ---------------------------------------------------------- TMA producer: K, V, Q, lse2 / D
       if (lane == 0) {
@@ -388,7 +389,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else if (warp >= 12) {
-    setmaxnreg_inc<176>();
+    setmaxnreg_inc<168>();
     // ------------------------------------------------------------ dQ drain
     // thread = query row wq * 32 + lane of the tile (TMEM lane of dQ).  The
     // whole row comes out of TMEM first (its columns are free again for the
