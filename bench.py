@@ -3,8 +3,8 @@
 One step = one pass of the whole hot path over one batch of synthetic input:
 cp_attn_fwd (zigzag index and gather, one persistent tensor-core launch over
 all P ring steps whose online softmax is the log-sum-exp merge) followed by
-cp_attn_bwd (preprocess, P ring-step tensor-core launches, prefix gradient
-sum).  The other bf16 workloads of the method are measured the same way and
+cp_attn_bwd (preprocess, one tensor-core launch over all P ring steps that
+sums dK / dV on chip, prefix gradient sum).  The other bf16 workloads of the method are measured the same way and
 reported under "workloads".  Default workload: "long" -- 131072 text tokens, P = 8
 simulated ranks, 32 heads, head_dim 128, bf16; inputs are ~1 GiB per tensor,
 far larger than L2, so no flush is needed between steps.
@@ -38,10 +38,10 @@ from vlm_zigzag_head_gb300 import workloads as W  # noqa: E402
 METRIC = "CP causal attention TFLOP/s fwd & fwd+bwd, % of GB300 BF16 tensor peak"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) per launch of the
-# backward ring-step kernel, mean over the ring-step launches of one call, from
-# one ncu capture of this kernel on the named workload.  An entry is removed
-# when the kernel changes, until it is captured again.
-MEASURED_TRAFFIC = {"long": 14.48e9}
+# tensor-core backward on the named workload, from one ncu capture of this
+# kernel (scaled from a smaller case where stated).  An entry is removed when
+# the kernel changes, until it is captured again.
+MEASURED_TRAFFIC = {}
 EX2_PER_CLK_SM = 32.0   # MUFU exp2 results per clock per SM (31.8 measured by a throughput loop)
 # every bf16 forward + backward workload of the method; the default line's
 # `value` is the 128K one, the others are reported under `workloads`
@@ -329,16 +329,21 @@ def run_cuda(args, w, rank, world, dist):
     bwd_ms = timed(lambda: cp.cp_attn_bwd(qd, kd, vd, out, lse, dod, cu, P, N, scale,
                                           workspace=ws_b, grads=grads, out_lo=out_lo), n_sub)
 
-    # dominant kernel: the tensor-core backward ring step (algorithmic FLOPs:
-    # 10 d per visible pair and head, summed over the P step launches)
+    # dominant kernel: the tensor-core backward (algorithmic FLOPs: 10 d per
+    # visible pair and head).  With 128-query tiles one launch covers every
+    # ring step of a call; with 64-query tiles (head_dim 128, softmax scale
+    # above 0.25) there are P ring-step launches, which share the call's FLOPs
     bwd_ms_k, bwd_launches = prof["tc_bwd_step"]
     fwd_ms_k, fwd_launches = prof["tc_fwd_step"]
-    bwd_launch_flops = 2.5 * f_flops / P
+    bwd_per_call = max(1, bwd_launches // max(1, args.steps))
+    bwd_launch_flops = 2.5 * f_flops / bwd_per_call
     roof = None
     if bwd_launches:
         avg = bwd_ms_k / bwd_launches
         ach = bwd_launch_flops / (avg / 1e3) / 1e12
-        roof = {"kernel": "tc_bwd_q128_kernel (backward ring step)", "bound": "tensor",
+        name = ("tc_bwd_q128_kernel (all ring steps)" if bwd_per_call == 1
+                else "tc_bwd_kernel (backward ring step)")
+        roof = {"kernel": name, "bound": "tensor",
                 "achieved": ach, "peak": peak_sus, "unit": "TFLOP/s", "frac": ach / peak_sus,
                 "peak_source": "%s bf16_tflops_sustained" % peak_src,
                 "traffic": (args.traffic if args.traffic is not None

@@ -45,6 +45,12 @@
  *    wait that exceeds its bound (see cp_set_wait_limit) makes the kernel
  *    record the fact in the workspace and return early; cp_workspace_status()
  *    reports it as CP_ERR_TIMEOUT.
+ *  - Bounds-checked build (libcpattn_checked.so, compiled with
+ *    -DCPATTN_BOUNDS_CHECK): before every TMA load, TMA reduce and global
+ *    store the tensor-core kernels test the row and head index against the
+ *    tensor's extent; an index outside it is not accessed, the kernel records
+ *    the site in the status word and stops, and cp_workspace_status() reports
+ *    CP_ERR_BOUNDS.  The normal build compiles these tests away.
  */
 #ifndef CPATTN_H_
 #define CPATTN_H_
@@ -67,7 +73,9 @@ typedef enum {
   CP_ERR_WORKSPACE = 5,   /* workspace missing or smaller than required */
   CP_ERR_CUDA = 6,        /* a CUDA runtime call failed (message has details) */
   CP_ERR_TIMEOUT = 7,     /* a bounded device-side wait gave up */
-  CP_ERR_UNSUPPORTED = 8  /* no kernel for this device / configuration */
+  CP_ERR_UNSUPPORTED = 8, /* no kernel for this device / configuration */
+  CP_ERR_BOUNDS = 9       /* bounds-checked build only: a kernel met an index
+                             outside its tensor, skipped the access and returned */
 } cp_status_t;
 
 typedef enum { CP_F32 = 0, CP_BF16 = 1 } cp_dtype_t;
@@ -216,7 +224,8 @@ cp_status_t cp_lse_merge(int n_parts, const float* part_out, const float* part_l
  *
  * Uses the final lse of the forward: D_i = dO_i . o_i, then for every ring
  * step the partial gradients of each rank's queries against the KV it met;
- * text dK/dV are accumulated for the rank that owns the KV.  At step 0 each
+ * text dK/dV are accumulated for the rank that owns the KV (on chip over all
+ * ring steps, in ring-step order, and written once).  At step 0 each
  * rank produces its own gradient of the replicated prefix K/V; these per-rank
  * gradients and the prefix queries' own term are summed in fixed order
  * (ranks 0..P-1, then the prefix-query term) -- the single-GPU stand-in for
@@ -285,7 +294,8 @@ cp_status_t cp_attn_bwd_gqa(const void* q, const void* k, const void* v, const v
 /*
  * cp_workspace_status -- synchronise `stream` and report whether a kernel of
  * the last cp_attn_fwd / cp_attn_bwd call that used `workspace` gave up on a
- * bounded device wait (CP_ERR_TIMEOUT) or CP_OK.  workspace = NULL: the same
+ * bounded device wait (CP_ERR_TIMEOUT), met an index outside a tensor
+ * (CP_ERR_BOUNDS, bounds-checked build only) or CP_OK.  workspace = NULL: the same
  * for the last cp_attn_fwd_noalloc call on the current device (its fixed
  * scratch holds the status word).
  */
@@ -298,10 +308,12 @@ cp_status_t cp_workspace_status(const void* workspace, void* stream);
  * the number of work items.  Forward figures are those of the 256-query items
  * of the tensor-core kernel; the 128-query items of the CUDA-core kernel are
  * checked to cover the same pairs, and the all-steps items of the default
- * tensor-core forward (every ring step of one query tile in one item) to
- * cover their sum.  Any output may be NULL.  Needs no GPU.
- * Errors: CP_ERR_INVALID_ARG, CP_ERR_SHAPE, CP_ERR_UNSUPPORTED (the forward
- * work lists disagree: an internal error).
+ * tensor-core forward (every ring step of one query tile in one item) and
+ * backward (every ring step of one key tile in one item, one item per key
+ * tile and prefix slot) to cover their sums.  Any output may be NULL.  Needs
+ * no GPU.
+ * Errors: CP_ERR_INVALID_ARG, CP_ERR_SHAPE, CP_ERR_UNSUPPORTED (the work
+ * lists disagree: an internal error).
  */
 cp_status_t cp_plan_pairs(const int32_t* cu_seqlens_h, int n_seqs, int prefix_len, int P,
                           int64_t* fwd_pairs, int64_t* bwd_pairs, int64_t* fwd_items,
@@ -334,11 +346,14 @@ cp_status_t cp_plan_unit_lists(const int32_t* cu_seqlens_h, int n_seqs, int pref
  * every kernel it launches (any thread).  The tensor-core forward is one
  * launch covering all ring steps; with CPATTN_FWD_PER_STEP=1 in the
  * environment it is P ring-step launches, which overlap one another's tails
- * and share one pair that counts as P launches.  cp_profile_end synchronises those events and returns, per
+ * and share one pair that counts as P launches.  The tensor-core backward is
+ * one launch covering all ring steps with 128-query tiles; with 64-query
+ * tiles (head_dim 128 with softmax scale above 0.25) it is P ring-step
+ * launches counted the same way.  cp_profile_end synchronises those events and returns, per
  * kernel kind, the summed milliseconds and the launch count in ms[8] /
  * launches[8] (either may be NULL):
  *   0 zigzag index   1 zigzag gather   2 tensor-core forward (ring steps)
- *   3 backward preprocess   4 tensor-core backward ring step
+ *   3 backward preprocess   4 tensor-core backward (ring steps)
  *   5 prefix-gradient sum   6 CUDA-core forward step   7 CUDA-core backward step
  * Errors: CP_ERR_CUDA.
  */

@@ -290,7 +290,8 @@ def _attn_bwd(q, k, v, out, lse, dout, cu_seqlens, P, prefix_len, softmax_scale,
 
 
 def cp_workspace_status(workspace: Optional[Workspace] = None, device=None) -> int:
-    """Synchronise the current stream; 0 or the CP_ERR_TIMEOUT status.  With
+    """Synchronise the current stream; 0, the CP_ERR_TIMEOUT status, or (in
+    the bounds-checked build, see ``_binding.bounds_checked``) CP_ERR_BOUNDS.  With
     no workspace it reads the status of :func:`cp_attn_fwd_noalloc`'s fixed
     scratch on ``device`` (default: the current device)."""
     if workspace is None:

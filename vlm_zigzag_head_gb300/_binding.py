@@ -5,13 +5,18 @@ fallback implementation anywhere in the package.
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 import threading
 
 _LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_lib", "libcpattn.so")
+_CHECKED_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_lib",
+                             "libcpattn_checked.so")
 _lock = threading.Lock()
 _lib = None
+_checked = None
+_use_checked = False
 
 c_i32p = ctypes.POINTER(ctypes.c_int32)
 c_i64p = ctypes.POINTER(ctypes.c_int64)
@@ -19,7 +24,7 @@ c_vp = ctypes.c_void_p
 
 STATUS = {0: "CP_OK", 1: "CP_ERR_INVALID_ARG", 2: "CP_ERR_SHAPE", 3: "CP_ERR_DTYPE",
           4: "CP_ERR_ALIGNMENT", 5: "CP_ERR_WORKSPACE", 6: "CP_ERR_CUDA", 7: "CP_ERR_TIMEOUT",
-          8: "CP_ERR_UNSUPPORTED"}
+          8: "CP_ERR_UNSUPPORTED", 9: "CP_ERR_BOUNDS"}
 CP_F32, CP_BF16 = 0, 1
 
 # name -> (restype, argtypes)
@@ -91,24 +96,51 @@ def lib_path() -> str:
     return _LIB_PATH
 
 
+def _load(path, how):
+    if not os.path.exists(path):
+        raise RuntimeError("%s is not built; run %s" % (path, how))
+    L = ctypes.CDLL(path)
+    for name, (res, args) in SIGNATURES.items():
+        fn = getattr(L, name)
+        fn.restype = res
+        fn.argtypes = args
+    return L
+
+
 def lib():
-    """The loaded library (raises if it was never built)."""
-    global _lib
+    """The loaded library (raises if it was never built).  Inside
+    ``bounds_checked()`` this is the bounds-checked debug build."""
+    global _lib, _checked
+    if _use_checked:
+        if _checked is None:
+            with _lock:
+                if _checked is None:
+                    _checked = _load(_CHECKED_PATH, "`python vlm_zigzag_head_gb300/build.py "
+                                     "--checked`")
+        return _checked
     if _lib is not None:
         return _lib
     with _lock:
         if _lib is None:
-            if not os.path.exists(_LIB_PATH):
-                raise RuntimeError("libcpattn.so is not built (%s); run "
-                                   "`python -c 'import __graft_entry__ as g; g.build()'`"
-                                   % _LIB_PATH)
-            L = ctypes.CDLL(_LIB_PATH)
-            for name, (res, args) in SIGNATURES.items():
-                fn = getattr(L, name)
-                fn.restype = res
-                fn.argtypes = args
-            _lib = L
+            _lib = _load(_LIB_PATH, "`python -c 'import __graft_entry__ as g; g.build()'`")
     return _lib
+
+
+@contextlib.contextmanager
+def bounds_checked():
+    """Route every call of the package, from any thread, through
+    libcpattn_checked.so while the block runs: the same kernels with each row
+    and head index tested before a TMA load, TMA reduce or global store (a
+    failure is skipped and reported as CP_ERR_BOUNDS by cp_workspace_status).
+    A debugging aid: the two libraries keep separate plan caches, wait limits
+    and fixed scratch."""
+    global _use_checked
+    prev = _use_checked
+    _use_checked = True
+    try:
+        yield lib()
+    finally:
+        _use_checked = prev
 
 
 def check(status: int):

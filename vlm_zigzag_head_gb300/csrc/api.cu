@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <map>
 #include <atomic>
 #include <cmath>
 #include <cstdio>
@@ -11,9 +12,11 @@
 #include <memory>
 #include <mutex>
 #include <string>
+#include <tuple>
 #include <vector>
 
 #include "../../include/cpattn.h"
+#include "check.cuh"
 #include "kernels.h"
 #include "plan.h"
 #include "tc.h"
@@ -125,6 +128,7 @@ struct PlanSet {
   FusedFwdPlan fused;  // fwd2 with all ring steps of a query tile in one item
   FwdPlan fwd_nat;   // text rows in natural order (fp32 dQ pass)
   BwdPlan bwd;
+  FusedBwdPlan bwd_fused;   // bwd with all ring steps of a key tile in one item (128-query kernel)
   std::vector<int32_t> samples;  // [n][4]: t0, c, off, ord0 (index kernel)
   std::mutex ul_mu;
   std::vector<std::shared_ptr<const UnitLists>> ul;  // recent unit lists
@@ -178,6 +182,7 @@ cp_status_t get_plans(const int32_t* cu, int n_seqs, int N, int P, int T, int H,
   plan_forward_fused(ps->fwd2, P, &ps->fused);
   plan_forward(pb, false, &ps->fwd_nat);
   plan_backward(pb, &ps->bwd);
+  plan_backward_fused(ps->bwd, P, 128, &ps->bwd_fused);
   int64_t ord = 0;
   for (int i = 0; i < n_seqs; ++i) {
     ps->samples.push_back(pb.cu[i] + N);
@@ -229,7 +234,8 @@ FwdWs fwd_layout(const PlanSet& ps, int H, int Hkv, int d, size_t elem, bool run
 }
 
 struct BwdWs {
-  size_t status = 0, items = 0, qitems = 0, cu = 0, D = 0, lse2 = 0, slots = 0, total = 0;
+  size_t status = 0, items = 0, runs = 0, qitems = 0, cu = 0, D = 0, lse2 = 0, slots = 0,
+         total = 0;
 };
 
 inline int64_t ld_pitch(int64_t T) { return (T + 3) / 4 * 4; }
@@ -239,7 +245,10 @@ BwdWs bwd_layout(const PlanSet& ps, int H, int Hkv, int d, bool simt, bool own_s
   const Problem& pb = ps.pb;
   size_t o = 0;
   w.status = o; o += kStatusBytes;
-  w.items = o; o = align_up(o + ps.bwd.items.size() * sizeof(BwdItem), 256);
+  w.items = o;
+  o = align_up(o + std::max(ps.bwd.items.size(), ps.bwd_fused.items.size()) * sizeof(BwdItem), 256);
+  w.runs = o;
+  if (!simt) o = align_up(o + ps.bwd_fused.runs.size() * sizeof(Seg), 256);
   w.qitems = o;
   if (simt) o = align_up(o + ps.fwd_nat.items.size() * sizeof(FwdItem), 256);
   w.cu = o; o = align_up(o + pb.cu.size() * sizeof(int32_t), 256);
@@ -361,6 +370,7 @@ const char* cp_status_string(cp_status_t s) {
     case CP_ERR_CUDA: return "CP_ERR_CUDA";
     case CP_ERR_TIMEOUT: return "CP_ERR_TIMEOUT";
     case CP_ERR_UNSUPPORTED: return "CP_ERR_UNSUPPORTED";
+    case CP_ERR_BOUNDS: return "CP_ERR_BOUNDS";
   }
   return "CP_ERR_UNKNOWN";
 }
@@ -526,6 +536,7 @@ cp_status_t cp_attn_fwd_gqa(const void* q, const void* k, const void* v, cp_dtyp
     a.scale_log2 = scale * 1.4426950408889634f;
     a.split_p = scale > kPrecisionSplitScale ? 1 : 0;
     a.o_run = o_run; a.lse_run = lse_run; a.run_rows = PR;
+    a.text_rows = PR;
     a.out = out; a.lse = lse; a.T = T; a.out_lo = out_lo;
     a.status = reinterpret_cast<int32_t*>(w + L.status);
     a.wait_limit = wait_limit();
@@ -661,9 +672,16 @@ cp_status_t cp_attn_bwd_gqa(const void* q, const void* k, const void* v, const v
   float* Dd = reinterpret_cast<float*>(w + L.D);
   float* lse2 = reinterpret_cast<float*>(w + L.lse2);
   CP_CUDA(cudaMemsetAsync(w + L.status, 0, kStatusBytes, st), "clear status");
-  CP_CUDA(stager().upload(w + L.items, ps->bwd.items.data(),
-                          ps->bwd.items.size() * sizeof(BwdItem), st),
+  // 128-query tiles (one launch over the all-steps plan), or 64-query tiles
+  // (one launch per ring step) for head_dim 128 with the dS split
+  const bool q128 = tc && bwd_uses_q128(d, scale);
+  const std::vector<BwdItem>& bitems = q128 ? ps->bwd_fused.items : ps->bwd.items;
+  CP_CUDA(stager().upload(w + L.items, bitems.data(), bitems.size() * sizeof(BwdItem), st),
           "upload work list");
+  if (q128)
+    CP_CUDA(stager().upload(w + L.runs, ps->bwd_fused.runs.data(),
+                            ps->bwd_fused.runs.size() * sizeof(Seg), st),
+            "upload run list");
   CP_CUDA(stager().upload(w + L.cu, pb.cu.data(), pb.cu.size() * 4, st), "upload cu_seqlens");
   const int64_t pitch = ld_pitch(T);
   {
@@ -684,8 +702,9 @@ cp_status_t cp_attn_bwd_gqa(const void* q, const void* k, const void* v, const v
       int dev = 0, sms = 0;
       CP_CUDA(cudaGetDevice(&dev), "cudaGetDevice");
       CP_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev), "SM count");
-      const double per_step = (double)ps->bwd.items.size() / P * Hkv;
-      while (G % (2 * kv_split) == 0 && per_step * kv_split < 4.0 * sms) kv_split *= 2;
+      const double per_launch =
+          q128 ? (double)bitems.size() * Hkv : (double)ps->bwd.items.size() / P * Hkv;
+      while (G % (2 * kv_split) == 0 && per_launch * kv_split < 4.0 * sms) kv_split *= 2;
     }
     if (kv_split > 1) {
       CP_CUDA(cudaMemsetAsync(dk, 0, (size_t)T * Hkv * d * sizeof(float), st), "clear dk");
@@ -697,8 +716,6 @@ cp_status_t cp_attn_bwd_gqa(const void* q, const void* k, const void* v, const v
     }
     TcBwdArgs a;
     const char* terr = nullptr;
-    // 128-query tiles, or 64-query tiles for head_dim 128 with the dS split
-    const bool q128 = bwd_uses_q128(d, scale);
     const int tq = bwd_tile_q(d, scale);
     bool ok = make_tmap_thd(&a.tm_q, q, T, H, d, tq, &terr) &&
               make_tmap_thd(&a.tm_k, k, T, Hkv, d, kBwdTileK, &terr) &&
@@ -713,19 +730,28 @@ cp_status_t cp_attn_bwd_gqa(const void* q, const void* k, const void* v, const v
     a.T = T;
     a.dq = dq; a.dk = dk; a.dv = dv;
     a.pre_k = pre_k; a.pre_v = pre_v; a.pre_rows = pre_rows;
+    a.n_slots = P + 1;
     a.status = reinterpret_cast<int32_t*>(w + L.status);
     a.wait_limit = wait_limit();
-    // as in the forward: later steps overlap the previous step's tail and
-    // wait for it only before the dK / dV epilogue
-    ProfScope ps_(4, st, P);
-    bool prev = false;
-    for (int step = 0; step < P; ++step) {
-      a.items = items + ps->bwd.step_begin[step];
-      a.n_items = ps->bwd.step_begin[step + 1] - ps->bwd.step_begin[step];
-      a.pdl = prev ? 1 : 0;
-      CP_CUDA(q128 ? launch_tc_bwd_q128(a, st) : launch_tc_bwd(a, st),
-              "tensor-core backward ring step");
-      prev = a.n_items > 0;
+    a.runs = reinterpret_cast<const Seg*>(w + L.runs);
+    if (q128) {   // every ring step in one launch: dK / dV written once
+      a.items = items;
+      a.n_items = (int)bitems.size();
+      a.pdl = 0;
+      ProfScope ps_(4, st, 1);
+      CP_CUDA(launch_tc_bwd_q128(a, st), "tensor-core backward (all ring steps)");
+    } else {
+      // one launch per ring step: later steps overlap the previous step's
+      // tail and wait for it only before the dK / dV epilogue
+      ProfScope ps_(4, st, P);
+      bool prev = false;
+      for (int step = 0; step < P; ++step) {
+        a.items = items + ps->bwd.step_begin[step];
+        a.n_items = ps->bwd.step_begin[step + 1] - ps->bwd.step_begin[step];
+        a.pdl = prev ? 1 : 0;
+        CP_CUDA(launch_tc_bwd(a, st), "tensor-core backward ring step");
+        prev = a.n_items > 0;
+      }
     }
   } else {
     CP_CUDA(stager().upload(w + L.qitems, ps->fwd_nat.items.data(),
@@ -763,6 +789,11 @@ cp_status_t cp_workspace_status(const void* ws, void* stream) {
     CP_CUDA(cudaMemcpy(&h, ws, sizeof(int32_t) * 2, cudaMemcpyDeviceToHost), "read status");
   } else {  // the fixed scratch of cp_attn_fwd_noalloc on the current device
     CP_CUDA(noalloc_read_status(&h.timeout), "read the fixed scratch's status");
+  }
+  if (h.timeout == kStatusBounds) {
+    char buf[96];
+    snprintf(buf, sizeof buf, "an index outside its tensor was skipped (site %d)", h.where);
+    return fail(CP_ERR_BOUNDS, buf);
   }
   if (h.timeout) {
     char buf[96];
@@ -818,10 +849,12 @@ cp_status_t cp_plan_pairs(const int32_t* cu, int n_seqs, int N, int P, int64_t* 
   FwdPlan f, f1;
   FusedFwdPlan fu;
   BwdPlan b;
+  FusedBwdPlan bu;
   plan_forward(pb, true, &f, kFwdPairQ);
   plan_forward(pb, true, &f1, kFwdTileQ);
   plan_forward_fused(f, P, &fu);
   plan_backward(pb, &b);
+  plan_backward_fused(b, P, 128, &bu);
   auto run_pairs = [](const Seg& sg, int q_len) {
     int64_t n = 0;
     for (int t = 0; t < q_len; ++t)
@@ -836,6 +869,23 @@ cp_status_t cp_plan_pairs(const int32_t* cu, int n_seqs, int N, int P, int64_t* 
     }
     return n;
   };
+  auto key_pairs = [](const BwdItem& it, const Seg* segs) {
+    int64_t n = 0;
+    for (int u = 0; u < it.k_len; ++u)
+      for (int g = 0; g < it.nseg; ++g) {
+        const Seg& sg = segs[g];
+        n += sg.causal ? std::max<int64_t>(0, sg.len - std::max<int64_t>(0, u - sg.delta)) : sg.len;
+      }
+    return n;
+  };
+  int64_t bwd_fused_pairs = 0, bwd_step_sum = 0;
+  std::map<std::tuple<int32_t, int32_t, int32_t>, int> seen;
+  for (const BwdItem& it : bu.items) {
+    if (it.flags != F_FIRST || it.run0 < 0 || it.run0 + it.nseg > (int64_t)bu.runs.size() ||
+        seen[std::make_tuple(it.dk_mode, it.k_row0, it.slot)]++ > 0)
+      return fail(CP_ERR_UNSUPPORTED, "all-steps backward item with a bad run range");
+    bwd_fused_pairs += key_pairs(it, bu.runs.data() + it.run0);
+  }
   int64_t fused_pairs = 0, step_sum = 0;
   for (const FwdItem& it : fu.items) {
     if (it.flags != (F_FIRST | F_FINAL) || it.run_row0 < 0 ||
@@ -847,17 +897,10 @@ cp_status_t cp_plan_pairs(const int32_t* cu, int n_seqs, int N, int P, int64_t* 
     int64_t fp = fwd_step_pairs(f, s), bp = 0;
     if (fp != fwd_step_pairs(f1, s))
       return fail(CP_ERR_UNSUPPORTED, "forward work lists of 128- and 256-row items disagree");
-    for (int x = b.step_begin[s]; x < b.step_begin[s + 1]; ++x) {
-      const BwdItem& it = b.items[x];
-      for (int u = 0; u < it.k_len; ++u)
-        for (int g = 0; g < it.nseg; ++g) {
-          const Seg& sg = it.seg[g];
-          int64_t vis = sg.causal ? std::max<int64_t>(0, sg.len - std::max<int64_t>(0, u - sg.delta))
-                                  : sg.len;
-          bp += vis;
-        }
-    }
+    for (int x = b.step_begin[s]; x < b.step_begin[s + 1]; ++x)
+      bp += key_pairs(b.items[x], b.items[x].seg);
     step_sum += fp;
+    bwd_step_sum += bp;
     if (fwd_pairs) fwd_pairs[s] = fp;
     if (bwd_pairs) bwd_pairs[s] = bp;
     if (fwd_items) fwd_items[s] = f.step_begin[s + 1] - f.step_begin[s];
@@ -865,6 +908,8 @@ cp_status_t cp_plan_pairs(const int32_t* cu, int n_seqs, int N, int P, int64_t* 
   }
   if (fused_pairs != step_sum)
     return fail(CP_ERR_UNSUPPORTED, "all-steps forward items disagree with the ring steps");
+  if (bwd_fused_pairs != bwd_step_sum)
+    return fail(CP_ERR_UNSUPPORTED, "all-steps backward items disagree with the ring steps");
   return CP_OK;
 }
 

@@ -10,8 +10,8 @@ namespace cpattn {
 
 // Device error word kept at the start of every workspace.
 struct DevStatus {
-  int32_t timeout;     // != 0: a bounded wait gave up
-  int32_t where;       // site code of the first timeout
+  int32_t timeout;     // 1: a bounded wait gave up; 3: an index check failed
+  int32_t where;       // site code of the first failure
   int32_t pad[62];
 };
 constexpr size_t kStatusBytes = 256;

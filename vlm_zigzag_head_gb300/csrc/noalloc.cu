@@ -213,6 +213,7 @@ extern "C" cp_status_t cp_attn_fwd_noalloc(const void* q, const void* k, const v
     a.scale_log2 = scale * 1.4426950408889634f;
     a.split_p = scale > kPrecisionSplitScale ? 1 : 0;
     a.o_run = nullptr; a.lse_run = nullptr; a.run_rows = 0;
+    a.text_rows = PR;
     a.out = out; a.lse = lse; a.T = T; a.out_lo = out_lo;
     a.status = reinterpret_cast<int32_t*>(w + o_status);
     a.wait_limit = device_wait_limit();

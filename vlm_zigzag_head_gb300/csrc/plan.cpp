@@ -5,6 +5,7 @@
 #include <cstdio>
 #include <map>
 #include <queue>
+#include <tuple>
 
 namespace cpattn {
 
@@ -272,6 +273,7 @@ void plan_backward(const Problem& pb, BwdPlan* plan) {
           // per-rank prefix gradient: rank r's text queries see the whole prefix
           for (int r = 0; r <= P; ++r) {
             BwdItem it{};
+            it.run0 = -1;
             it.k_row0 = (int32_t)(pb.cu[i] + u0);
             it.k_len = klen;
             it.dk_mode = DK_PREFIX_SLOT;
@@ -298,6 +300,7 @@ void plan_backward(const Problem& pb, BwdPlan* plan) {
           const int ck = chunk_id(P, j, w);
           for (int64_t u0 = 0; u0 < c; u0 += kBwdTileK) {
             BwdItem it{};
+            it.run0 = -1;
             it.k_row0 = (int32_t)(g.chunk_row(i, j, w) + u0);
             it.k_len = (int32_t)std::min<int64_t>(kBwdTileK, c - u0);
             it.dk_mode = DK_TEXT;
@@ -324,6 +327,45 @@ void plan_backward(const Problem& pb, BwdPlan* plan) {
     plan->items.insert(plan->items.end(), step.begin(), step.end());
     plan->step_begin.push_back((int32_t)plan->items.size());
   }
+}
+
+void plan_backward_fused(const BwdPlan& per_step, int P, int tile_q, FusedBwdPlan* out) {
+  // group the per-step items by destination (text key tile, or prefix key
+  // tile and slot), keeping ring-step order
+  struct Acc {
+    BwdItem head;
+    std::vector<Seg> segs;
+  };
+  std::vector<Acc> acc;
+  std::map<std::tuple<int32_t, int32_t, int32_t>, size_t> where;  // (dk_mode, k_row0, slot)
+  for (int s = 0; s < P; ++s) {
+    for (int x = per_step.step_begin[s]; x < per_step.step_begin[s + 1]; ++x) {
+      const BwdItem& it = per_step.items[x];
+      const auto key = std::make_tuple(it.dk_mode, it.k_row0, it.slot);
+      auto f = where.find(key);
+      if (f == where.end()) {
+        f = where.emplace(key, acc.size()).first;
+        acc.push_back({it, {}});
+      }
+      for (int g = 0; g < it.nseg; ++g) acc[f->second].segs.push_back(it.seg[g]);
+    }
+  }
+  out->items.clear();
+  out->runs.clear();
+  for (Acc& a : acc) {
+    BwdItem it = a.head;
+    it.nseg = (int32_t)a.segs.size();
+    it.run0 = (int32_t)out->runs.size();
+    it.flags = F_FIRST;
+    for (int g = 0; g < kBwdMaxSeg; ++g) it.seg[g] = Seg{};
+    int64_t tiles = 0;
+    for (const Seg& sg : a.segs) tiles += cdiv(bwd_visible(sg), tile_q);
+    it.n_tiles = (int32_t)tiles;
+    out->runs.insert(out->runs.end(), a.segs.begin(), a.segs.end());
+    out->items.push_back(it);
+  }
+  std::stable_sort(out->items.begin(), out->items.end(),
+                   [](const BwdItem& a, const BwdItem& b) { return a.n_tiles > b.n_tiles; });
 }
 
 }  // namespace cpattn

@@ -22,6 +22,7 @@ constexpr int kFwdTileK = 128;  // keys per forward KV tile
 constexpr int kBwdTileK = 128;  // keys of one backward work item
 constexpr int kBwdTileQ = 64;   // query rows per backward inner tile
 constexpr int kMaxSeg = 3;
+constexpr int kBwdMaxSeg = 2;   // query runs of a per-step backward item (two chunks of a rank)
 
 enum : int32_t { SRC_TEXT = 0, SRC_NAT = 1 };        // rank-local text buffer / natural order
 enum : int32_t { F_FIRST = 1, F_FINAL = 2 };         // forward merge epilogue modes
@@ -44,15 +45,18 @@ struct FwdItem {
   Seg seg[kMaxSeg];
 };
 
-// Backward: one key tile (<= kBwdTileK rows, natural order) against up to
-// kMaxSeg query runs (natural order).
+// Backward: one key tile (<= kBwdTileK rows, natural order) against query
+// runs (natural order): up to kBwdMaxSeg inline (per-step plans), or nseg
+// runs of the plan's run list from run0 on (all-steps plans).
 struct BwdItem {
   int32_t k_row0, k_len, nseg, n_tiles;
   int32_t dk_mode;  // DK_TEXT: dk/dv natural rows k_row0..; DK_PREFIX_SLOT: slot buffer
   int32_t dk_row0;  // row inside the prefix slot buffer (DK_PREFIX_SLOT)
   int32_t slot;     // prefix slot: rank 0..P-1, or P for the prefix queries' own term
   int32_t flags;    // F_FIRST: overwrite the destination, else accumulate
-  Seg seg[kMaxSeg];
+  int32_t run0;     // all-steps plans: index of the first run in the run list; else -1
+  int32_t pad[7];
+  Seg seg[kBwdMaxSeg];
 };
 
 static_assert(sizeof(Seg) == 32, "Seg layout");
@@ -120,5 +124,16 @@ void plan_unit_lists(const std::vector<FwdItem>& items, int H, int grid,
 // the second tile with delta + 128).
 void plan_forward(const Problem& pb, bool text_perm, FwdPlan* plan, int tile_q = kFwdTileQ);
 void plan_backward(const Problem& pb, BwdPlan* plan);
+
+// All ring steps fused per key tile (the mirror of FusedFwdPlan): each item
+// lists, in ring-step order, every query run its key tile meets over steps
+// 0..P-1, so that dK / dV accumulate on chip across the steps and are written
+// once (flags = F_FIRST).  Items: nseg runs from run0 in `runs`; n_tiles =
+// query tiles of tile_q rows (the cost); heaviest first.
+struct FusedBwdPlan {
+  std::vector<BwdItem> items;
+  std::vector<Seg> runs;
+};
+void plan_backward_fused(const BwdPlan& per_step, int P, int tile_q, FusedBwdPlan* out);
 
 }  // namespace cpattn

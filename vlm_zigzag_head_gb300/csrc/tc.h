@@ -46,11 +46,13 @@ struct TcFwdArgs {
   float scale_log2;           // softmax scale * log2(e)
   int split_p;                // P enters PV as bf16 hi + lo (softmax scale > kPrecisionSplitScale)
   int pdl;                    // launched as a programmatic dependent of the previous ring step
+                              // (64-query kernel; the 128-query kernel is one launch per call)
   float* o_run; float* lse_run; int64_t run_rows;
   void* out; float* lse; int64_t T;
   void* out_lo;               // nullable: bf16 remainder o - bf16(o)
   int32_t* status;            // DevStatus of the workspace
   long long wait_limit;
+  int64_t text_rows;          // rows of the rank-local (gathered) tensors (index checks)
 };
 cudaError_t launch_tc_fwd(const TcFwdArgs& a, cudaStream_t st);
 
@@ -59,6 +61,7 @@ struct TcBwdArgs {
   CUtensorMap tm_ld;                     // [2][H][pitch] fp32: lse2, D
   CUtensorMap tm_dq;                     // dq fp32 [T][H][d], box {d, 1, 16}: reduce-add target
   const BwdItem* items;
+  const Seg* runs;            // run list of an all-steps plan (128-query kernel); else unused
   int n_items, H, d;
   int Hkv;                    // KV heads; one CTA per (key tile, KV head) walks its H / Hkv query heads
   float scale, scale_log2;
@@ -70,10 +73,14 @@ struct TcBwdArgs {
   int kv_split;               // CTAs sharing one KV head's query heads (divides H / Hkv); > 1:
                               // dK / dV / prefix slots are reduce-added into zeroed memory
   int pdl;                    // launched as a programmatic dependent of the previous ring step
+                              // (64-query kernel; the 128-query kernel is one launch per call)
+  int n_slots;                // prefix-gradient slots (P + 1) behind pre_k / pre_v (index checks)
 };
 cudaError_t launch_tc_bwd(const TcBwdArgs& a, cudaStream_t st);
 
-// The backward walks 128-query tiles (tc_bwd_q128.cu) except at head_dim 128
+// The backward walks 128-query tiles (tc_bwd_q128.cu: one launch over the
+// all-steps plan, every item a key tile with the query runs of all ring
+// steps) except at head_dim 128
 // with the dS precision split, whose second dS buffer does not fit in shared
 // memory beside 128-query tiles; that case walks 64-query tiles (tc_bwd.cu).
 // The tensor maps differ: Q / dO boxes of bwd_tile_q(...) rows, an lse2 / D

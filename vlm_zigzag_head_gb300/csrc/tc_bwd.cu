@@ -39,6 +39,7 @@
 
 #include <type_traits>
 
+#include "check.cuh"
 #include "kernels.h"
 #include "ptx.cuh"
 #include "tc.h"
@@ -201,7 +202,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
     // ------------------------------------------------------------ TMA producer
     int issued = 0;
     bool kv_issued = false;
-    if (n_all > 0) {
+    if (n_all > 0 && lane == 0 &&
+        !(CP_IN_RANGE(it.k_row0, 0, a.T, a.status, 301) && CP_IN_RANGE(hk, 0, a.Hkv, a.status, 302)))
+      *abort = 1;
+    if (n_all > 0 && !*abort) {
       if (lane == 0) {
         mbar_expect_tx(&bars->kv_full, 4 * L::kKVBox);
         for (int b = 0; b < 2; ++b) {
@@ -233,6 +237,13 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
         // box starts at the row rounded down to 4 (16-byte TMA alignment)
         const int row0 = q0 + t * kBQ;
         const int grow = sg.row0 + row0;
+        int c_ok = 1;
+        if (lane == 0)
+          c_ok = CP_IN_RANGE(grow, 0, a.T, a.status, 303) && CP_IN_RANGE(hq, 0, a.H, a.status, 304);
+        if (!__shfl_sync(0xffffffffu, c_ok, 0)) {
+          if (lane == 0) *abort = 1;
+          break;
+        }
         if (lane == 0) {
           mbar_expect_tx(&bars->qdo_full[st], 4 * L::kQBox + L::kLdBytes);
           for (int b = 0; b < 2; ++b) {
@@ -397,8 +408,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
           }
           // rows past the run carry exact zeros (P = 0 there); rows past T are
           // clipped by the tensor map
-          tma_reduce_add_3d(&a.tm_dq, smem + L::kStg + sb * L::kStgBytes, 0, hq,
-                            grow + r4 * L::kStgRows);
+          if (CP_IN_RANGE(grow, 0, a.T, a.status, 305) && CP_IN_RANGE(hq, 0, a.H, a.status, 306)) {
+            tma_reduce_add_3d(&a.tm_dq, smem + L::kStg + sb * L::kStgBytes, 0, hq,
+                              grow + r4 * L::kStgRows);
+          }
           bulk_commit();
           // free this round's buffer as soon as the reduce has read it, so the
           // staging warps can run up to N rounds ahead of this thread
@@ -533,9 +546,13 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
       tc_fence_after();
       // warpgroup 0 writes dK (scaled), warpgroup 1 writes dV
       float* dst;
+      bool row_ok = key_ok && CP_IN_RANGE(hk, 0, a.Hkv, a.status, 307);
       if (it.dk_mode == DK_TEXT) {
+        row_ok = row_ok && CP_IN_RANGE(it.k_row0 + u, 0, a.T, a.status, 308);
         dst = (g == 0 ? a.dk : a.dv) + ((long long)(it.k_row0 + u) * a.Hkv + hk) * kD;
       } else {
+        row_ok = row_ok && CP_IN_RANGE(it.slot, 0, a.n_slots, a.status, 309) &&
+                 CP_IN_RANGE(it.dk_row0 + u, 0, a.pre_rows, a.status, 310);
         const long long row = (long long)it.slot * a.pre_rows + it.dk_row0 + u;
         dst = (g == 0 ? a.pre_k : a.pre_v) + (row * a.Hkv + hk) * kD;
       }
@@ -553,7 +570,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
 #pragma unroll
           for (int x = 0; x < 32; ++x) r[x] = 0u;
         }
-        if (!key_ok) continue;
+        if (!row_ok) continue;
 #pragma unroll
         for (int x = 0; x < 32; x += 4) {
           float4 v = make_float4(__uint_as_float(r[x]) * mul, __uint_as_float(r[x + 1]) * mul,

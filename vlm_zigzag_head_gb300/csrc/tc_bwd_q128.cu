@@ -1,12 +1,14 @@
-// Ring-step attention backward on 5th-generation tensor cores (sm_103a), with
-// 128-query tiles so that every product is a 128 x 128 (x D) MMA.
+// Attention backward over all ring steps in one launch, on 5th-generation
+// tensor cores (sm_103a), with 128-query tiles so that every product is a
+// 128 x 128 (x D) MMA.
 //
-// One CTA owns one key tile (128 keys of one KV head) of a ring step and walks
-// the query runs that met those keys at that step, for every query head that
-// reads this KV head (page "context-parallel-multimodal" §4.2: each rank
-// differentiates its queries against the KV it saw; the KV owner receives
-// dK/dV; the replicated prefix gets one gradient per rank).  Per 128-row query
-// tile i, with the final lse:
+// One CTA owns one key tile (128 keys of one KV head) and walks, in ring-step
+// order, the query runs that meet those keys over all ring steps, for every
+// query head that reads this KV head (page "context-parallel-multimodal"
+// §4.2: each rank differentiates its queries against the KV it saw; the KV
+// owner receives dK/dV, here summed on chip over the steps and written once;
+// the replicated prefix gets one gradient per rank, one item per slot).  Per
+// 128-row query tile i, with the final lse:
 //
 //   S^T  = K Q^T          dP^T = V dO^T                          (TMEM)
 //   P^T  = exp2(S^T * scale*log2e - lse2),  dS^T = P^T (dP^T - D)  (registers)
@@ -47,6 +49,7 @@
 
 #include <type_traits>
 
+#include "check.cuh"
 #include "kernels.h"
 #include "ptx.cuh"
 #include "tc.h"
@@ -93,7 +96,8 @@ struct Lay {
   static constexpr int kLdBytes = 2 * kLdRows * 4;
   static constexpr int kLdStride = (kLdBytes + 127) / 128 * 128;
   static constexpr int kItem = kLd + kQStages * kLdStride;
-  static constexpr int kBars = kItem + 128;
+  static constexpr int kInfo = kItem + 128;                 // [stage] TileInfo of the Q tile
+  static constexpr int kBars = kInfo + kQStages * 32;
   static constexpr int kBytes = kBars + 256;
   static constexpr int kAlloc = kBytes + 1024;
   static_assert(kStg % 1024 == 0, "swizzled staging must be 1024-byte aligned");
@@ -101,6 +105,16 @@ struct Lay {
 };
 static_assert(Lay<128, false>::kAlloc <= 227 * 1024, "shared memory budget");
 static_assert(Lay<64, true>::kAlloc <= 227 * 1024, "shared memory budget");
+
+// What the P / dS warps need of a query tile, written by the Q producer
+// beside the tile (published by the same barrier as the Q load).
+struct TileInfo {
+  int32_t tile_row;   // natural row of the tile's first query
+  int32_t row_in;     // the same query's position inside its run
+  int32_t causal, delta, len;   // the run's visibility rule and length
+  int32_t pad[3];
+};
+static_assert(sizeof(TileInfo) == 32, "TileInfo layout");
 
 struct Bars {
   uint64_t kv_full;
@@ -124,19 +138,28 @@ __device__ __forceinline__ int run_qstart(const Seg& s) {
   return s.causal && s.delta < 0 ? -s.delta : 0;
 }
 
-// The g-th query tile of the item: its run, the run's first query and the
-// tile index inside the run.
-__device__ __forceinline__ void tile_of(const BwdItem& it, int g, Seg& sg, int& q0, int& t) {
-  for (int s = 0; s < it.nseg; ++s) {
-    const int nt = run_qtiles(it.seg[s]);
-    if (g < nt) {
-      sg = it.seg[s];
-      q0 = run_qstart(sg);
-      t = g;
-      return;
-    }
-    g -= nt;
+// Each role walks the item's query tiles in order: g advances by one, or
+// wraps to 0 for the next query head.  The walk keeps its current run and
+// the number of tiles before it, so finding the g-th tile (its run, the run's
+// first query and the tile index inside the run) costs one run read.
+struct TileWalk {
+  int s = 0, base = 0;
+};
+__device__ __forceinline__ void tile_of(const Seg* runs, int nseg, int g, TileWalk& w, Seg& sg,
+                                        int& q0, int& t) {
+  if (g < w.base) {
+    w.s = 0;
+    w.base = 0;
   }
+  sg = runs[w.s];
+  int nt = run_qtiles(sg);
+  while (g >= w.base + nt && w.s + 1 < nseg) {
+    w.base += nt;
+    sg = runs[++w.s];
+    nt = run_qtiles(sg);
+  }
+  q0 = run_qstart(sg);
+  t = g - w.base;
 }
 
 __device__ __forceinline__ void record_timeout(int32_t* status, volatile int* abort, int site) {
@@ -200,18 +223,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
-  // the next ring step's CTAs may take SMs as this step's CTAs finish; they
-  // wait for this grid before their dK / dV epilogue (griddep_wait below)
-  griddep_launch_dependents();
 
+  // the item's query runs, in ring-step order, from the plan's run list
   const int nseg = it.nseg;
+  const Seg* runs = a.runs + it.run0;
   int n_qt = 0;   // query tiles of one query head
-  for (int s = 0; s < nseg; ++s) n_qt += run_qtiles(it.seg[s]);
+  for (int s = 0; s < nseg; ++s) n_qt += run_qtiles(runs[s]);
   // Every role walks the same Gs * n_qt query tiles in the same order: query
   // head hq0 + j / n_qt, tile j % n_qt.  dK / dV of the KV head accumulate
-  // over all of them.  Concurrent CTAs are neighbouring key tiles that meet
-  // the same queries in the same order, so the Q / dO tiles they load are
-  // shared through L2.
+  // over all of them, across every ring step, and are written once.
+  // Concurrent CTAs are neighbouring key tiles that meet the same queries in
+  // the same order, so the Q / dO tiles they load are shared through L2.
   const int n_all = Gs * n_qt;
 
   if (warp < 4) {
@@ -221,7 +243,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) {
         int issued = 0;
         bool kv_issued = false;
-        if (n_all > 0) {
+        if (n_all > 0 && !(CP_IN_RANGE(it.k_row0, 0, a.T, a.status, 201) &&
+                           CP_IN_RANGE(hk, 0, a.Hkv, a.status, 202))) {
+          *abort = 1;
+        } else if (n_all > 0) {
           mbar_expect_tx(&bars->kv_full, 2 * L::kTile);
           for (int b = 0; b < D / 64; ++b) {
             tma_load_3d(&a.tm_k, &bars->kv_full, smem + L::kK + b * L::kBox, b * 64, hk, it.k_row0);
@@ -229,6 +254,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           kv_issued = true;
         }
+        TileWalk walk;
         int jt = 0, hq = hq0;
         for (int j = 0; j < n_all; ++j, jt = jt + 1 == n_qt ? 0 : jt + 1, hq += jt == 0) {
           const int st = j % kQStages;
@@ -239,8 +265,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           Seg sg;
           int q0, t;
-          tile_of(it, jt, sg, q0, t);
+          tile_of(runs, nseg, jt, walk, sg, q0, t);
           const int grow = sg.row0 + q0 + t * kBQ;   // natural row of the tile's first query
+          if (!CP_IN_RANGE(grow, 0, a.T, a.status, 203) || !CP_IN_RANGE(hq, 0, a.H, a.status, 204)) {
+            *abort = 1;
+            break;
+          }
+          TileInfo* info = reinterpret_cast<TileInfo*>(smem + L::kInfo) + st;
+          info->tile_row = grow;
+          info->row_in = q0 + t * kBQ;
+          info->causal = sg.causal;
+          info->delta = sg.delta;
+          info->len = sg.len;
           mbar_expect_tx(&bars->q_full[st], L::kTile + L::kLdBytes);
           for (int b = 0; b < D / 64; ++b)
             tma_load_3d(&a.tm_q, &bars->q_full[st], smem + L::kQ + st * L::kTile + b * L::kBox,
@@ -264,6 +300,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) {
         constexpr int S = L::kDOStages;
         int issued = 0;
+        TileWalk walk;
         int jt = 0, hq = hq0;
         for (int j = 0; j < n_all; ++j, jt = jt + 1 == n_qt ? 0 : jt + 1, hq += jt == 0) {
           const int st = j % S;
@@ -273,8 +310,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           Seg sg;
           int q0, t;
-          tile_of(it, jt, sg, q0, t);
+          tile_of(runs, nseg, jt, walk, sg, q0, t);
           const int grow = sg.row0 + q0 + t * kBQ;
+          if (!CP_IN_RANGE(grow, 0, a.T, a.status, 205) || !CP_IN_RANGE(hq, 0, a.H, a.status, 206)) {
+            *abort = 1;
+            break;
+          }
           mbar_expect_tx(&bars->do_full[st], L::kTile);
           for (int b = 0; b < D / 64; ++b)
             tma_load_3d(&a.tm_do, &bars->do_full[st], smem + L::kDO + st * L::kTile + b * L::kBox,
@@ -405,11 +446,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int sw = lane & 7;
     bool ok = true;
     bool pending = false;
+    TileWalk walk;
     int jt = 0, hq = hq0;
     for (int j = 0; ok && j < n_all; ++j, jt = jt + 1 == n_qt ? 0 : jt + 1, hq += jt == 0) {
       Seg sg;
       int q0, t;
-      tile_of(it, jt, sg, q0, t);
+      tile_of(runs, nseg, jt, walk, sg, q0, t);
       const int grow = sg.row0 + q0 + t * kBQ + wq * 32;   // natural row of this warp's first query
       if (!mbar_wait(&bars->dq_full, j & 1, lim, abort)) { ok = false; break; }
       tc_fence_after();
@@ -437,7 +479,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) {
+        if (lane == 0 && CP_IN_RANGE(grow - wq * 32, 0, a.T, a.status, 207) &&
+            CP_IN_RANGE(hq, 0, a.H, a.status, 208)) {
           tma_reduce_add_3d(&a.tm_dq, stg, c * 32, hq, grow);
           bulk_commit();
         }
@@ -458,10 +501,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool key_ok = u < it.k_len;
     const int sw = u & 7;
     bool ok = true;
-    for (int i = 0, jt = 0; ok && i < n_all; ++i, jt = jt + 1 == n_qt ? 0 : jt + 1) {
-      Seg sg;
-      int q0, t;
-      tile_of(it, jt, sg, q0, t);
+    for (int i = 0; ok && i < n_all; ++i) {
       const int st = i % kQStages;
       if (!mbar_wait(&bars->s_full, i & 1, lim, abort) ||
           !mbar_wait(&bars->q_full[st], (i / kQStages) & 1, lim, abort)) {
@@ -469,20 +509,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       tc_fence_after();
+      // the slot is rewritten only after this tile's dK product, which waits
+      // for this warpgroup's dS
+      const TileInfo ti = reinterpret_cast<const TileInfo*>(smem + L::kInfo)[st];
       uint32_t rs[2][32];
       tmem_ld32(tmem + lane_off + kColS + g * 64, rs[0]);
       tmem_ld32(tmem + lane_off + kColS + g * 64 + 32, rs[1]);
       tmem_ld_wait();
       reg_fence32(rs[0]);
       reg_fence32(rs[1]);
-      const int tile_row = sg.row0 + q0 + t * kBQ;          // natural row of the tile's first query
-      const int row0 = q0 + t * kBQ + g * 64;               // first query of this half (inside the run)
+      const int tile_row = ti.tile_row;                     // natural row of the tile's first query
+      const int row0 = ti.row_in + g * 64;                  // first query of this half (inside the run)
       const float* ld = reinterpret_cast<const float*>(smem + L::kLd + st * L::kLdStride) +
                         (tile_row & 3) + g * 64;
       // key u is visible to query row0 + x iff x < len - row0 and, for a causal
       // run, u <= row0 + x + delta
-      const int first_vis = sg.causal ? u - sg.delta - row0 : 0;
-      const int end_vis = key_ok ? sg.len - row0 : 0;
+      const int first_vis = ti.causal ? u - ti.delta - row0 : 0;
+      const int end_vis = key_ok ? ti.len - row0 : 0;
       const bool whole = __all_sync(0xffffffffu, first_vis <= 0 && end_vis >= 64);
       const bool vec = (tile_row & 3) == 0;
       // ---- P^T: probabilities of the 64 queries, computed in place over S and
@@ -573,18 +616,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     // ------------------------------------------------------------ dK / dV epilogue
     if (ok && n_all > 0 && !mbar_wait(&bars->dkv_done, 0, lim, abort)) ok = false;
-    // dK / dV rows accumulate over ring steps: the previous step's grid must
-    // be complete (a no-op unless launched as a programmatic dependent)
-    griddep_wait();
     if (!ok) {
       record_timeout(a.status, abort, 25);
     } else {
       tc_fence_after();
       // warpgroup 0 writes dK (scaled), warpgroup 1 writes dV
       float* dst;
+      bool row_ok = key_ok && CP_IN_RANGE(hk, 0, a.Hkv, a.status, 209);
       if (it.dk_mode == DK_TEXT) {
+        row_ok = row_ok && CP_IN_RANGE(it.k_row0 + u, 0, a.T, a.status, 210);
         dst = (g == 0 ? a.dk : a.dv) + ((long long)(it.k_row0 + u) * a.Hkv + hk) * D;
       } else {
+        row_ok = row_ok && CP_IN_RANGE(it.slot, 0, a.n_slots, a.status, 211) &&
+                 CP_IN_RANGE(it.dk_row0 + u, 0, a.pre_rows, a.status, 212);
         const long long row = (long long)it.slot * a.pre_rows + it.dk_row0 + u;
         dst = (g == 0 ? a.pre_k : a.pre_v) + (row * a.Hkv + hk) * D;
       }
@@ -602,7 +646,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int x = 0; x < 32; ++x) r[x] = 0u;
         }
-        if (!key_ok) continue;
+        if (!row_ok) continue;
 #pragma unroll
         for (int x = 0; x < 32; x += 4) {
           float4 v = make_float4(__uint_as_float(r[x]) * mul, __uint_as_float(r[x + 1]) * mul,
@@ -637,23 +681,15 @@ cudaError_t launch_q128(const TcBwdArgs& a, cudaStream_t st) {
   if (e != cudaSuccess) return e;
   const long long blocks = (long long)a.n_items * a.Hkv * a.kv_split;
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)blocks);
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = a.pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, tc_bwd_q128_kernel<D, kSplit, kShared>, a);
+  tc_bwd_q128_kernel<D, kSplit, kShared><<<(unsigned)blocks, kThreads, smem, st>>>(a);
+  return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_tc_bwd_q128(const TcBwdArgs& a, cudaStream_t st) {
   if (a.n_items == 0) return cudaSuccess;
+  if (a.runs == nullptr) return cudaErrorInvalidValue;   // all-steps items only
   if (a.kv_split < 1 || (a.H / a.Hkv) % a.kv_split != 0) return cudaErrorInvalidValue;
   const bool split = a.scale > kPrecisionSplitScale;
   if (a.d == 128) {

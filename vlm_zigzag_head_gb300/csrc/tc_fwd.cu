@@ -40,6 +40,7 @@
 // swizzled layout TMA writes, 1024-byte aligned.
 #include <cuda_bf16.h>
 
+#include "check.cuh"
 #include "kernels.h"
 #include "ptx.cuh"
 #include "tc.h"
@@ -195,10 +196,16 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
       const UnitRange ur = cta_units(a);
       for (int u = ur.begin; u < ur.end && !*abort; u += ur.step) {
         const int uid = unit_id(a, u);
+        if (!CP_IN_RANGE(uid, 0, (long long)a.n_items * a.H, a.status, 101)) { *abort = 1; break; }
         const FwdItem& it = a.items[uid % a.n_items];
         const int hk = (uid / a.n_items) / G;
         for (int s = 0; s < it.nseg && !*abort; ++s) {
           const Seg sg = item_seg(a, it, s);
+          if (!CP_IN_RANGE(sg.row0, 0, sg.src == SRC_TEXT ? a.text_rows : a.T, a.status, 102) ||
+              !CP_IN_RANGE(hk, 0, a.Hkv, a.status, 103)) {
+            *abort = 1;
+            break;
+          }
           const CUtensorMap* m = is_k ? (sg.src == SRC_TEXT ? &a.tm_k_text : &a.tm_k_nat)
                                       : (sg.src == SRC_TEXT ? &a.tm_v_text : &a.tm_v_nat);
           const int nt = run_tiles(sg, it.q_len);
@@ -240,6 +247,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
         if (item_tiles(a, it) == 0) continue;
         if (n > 0 && !mbar_wait(&bars->q_empty, (n - 1) & 1, lim, abort)) {
           record_timeout(a.status, abort, 6);
+          break;
+        }
+        if (!CP_IN_RANGE(it.q_row0, 0, it.q_src == SRC_TEXT ? a.text_rows : a.T, a.status, 104) ||
+            !CP_IN_RANGE(uid / a.n_items, 0, a.H, a.status, 105)) {
+          *abort = 1;
           break;
         }
         const CUtensorMap* qm = it.q_src == SRC_TEXT ? &a.tm_q_text : &a.tm_q_nat;
@@ -486,7 +498,14 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
     }
     {
       tc_fence_after();
-      const bool valid = tq < q_len;
+      bool valid = tq < q_len;
+      if (valid && (it.flags & F_FINAL) &&
+          !(CP_IN_RANGE(it.out_row0 + tq, 0, a.T, a.status, 106) &&
+            CP_IN_RANGE(h, 0, a.H, a.status, 107)))
+        valid = false;   // checked build: the row is skipped
+      if (valid && it.run_row0 >= 0 && a.runs == nullptr &&
+          !CP_IN_RANGE(it.run_row0 + tq, 0, a.run_rows, a.status, 108))
+        valid = false;
       float lse_s = l > 0.f ? (m + __log2f(l)) * 0.6931471805599453f : -INFINITY;
       const float inv = l > 0.f ? 1.f / l : 0.f;
       const int flags = it.flags;
