@@ -41,7 +41,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # tensor-core backward on the named workload, from one ncu capture of this
 # kernel (scaled from a smaller case where stated).  An entry is removed when
 # the kernel changes, until it is captured again.
-MEASURED_TRAFFIC = {}
+MEASURED_TRAFFIC = {"long": 26.99e9}
 EX2_PER_CLK_SM = 32.0   # MUFU exp2 results per clock per SM (31.8 measured by a throughput loop)
 # every bf16 forward + backward workload of the method; the default line's
 # `value` is the 128K one, the others are reported under `workloads`
@@ -347,7 +347,7 @@ def run_cuda(args, w, rank, world, dist):
                 "achieved": ach, "peak": peak_sus, "unit": "TFLOP/s", "frac": ach / peak_sus,
                 "peak_source": "%s bf16_tflops_sustained" % peak_src,
                 "traffic": (args.traffic if args.traffic is not None
-                            else MEASURED_TRAFFIC.get(w.name) if w.kv_heads == w.H else None),
+                            else MEASURED_TRAFFIC.get(w.name) if w == W.get(w.name) else None),
                 "launch_ms": avg,
                 "flops_per_launch": bwd_launch_flops}
     kernels = {}
@@ -459,6 +459,8 @@ def main():
     ap.add_argument("--workload", default="long", choices=sorted(W.WORKLOADS))
     ap.add_argument("--kv-heads", type=int, default=0,
                     help="KV heads for grouped-query attention (default: as many as query heads)")
+    ap.add_argument("--text-len", type=int, default=0,
+                    help="text tokens of a one-sample workload (smaller profiling cases)")
     ap.add_argument("--oracle-queries", type=int, default=32768)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -469,7 +471,14 @@ def main():
     ap.add_argument("--traffic", type=float, default=None,
                     help="DRAM bytes per launch of the dominant kernel from an ncu capture")
     args = ap.parse_args()
-    w = W.get(args.workload, H_kv=args.kv_heads) if args.kv_heads else W.get(args.workload)
+    over = {}
+    if args.kv_heads:
+        over["H_kv"] = args.kv_heads
+    if args.text_len:
+        if W.get(args.workload).n_seqs != 1:
+            raise SystemExit("--text-len applies to one-sample workloads")
+        over["text_lens"] = (args.text_len,)
+    w = W.get(args.workload, **over)
     if w.dtype != "bf16" or not w.backward:
         raise SystemExit("bench workloads are the bf16 forward+backward ones")
     world = int(os.environ.get("WORLD_SIZE", "1"))
