@@ -330,20 +330,15 @@ def run_cuda(args, w, rank, world, dist):
                                           workspace=ws_b, grads=grads, out_lo=out_lo), n_sub)
 
     # dominant kernel: the tensor-core backward (algorithmic FLOPs: 10 d per
-    # visible pair and head).  With 128-query tiles one launch covers every
-    # ring step of a call; with 64-query tiles (head_dim 128, softmax scale
-    # above 0.25) there are P ring-step launches, which share the call's FLOPs
+    # visible pair and head), one launch over every ring step of a call
     bwd_ms_k, bwd_launches = prof["tc_bwd_step"]
     fwd_ms_k, fwd_launches = prof["tc_fwd_step"]
-    bwd_per_call = max(1, bwd_launches // max(1, args.steps))
-    bwd_launch_flops = 2.5 * f_flops / bwd_per_call
+    bwd_launch_flops = 2.5 * f_flops
     roof = None
     if bwd_launches:
         avg = bwd_ms_k / bwd_launches
         ach = bwd_launch_flops / (avg / 1e3) / 1e12
-        name = ("tc_bwd_q128_kernel (all ring steps)" if bwd_per_call == 1
-                else "tc_bwd_kernel (backward ring step)")
-        roof = {"kernel": name, "bound": "tensor",
+        roof = {"kernel": "tc_bwd_q128_kernel (all ring steps)", "bound": "tensor",
                 "achieved": ach, "peak": peak_sus, "unit": "TFLOP/s", "frac": ach / peak_sus,
                 "peak_source": "%s bf16_tflops_sustained" % peak_src,
                 "traffic": (args.traffic if args.traffic is not None

@@ -150,14 +150,25 @@ cp_status_t cp_zigzag_scatter(const void* src, void* dst, size_t row_bytes, cons
  *   out_lo     NULL, or (CP_BF16 only) [T][H][d] bf16: receives the rounding
  *              remainder o - out of the fp32 result o, so that out + out_lo
  *              carries o to about 16 bits.  Pass it to cp_attn_bwd.
- *   workspace  >= cp_attn_fwd_workspace_size(...) bytes, 256-byte aligned
+ *   workspace  >= cp_attn_fwd_workspace_size(...) bytes, 256-byte aligned;
+ *              the size depends on softmax_scale (below)
+ *
+ * Softmax scales above 0.25 (e.g. scale 1 on queries that carry 1/sqrt(d)
+ * already) make dQ large enough that one bf16 rounding of the probabilities
+ * shows in it.  There the CP_BF16 path runs the products that take a
+ * probability-sized operand on f16 operands (three more mantissa bits): in
+ * this call P V, with V replaced by a per-call f16 copy V * 2^-e whose
+ * largest magnitude lies in [2^14, 2^15), e a power of two found on the
+ * device (|e| <= 60); O is multiplied back by 2^e in fp32.  The scaling is
+ * exact, so the copy loses nothing for values within 2^29 of the largest.
+ * The workspace then also holds that copy (T x H_kv x d x 2 bytes).
  * Errors: CP_ERR_INVALID_ARG, CP_ERR_SHAPE, CP_ERR_DTYPE, CP_ERR_ALIGNMENT,
  * CP_ERR_WORKSPACE, CP_ERR_CUDA, CP_ERR_UNSUPPORTED (CP_BF16 on a device
  * without tcgen05).  T == 0 is a no-op returning CP_OK.
  */
 size_t cp_attn_fwd_workspace_size(cp_dtype_t dt, int T, int H, int d,
                                   const int32_t* cu_seqlens_h, int n_seqs, int P,
-                                  int prefix_len);
+                                  int prefix_len, float softmax_scale);
 cp_status_t cp_attn_fwd(const void* q, const void* k, const void* v, cp_dtype_t dt, int T,
                         int H, int d, const int32_t* cu_seqlens_h, int n_seqs, int P,
                         int prefix_len, float softmax_scale, void* out, float* lse,
@@ -182,6 +193,7 @@ cp_status_t cp_attn_fwd(const void* q, const void* k, const void* v, cp_dtype_t 
  *    the zigzag table and the rank-local q/k/v: 3 x rows x H x d x 2 bytes,
  *    rows = text tokens.  At d = 128 that is 768 bytes per (text token, head),
  *    so about 85 000 (token, head) pairs, e.g. 8192 tokens with 10 heads.
+ *    Above softmax scale 0.25 the f16 copy of v adds 2 x T x H x d bytes.
  *    CP_F32 merges its ring steps through an fp32 running result held in the
  *    scratch as well (about 1.6 KB per pair at d = 128).  Larger problems
  *    return CP_ERR_WORKSPACE with the number of bytes they would need.
@@ -240,12 +252,17 @@ cp_status_t cp_lse_merge(int n_parts, const float* part_out, const float* part_l
  *   prefix_grad_per_rank  NULL, or [2][P+1][n_seqs*prefix_len][H][d] fp32:
  *                       receives the per-rank prefix dK (slot 0) and dV
  *                       (slot 1) before the sum; index P = prefix-query term.
- *   workspace           >= cp_attn_bwd_workspace_size(...) bytes
+ *   workspace           >= cp_attn_bwd_workspace_size(...) bytes; above
+ *                       softmax scale 0.25 it also holds f16 copies of q and k
+ *                       (scaled as V in cp_attn_fwd): the products S = Q K^T,
+ *                       dQ = dS K and dK = dS^T Q then run on f16 operands,
+ *                       dS rounded to f16 after a power-of-two scaling that
+ *                       bounds it by 2^15 (from max |v| and max |dout|)
  * Errors: as cp_attn_fwd.
  */
 size_t cp_attn_bwd_workspace_size(cp_dtype_t dt, int T, int H, int d,
                                   const int32_t* cu_seqlens_h, int n_seqs, int P,
-                                  int prefix_len);
+                                  int prefix_len, float softmax_scale);
 cp_status_t cp_attn_bwd(const void* q, const void* k, const void* v, const void* out,
                         const void* out_lo, const float* lse, const void* dout, cp_dtype_t dt,
                         int T, int H, int d,
@@ -275,14 +292,14 @@ cp_status_t cp_attn_bwd(const void* q, const void* k, const void* v, const void*
  */
 size_t cp_attn_fwd_workspace_size_gqa(cp_dtype_t dt, int T, int H, int H_kv, int d,
                                       const int32_t* cu_seqlens_h, int n_seqs, int P,
-                                      int prefix_len);
+                                      int prefix_len, float softmax_scale);
 cp_status_t cp_attn_fwd_gqa(const void* q, const void* k, const void* v, cp_dtype_t dt, int T,
                             int H, int H_kv, int d, const int32_t* cu_seqlens_h, int n_seqs,
                             int P, int prefix_len, float softmax_scale, void* out, float* lse,
                             void* out_lo, void* workspace, size_t ws_bytes, void* stream);
 size_t cp_attn_bwd_workspace_size_gqa(cp_dtype_t dt, int T, int H, int H_kv, int d,
                                       const int32_t* cu_seqlens_h, int n_seqs, int P,
-                                      int prefix_len);
+                                      int prefix_len, float softmax_scale);
 cp_status_t cp_attn_bwd_gqa(const void* q, const void* k, const void* v, const void* out,
                             const void* out_lo, const float* lse, const void* dout,
                             cp_dtype_t dt, int T, int H, int H_kv, int d,
@@ -347,9 +364,10 @@ cp_status_t cp_plan_unit_lists(const int32_t* cu_seqlens_h, int n_seqs, int pref
  * launch covering all ring steps; with CPATTN_FWD_PER_STEP=1 in the
  * environment it is P ring-step launches, which overlap one another's tails
  * and share one pair that counts as P launches.  The tensor-core backward is
- * one launch covering all ring steps with 128-query tiles; with 64-query
- * tiles (head_dim 128 with softmax scale above 0.25) it is P ring-step
- * launches counted the same way.  cp_profile_end synchronises those events and returns, per
+ * one launch covering all ring steps.  Above softmax scale 0.25 the f16
+ * operand copies are made inside the gather (forward) and preprocess
+ * (backward) pairs, which then count 3 launches each.  cp_profile_end
+ * synchronises those events and returns, per
  * kernel kind, the summed milliseconds and the launch count in ms[8] /
  * launches[8] (either may be NULL):
  *   0 zigzag index   1 zigzag gather   2 tensor-core forward (ring steps)

@@ -105,8 +105,8 @@ def test_bad_arguments_return_status(cplib):
     assert L.cp_zigzag_index(None, 1, 0, 2, None, None, 0, None) == 1
     assert L.cp_zigzag_index(cu, 1, 0, 0, None, None, 0, None) == 1       # P < 1
     assert L.cp_zigzag_index(B.cu_array([0, 3]), 1, 4, 1, None, None, 0, None) == 2  # prefix > len
-    assert L.cp_attn_fwd_workspace_size(1, 10, 1, 64, cu, 1, 2, 0) == 0
-    assert L.cp_attn_fwd_workspace_size(1, 8, 1, 64, B.cu_array([0, 8]), 1, 2, 0) > 0
+    assert L.cp_attn_fwd_workspace_size(1, 10, 1, 64, cu, 1, 2, 0, 0.1) == 0
+    assert L.cp_attn_fwd_workspace_size(1, 8, 1, 64, B.cu_array([0, 8]), 1, 2, 0, 0.1) > 0
     # d not in {64,128}, wrong dtype, null tensors, misaligned pointers
     cu8 = B.cu_array([0, 8])
     fake = ctypes.c_void_p(1 << 20)
@@ -131,14 +131,14 @@ def test_grouped_kv_arguments(cplib):
     calls."""
     L = cplib
     cu = B.cu_array([0, 16])
-    assert L.cp_attn_fwd_workspace_size_gqa(1, 16, 6, 4, 128, cu, 1, 2, 0) == 0
-    assert L.cp_attn_bwd_workspace_size_gqa(1, 16, 4, 0, 128, cu, 1, 2, 0) == 0
-    assert L.cp_attn_fwd_workspace_size_gqa(1, 16, 8, 8, 128, cu, 1, 2, 0) == \
-        L.cp_attn_fwd_workspace_size(1, 16, 8, 128, cu, 1, 2, 0)
-    assert L.cp_attn_bwd_workspace_size_gqa(0, 16, 8, 8, 64, cu, 1, 2, 0) == \
-        L.cp_attn_bwd_workspace_size(0, 16, 8, 64, cu, 1, 2, 0)
-    assert 0 < L.cp_attn_fwd_workspace_size_gqa(1, 16, 8, 2, 128, cu, 1, 2, 0) < \
-        L.cp_attn_fwd_workspace_size_gqa(1, 16, 8, 8, 128, cu, 1, 2, 0)
+    assert L.cp_attn_fwd_workspace_size_gqa(1, 16, 6, 4, 128, cu, 1, 2, 0, 0.1) == 0
+    assert L.cp_attn_bwd_workspace_size_gqa(1, 16, 4, 0, 128, cu, 1, 2, 0, 0.1) == 0
+    assert L.cp_attn_fwd_workspace_size_gqa(1, 16, 8, 8, 128, cu, 1, 2, 0, 0.1) == \
+        L.cp_attn_fwd_workspace_size(1, 16, 8, 128, cu, 1, 2, 0, 0.1)
+    assert L.cp_attn_bwd_workspace_size_gqa(0, 16, 8, 8, 64, cu, 1, 2, 0, 0.1) == \
+        L.cp_attn_bwd_workspace_size(0, 16, 8, 64, cu, 1, 2, 0, 0.1)
+    assert 0 < L.cp_attn_fwd_workspace_size_gqa(1, 16, 8, 2, 128, cu, 1, 2, 0, 0.1) < \
+        L.cp_attn_fwd_workspace_size_gqa(1, 16, 8, 8, 128, cu, 1, 2, 0, 0.1)
     fake = ctypes.c_void_p(1 << 20)
     st = L.cp_attn_fwd_gqa(fake, fake, fake, 1, 16, 6, 4, 128, cu, 1, 2, 0, 1.0, fake, fake,
                            None, fake, 1 << 20, None)
@@ -157,9 +157,24 @@ def test_forward_workspace_is_sized_by_schedule(cplib):
     L = cplib
     rows, H, d = 4096, 8, 128
     cu = B.cu_array([0, rows])
-    ws_bf16 = L.cp_attn_fwd_workspace_size(1, rows, H, d, cu, 1, 2, 0)
-    ws_f32 = L.cp_attn_fwd_workspace_size(0, rows, H, d, cu, 1, 2, 0)
+    ws_bf16 = L.cp_attn_fwd_workspace_size(1, rows, H, d, cu, 1, 2, 0, 0.1)
+    ws_f32 = L.cp_attn_fwd_workspace_size(0, rows, H, d, cu, 1, 2, 0, 0.1)
     qkv_bf16, qkv_f32 = 3 * rows * H * d * 2, 3 * rows * H * d * 4
     running = rows * H * (d + 1) * 4
     assert qkv_bf16 <= ws_bf16 < qkv_bf16 + running // 4
     assert ws_f32 >= qkv_f32 + running
+
+
+def test_f16_operand_copies_are_sized_by_softmax_scale(cplib):
+    """Above softmax scale 0.25 the bf16 forward keeps an f16 copy of V and the
+    backward f16 copies of Q and K (plus one 256-byte block of factors); at or
+    below it, and for fp32, nothing is added."""
+    L = cplib
+    rows, H, Hkv, d = 4096, 8, 2, 128
+    cu = B.cu_array([0, rows])
+    f = lambda dt, sc: L.cp_attn_fwd_workspace_size_gqa(dt, rows, H, Hkv, d, cu, 1, 2, 0, sc)  # noqa: E731
+    b = lambda dt, sc: L.cp_attn_bwd_workspace_size_gqa(dt, rows, H, Hkv, d, cu, 1, 2, 0, sc)  # noqa: E731
+    assert f(1, 0.25) == f(1, 0.088) and b(1, 0.25) == b(1, 0.088)
+    assert f(1, 1.0) - f(1, 0.25) == 256 + rows * Hkv * d * 2
+    assert b(1, 1.0) - b(1, 0.25) == 256 + rows * (H + Hkv) * d * 2
+    assert f(0, 1.0) == f(0, 0.1) and b(0, 1.0) == b(0, 0.1)

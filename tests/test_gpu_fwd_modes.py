@@ -51,7 +51,7 @@ def _cu(prefix, texts):
 CASES = [
     # (P, prefix, texts, H, scale, q_mul)
     (1, 0, [512], 2, 128 ** -0.5, 1.0),                 # one ring step
-    (2, 0, [2048], 4, 1.0, 128 ** -0.5),                # text, P split into hi + lo
+    (2, 0, [2048], 4, 1.0, 128 ** -0.5),                # text, scale 1: PV on f16 operands
     (4, 576, [1536, 512, 0], 2, 128 ** -0.5, 1.0),      # prefix, packed, text-less sample
     (8, 0, [4096], 2, 128 ** -0.5, 1.0),                # P = 8: 15 key runs per tile
     (3, 37, [384, 1152], 3, 128 ** -0.5, 1.0),          # ragged chunks (c = 64, 192)

@@ -63,10 +63,10 @@ CASES = [
     # (P, prefix, texts, H, H_kv, d, dtype, scale, q_mul)
     (2, 0, [2048], 8, 2, 128, torch.bfloat16, 128 ** -0.5, 1.0),        # text, G = 4
     (4, 192, [1024, 512], 8, 1, 128, torch.bfloat16, 128 ** -0.5, 1.0),  # MQA, prefix, packed
-    (3, 37, [384, 0, 1152], 6, 3, 128, torch.bfloat16, 1.0, 128 ** -0.5),  # dS hi+lo path
+    (3, 37, [384, 0, 1152], 6, 3, 128, torch.bfloat16, 1.0, 128 ** -0.5),  # scale 1: f16 operands
     (2, 5, [256, 128], 4, 2, 64, torch.bfloat16, 0.125, 1.0),            # d = 64
-    (3, 37, [384, 0, 768], 4, 2, 64, torch.bfloat16, 1.0, 64 ** -0.5),   # d = 64, dS hi+lo
-    (2, 0, [1024], 2, 2, 64, torch.bfloat16, 1.0, 64 ** -0.5),           # d = 64, dS hi+lo, MHA
+    (3, 37, [384, 0, 768], 4, 2, 64, torch.bfloat16, 1.0, 64 ** -0.5),   # d = 64, scale 1
+    (2, 0, [1024], 2, 2, 64, torch.bfloat16, 1.0, 64 ** -0.5),           # d = 64, scale 1, MHA
     (2, 5, [64, 32], 4, 2, 64, torch.float32, 0.125, 1.0),               # fp32 CUDA-core path
 ]
 

@@ -167,14 +167,16 @@ def _attn_fwd(q, k, v, cu_seqlens, P, prefix_len, softmax_scale, out, lse, works
     n = len(cu_seqlens) - 1
     L = _b.lib()
     if gqa:
-        nbytes = L.cp_attn_fwd_workspace_size_gqa(dt, T, H, Hkv, d, cu, n, P, prefix_len)
+        nbytes = L.cp_attn_fwd_workspace_size_gqa(dt, T, H, Hkv, d, cu, n, P, prefix_len,
+                                                  float(softmax_scale))
 
         def run(ws_ptr, ws_bytes):
             return L.cp_attn_fwd_gqa(_ptr(q), _ptr(k), _ptr(v), dt, T, H, Hkv, d, cu, n, P,
                                      prefix_len, float(softmax_scale), _ptr(out), _ptr(lse),
                                      _ptr(out_lo), ws_ptr, ws_bytes, _stream(q.device))
     else:
-        nbytes = L.cp_attn_fwd_workspace_size(dt, T, H, d, cu, n, P, prefix_len)
+        nbytes = L.cp_attn_fwd_workspace_size(dt, T, H, d, cu, n, P, prefix_len,
+                                              float(softmax_scale))
 
         def run(ws_ptr, ws_bytes):
             return L.cp_attn_fwd(_ptr(q), _ptr(k), _ptr(v), dt, T, H, d, cu, n, P, prefix_len,
@@ -265,7 +267,8 @@ def _attn_bwd(q, k, v, out, lse, dout, cu_seqlens, P, prefix_len, softmax_scale,
     cu = _b.cu_array(cu_seqlens)
     L = _b.lib()
     if gqa:
-        nbytes = L.cp_attn_bwd_workspace_size_gqa(dt, T, H, Hkv, d, cu, n, P, prefix_len)
+        nbytes = L.cp_attn_bwd_workspace_size_gqa(dt, T, H, Hkv, d, cu, n, P, prefix_len,
+                                                  float(softmax_scale))
 
         def run(ws_ptr, ws_bytes):
             return L.cp_attn_bwd_gqa(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(out_lo),
@@ -273,7 +276,8 @@ def _attn_bwd(q, k, v, out, lse, dout, cu_seqlens, P, prefix_len, softmax_scale,
                                      prefix_len, float(softmax_scale), _ptr(dq), _ptr(dk),
                                      _ptr(dv), _ptr(pgrad), ws_ptr, ws_bytes, _stream(q.device))
     else:
-        nbytes = L.cp_attn_bwd_workspace_size(dt, T, H, d, cu, n, P, prefix_len)
+        nbytes = L.cp_attn_bwd_workspace_size(dt, T, H, d, cu, n, P, prefix_len,
+                                              float(softmax_scale))
 
         def run(ws_ptr, ws_bytes):
             return L.cp_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(out_lo), _ptr(lse),

@@ -38,7 +38,7 @@ SIGNATURES = {
     "cp_zigzag_scatter": (ctypes.c_int, [c_vp, c_vp, ctypes.c_size_t, c_vp, ctypes.c_int, c_vp]),
     "cp_attn_fwd_workspace_size": (ctypes.c_size_t, [ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                                      ctypes.c_int, c_i32p, ctypes.c_int,
-                                                     ctypes.c_int, ctypes.c_int]),
+                                                     ctypes.c_int, ctypes.c_int, ctypes.c_float]),
     "cp_attn_fwd": (ctypes.c_int, [c_vp, c_vp, c_vp, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                    ctypes.c_int, c_i32p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                    ctypes.c_float, c_vp, c_vp, c_vp, c_vp, ctypes.c_size_t,
@@ -50,7 +50,7 @@ SIGNATURES = {
     "cp_attn_fwd_workspace_size_gqa": (ctypes.c_size_t, [ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                                          ctypes.c_int, ctypes.c_int, c_i32p,
                                                          ctypes.c_int, ctypes.c_int,
-                                                         ctypes.c_int]),
+                                                         ctypes.c_int, ctypes.c_float]),
     "cp_attn_fwd_gqa": (ctypes.c_int, [c_vp, c_vp, c_vp, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                        ctypes.c_int, ctypes.c_int, c_i32p, ctypes.c_int,
                                        ctypes.c_int, ctypes.c_int, ctypes.c_float, c_vp, c_vp,
@@ -58,7 +58,7 @@ SIGNATURES = {
     "cp_attn_bwd_workspace_size_gqa": (ctypes.c_size_t, [ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                                          ctypes.c_int, ctypes.c_int, c_i32p,
                                                          ctypes.c_int, ctypes.c_int,
-                                                         ctypes.c_int]),
+                                                         ctypes.c_int, ctypes.c_float]),
     "cp_attn_bwd_gqa": (ctypes.c_int, [c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, ctypes.c_int,
                                        ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                        c_i32p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
@@ -68,7 +68,7 @@ SIGNATURES = {
                                     ctypes.c_int, c_vp, ctypes.c_int, c_vp, c_vp]),
     "cp_attn_bwd_workspace_size": (ctypes.c_size_t, [ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                                      ctypes.c_int, c_i32p, ctypes.c_int,
-                                                     ctypes.c_int, ctypes.c_int]),
+                                                     ctypes.c_int, ctypes.c_int, ctypes.c_float]),
     "cp_attn_bwd": (ctypes.c_int, [c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, ctypes.c_int,
                                    ctypes.c_int,
                                    ctypes.c_int, ctypes.c_int, c_i32p, ctypes.c_int, ctypes.c_int,

@@ -203,14 +203,15 @@ cp_status_t get_plans(const int32_t* cu, int n_seqs, int N, int P, int T, int H,
 // ---------------------------------------------------------------------------
 struct FwdWs {
   size_t status = 0, items = 0, runs = 0, units = 0, idx = 0, qkv[3] = {0, 0, 0},
-         o_run = 0, lse_run = 0, total = 0;
+         o_run = 0, lse_run = 0, scales = 0, v16 = 0, total = 0;
 };
 
 // `running`: reserve the fp32 running result (o_run, lse_run) that the
 // per-step schedules merge into (fp32 inputs, or bf16 under
 // CPATTN_FWD_PER_STEP=1).  The default all-steps tensor-core forward keeps its
 // merge on chip and needs none.
-FwdWs fwd_layout(const PlanSet& ps, int H, int Hkv, int d, size_t elem, bool running) {
+// `f16`: the f16 copy of V and its factors (bf16 above softmax scale 0.25).
+FwdWs fwd_layout(const PlanSet& ps, int H, int Hkv, int d, size_t elem, bool running, bool f16) {
   FwdWs w;
   size_t o = 0;
   w.status = o; o += kStatusBytes;
@@ -229,18 +230,24 @@ FwdWs fwd_layout(const PlanSet& ps, int H, int Hkv, int d, size_t elem, bool run
   if (running) o = align_up(o + (size_t)ps.pb.text_rows * H * d * sizeof(float), 256);
   w.lse_run = o;
   if (running) o = align_up(o + (size_t)ps.pb.text_rows * H * sizeof(float), 256);
+  w.scales = o;
+  if (f16) o = align_up(o + sizeof(OpScales), 256);
+  w.v16 = o;
+  if (f16) o = align_up(o + (size_t)ps.pb.T * Hkv * d * 2, 256);
   w.total = o;
   return w;
 }
 
 struct BwdWs {
   size_t status = 0, items = 0, runs = 0, qitems = 0, cu = 0, D = 0, lse2 = 0, slots = 0,
-         total = 0;
+         scales = 0, q16 = 0, k16 = 0, total = 0;
 };
 
 inline int64_t ld_pitch(int64_t T) { return (T + 3) / 4 * 4; }
 
-BwdWs bwd_layout(const PlanSet& ps, int H, int Hkv, int d, bool simt, bool own_slots) {
+// `f16`: the f16 copies of Q and K and their factors (bf16 above softmax
+// scale 0.25).
+BwdWs bwd_layout(const PlanSet& ps, int H, int Hkv, int d, bool simt, bool own_slots, bool f16) {
   BwdWs w;
   const Problem& pb = ps.pb;
   size_t o = 0;
@@ -259,6 +266,12 @@ BwdWs bwd_layout(const PlanSet& ps, int H, int Hkv, int d, bool simt, bool own_s
   w.slots = o;
   if (own_slots)
     o = align_up(o + 2ull * (pb.P + 1) * pb.n_seqs * pb.N * Hkv * d * sizeof(float), 256);
+  w.scales = o;
+  if (f16) o = align_up(o + sizeof(OpScales), 256);
+  w.q16 = o;
+  if (f16) o = align_up(o + (size_t)pb.T * H * d * 2, 256);
+  w.k16 = o;
+  if (f16) o = align_up(o + (size_t)pb.T * Hkv * d * 2, 256);
   w.total = o;
   return w;
 }
@@ -435,16 +448,17 @@ cp_status_t cp_zigzag_scatter(const void* src, void* dst, size_t row_bytes, cons
 }
 
 size_t cp_attn_fwd_workspace_size_gqa(cp_dtype_t dt, int T, int H, int Hkv, int d,
-                                      const int32_t* cu, int n_seqs, int P, int N) {
+                                      const int32_t* cu, int n_seqs, int P, int N, float scale) {
   std::shared_ptr<PlanSet> ps;
   if (!cu || H < 1 || Hkv < 1 || H % Hkv != 0 || (dt != CP_F32 && dt != CP_BF16)) return 0;
   if (get_plans(cu, n_seqs, N, P, T, H, d, &ps) != CP_OK) return 0;
-  return fwd_layout(*ps, H, Hkv, d, dt == CP_BF16 ? 2 : 4, fwd_needs_running(dt)).total;
+  const bool f16 = dt == CP_BF16 && uses_f16_operands(scale);
+  return fwd_layout(*ps, H, Hkv, d, dt == CP_BF16 ? 2 : 4, fwd_needs_running(dt), f16).total;
 }
 
 size_t cp_attn_fwd_workspace_size(cp_dtype_t dt, int T, int H, int d, const int32_t* cu,
-                                  int n_seqs, int P, int N) {
-  return cp_attn_fwd_workspace_size_gqa(dt, T, H, H, d, cu, n_seqs, P, N);
+                                  int n_seqs, int P, int N, float scale) {
+  return cp_attn_fwd_workspace_size_gqa(dt, T, H, H, d, cu, n_seqs, P, N, scale);
 }
 
 cp_status_t cp_attn_fwd(const void* q, const void* k, const void* v, cp_dtype_t dt, int T, int H,
@@ -472,7 +486,8 @@ cp_status_t cp_attn_fwd_gqa(const void* q, const void* k, const void* v, cp_dtyp
   const bool tc = bf16;   // bf16: tensor cores; fp32: the CUDA-core parity path
   if (tc && (s = check_device_for_bf16()) != CP_OK) return s;
   const size_t elem = bf16 ? 2 : 4;
-  const FwdWs L = fwd_layout(*ps, H, Hkv, d, elem, fwd_needs_running(dt));
+  const bool f16 = tc && uses_f16_operands(scale);
+  const FwdWs L = fwd_layout(*ps, H, Hkv, d, elem, fwd_needs_running(dt), f16);
   if (!ws || ws_bytes < L.total)
     return fail(CP_ERR_WORKSPACE, "workspace smaller than cp_attn_fwd_workspace_size()");
   if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0)
@@ -501,10 +516,22 @@ cp_status_t cp_attn_fwd_gqa(const void* q, const void* k, const void* v, cp_dtyp
     CP_CUDA(launch_zigzag_index(ps->samples.data(), n_seqs, P, pb.R, idx, nullptr, st),
             "zigzag index kernel");
   }
+  // above softmax scale 0.25: PV on f16 operands, V from its scaled f16 copy
+  OpScales* sc = reinterpret_cast<OpScales*>(w + L.scales);
+  const void* vsrc = v;
   const void* src[3] = {q, k, v};
   void* dst[3] = {w + L.qkv[0], w + L.qkv[1], w + L.qkv[2]};
   {
-    ProfScope ps_(1, st);
+    ProfScope ps_(1, st, f16 ? 3 : 1);
+    if (f16) {
+      const int64_t n = (int64_t)T * Hkv * d;
+      void* v16 = w + L.v16;
+      CP_CUDA(cudaMemsetAsync(sc, 0, sizeof(OpScales), st), "clear operand scales");
+      CP_CUDA(launch_absmax_bf16(&v, &n, 1, sc, st), "max |V|");
+      CP_CUDA(launch_to_f16_scaled(&v, &v16, &n, 1, sc, false, d, st), "f16 copy of V");
+      vsrc = v16;
+      src[2] = vsrc;
+    }
     if (Hkv == H) {
       CP_CUDA(launch_gather_rows(src, dst, 3, (size_t)H * d * elem, idx, (int)pb.text_rows,
                                  false, st),
@@ -527,14 +554,15 @@ cp_status_t cp_attn_fwd_gqa(const void* q, const void* k, const void* v, cp_dtyp
     const int64_t PR = pb.text_rows;
     bool ok = make_tmap_thd(&a.tm_q_text, dst[0], PR, H, d, 128, &terr) &&
               make_tmap_thd(&a.tm_k_text, dst[1], PR, Hkv, d, 128, &terr) &&
-              make_tmap_thd(&a.tm_v_text, dst[2], PR, Hkv, d, 128, &terr) &&
+              make_tmap_thd(&a.tm_v_text, dst[2], PR, Hkv, d, 128, &terr, f16) &&
               make_tmap_thd(&a.tm_q_nat, q, T, H, d, 128, &terr) &&
               make_tmap_thd(&a.tm_k_nat, k, T, Hkv, d, 128, &terr) &&
-              make_tmap_thd(&a.tm_v_nat, v, T, Hkv, d, 128, &terr);
+              make_tmap_thd(&a.tm_v_nat, vsrc, T, Hkv, d, 128, &terr, f16);
     if (!ok) return fail(CP_ERR_CUDA, std::string("tensor map: ") + (terr ? terr : "?"));
     a.H = H; a.Hkv = Hkv; a.d = d;
     a.scale_log2 = scale * 1.4426950408889634f;
-    a.split_p = scale > kPrecisionSplitScale ? 1 : 0;
+    a.f16_pv = f16 ? 1 : 0;
+    a.op_scales = f16 ? sc : nullptr;
     a.o_run = o_run; a.lse_run = lse_run; a.run_rows = PR;
     a.text_rows = PR;
     a.out = out; a.lse = lse; a.T = T; a.out_lo = out_lo;
@@ -616,17 +644,17 @@ cp_status_t cp_lse_merge(int n_parts, const float* part_out, const float* part_l
 }
 
 size_t cp_attn_bwd_workspace_size_gqa(cp_dtype_t dt, int T, int H, int Hkv, int d,
-                                      const int32_t* cu, int n_seqs, int P, int N) {
+                                      const int32_t* cu, int n_seqs, int P, int N, float scale) {
   std::shared_ptr<PlanSet> ps;
   if (!cu || H < 1 || Hkv < 1 || H % Hkv != 0 || (dt != CP_F32 && dt != CP_BF16)) return 0;
   if (get_plans(cu, n_seqs, N, P, T, H, d, &ps) != CP_OK) return 0;
   const bool simt = dt != CP_BF16;   // fp32: the CUDA-core parity path
-  return bwd_layout(*ps, H, Hkv, d, simt, true).total;
+  return bwd_layout(*ps, H, Hkv, d, simt, true, !simt && uses_f16_operands(scale)).total;
 }
 
 size_t cp_attn_bwd_workspace_size(cp_dtype_t dt, int T, int H, int d, const int32_t* cu,
-                                  int n_seqs, int P, int N) {
-  return cp_attn_bwd_workspace_size_gqa(dt, T, H, H, d, cu, n_seqs, P, N);
+                                  int n_seqs, int P, int N, float scale) {
+  return cp_attn_bwd_workspace_size_gqa(dt, T, H, H, d, cu, n_seqs, P, N, scale);
 }
 
 cp_status_t cp_attn_bwd(const void* q, const void* k, const void* v, const void* out,
@@ -657,7 +685,9 @@ cp_status_t cp_attn_bwd_gqa(const void* q, const void* k, const void* v, const v
   const bool bf16 = dt == CP_BF16;
   const bool tc = bf16;   // bf16: tensor cores (head_dim 64 and 128); fp32: CUDA cores
   if (tc && (s = check_device_for_bf16()) != CP_OK) return s;
-  const BwdWs L = bwd_layout(*ps, H, Hkv, d, !tc, pgrad == nullptr);
+  // above softmax scale 0.25: S^T, dQ and dK on f16 operands (scaled copies of Q, K)
+  const bool f16 = tc && uses_f16_operands(scale);
+  const BwdWs L = bwd_layout(*ps, H, Hkv, d, !tc, pgrad == nullptr, f16);
   if (!ws || ws_bytes < L.total)
     return fail(CP_ERR_WORKSPACE, "workspace smaller than cp_attn_bwd_workspace_size()");
   if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0)
@@ -672,22 +702,32 @@ cp_status_t cp_attn_bwd_gqa(const void* q, const void* k, const void* v, const v
   float* Dd = reinterpret_cast<float*>(w + L.D);
   float* lse2 = reinterpret_cast<float*>(w + L.lse2);
   CP_CUDA(cudaMemsetAsync(w + L.status, 0, kStatusBytes, st), "clear status");
-  // 128-query tiles (one launch over the all-steps plan), or 64-query tiles
-  // (one launch per ring step) for head_dim 128 with the dS split
-  const bool q128 = tc && bwd_uses_q128(d, scale);
-  const std::vector<BwdItem>& bitems = q128 ? ps->bwd_fused.items : ps->bwd.items;
+  // tensor cores: one launch over the all-steps plan; CUDA cores: per step
+  const std::vector<BwdItem>& bitems = tc ? ps->bwd_fused.items : ps->bwd.items;
   CP_CUDA(stager().upload(w + L.items, bitems.data(), bitems.size() * sizeof(BwdItem), st),
           "upload work list");
-  if (q128)
+  if (tc)
     CP_CUDA(stager().upload(w + L.runs, ps->bwd_fused.runs.data(),
                             ps->bwd_fused.runs.size() * sizeof(Seg), st),
             "upload run list");
   CP_CUDA(stager().upload(w + L.cu, pb.cu.data(), pb.cu.size() * 4, st), "upload cu_seqlens");
   const int64_t pitch = ld_pitch(T);
+  OpScales* sc = reinterpret_cast<OpScales*>(w + L.scales);
+  void* q16 = w + L.q16;
+  void* k16 = w + L.k16;
   {
-    ProfScope ps_(3, st);
+    ProfScope ps_(3, st, f16 ? 3 : 1);
     CP_CUDA(launch_bwd_preprocess(out, out_lo, dout, bf16, lse, T, H, d, Dd, lse2, pitch, st),
             "bwd preprocess");
+    if (f16) {   // max |Q|, |K|, |V|, |dO|; then Q, K * 2^-e in f16 and the factors
+      const void* srcs[4] = {q, k, v, dout};
+      void* dsts[2] = {q16, k16};
+      const int64_t n[4] = {(int64_t)T * H * d, (int64_t)T * Hkv * d, (int64_t)T * Hkv * d,
+                            (int64_t)T * H * d};
+      CP_CUDA(cudaMemsetAsync(sc, 0, sizeof(OpScales), st), "clear operand scales");
+      CP_CUDA(launch_absmax_bf16(srcs, n, 4, sc, st), "max |Q|, |K|, |V|, |dO|");
+      CP_CUDA(launch_to_f16_scaled(srcs, dsts, n, 2, sc, true, d, st), "f16 copies of Q, K");
+    }
   }
   const BwdItem* items = reinterpret_cast<const BwdItem*>(w + L.items);
   if (tc) {
@@ -702,8 +742,7 @@ cp_status_t cp_attn_bwd_gqa(const void* q, const void* k, const void* v, const v
       int dev = 0, sms = 0;
       CP_CUDA(cudaGetDevice(&dev), "cudaGetDevice");
       CP_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev), "SM count");
-      const double per_launch =
-          q128 ? (double)bitems.size() * Hkv : (double)ps->bwd.items.size() / P * Hkv;
+      const double per_launch = (double)bitems.size() * Hkv;
       while (G % (2 * kv_split) == 0 && per_launch * kv_split < 4.0 * sms) kv_split *= 2;
     }
     if (kv_split > 1) {
@@ -716,14 +755,13 @@ cp_status_t cp_attn_bwd_gqa(const void* q, const void* k, const void* v, const v
     }
     TcBwdArgs a;
     const char* terr = nullptr;
-    const int tq = bwd_tile_q(d, scale);
-    bool ok = make_tmap_thd(&a.tm_q, q, T, H, d, tq, &terr) &&
-              make_tmap_thd(&a.tm_k, k, T, Hkv, d, kBwdTileK, &terr) &&
+    constexpr int tq = 128;   // query rows per tile
+    bool ok = make_tmap_thd(&a.tm_q, f16 ? q16 : q, T, H, d, tq, &terr, f16) &&
+              make_tmap_thd(&a.tm_k, f16 ? k16 : k, T, Hkv, d, kBwdTileK, &terr, f16) &&
               make_tmap_thd(&a.tm_v, v, T, Hkv, d, kBwdTileK, &terr) &&
               make_tmap_thd(&a.tm_do, dout, T, H, d, tq, &terr) &&
               make_tmap_ld(&a.tm_ld, lse2, pitch, H, tq + 4, &terr) &&
-              (q128 ? make_tmap_f32_sw128(&a.tm_dq, dq, T, H, d, 32, &terr)
-                    : make_tmap_f32_thd(&a.tm_dq, dq, T, H, d, 16, &terr));
+              make_tmap_f32_sw128(&a.tm_dq, dq, T, H, d, 32, &terr);
     if (!ok) return fail(CP_ERR_CUDA, std::string("tensor map: ") + (terr ? terr : "?"));
     a.H = H; a.Hkv = Hkv; a.kv_split = kv_split; a.d = d; a.scale = scale;
     a.scale_log2 = scale * 1.4426950408889634f;
@@ -734,25 +772,13 @@ cp_status_t cp_attn_bwd_gqa(const void* q, const void* k, const void* v, const v
     a.status = reinterpret_cast<int32_t*>(w + L.status);
     a.wait_limit = wait_limit();
     a.runs = reinterpret_cast<const Seg*>(w + L.runs);
-    if (q128) {   // every ring step in one launch: dK / dV written once
-      a.items = items;
-      a.n_items = (int)bitems.size();
-      a.pdl = 0;
-      ProfScope ps_(4, st, 1);
-      CP_CUDA(launch_tc_bwd_q128(a, st), "tensor-core backward (all ring steps)");
-    } else {
-      // one launch per ring step: later steps overlap the previous step's
-      // tail and wait for it only before the dK / dV epilogue
-      ProfScope ps_(4, st, P);
-      bool prev = false;
-      for (int step = 0; step < P; ++step) {
-        a.items = items + ps->bwd.step_begin[step];
-        a.n_items = ps->bwd.step_begin[step + 1] - ps->bwd.step_begin[step];
-        a.pdl = prev ? 1 : 0;
-        CP_CUDA(launch_tc_bwd(a, st), "tensor-core backward ring step");
-        prev = a.n_items > 0;
-      }
-    }
+    a.f16 = f16 ? 1 : 0;
+    a.op_scales = f16 ? sc : nullptr;
+    // every ring step in one launch: dK / dV summed on chip and written once
+    a.items = items;
+    a.n_items = (int)bitems.size();
+    ProfScope ps_(4, st, 1);
+    CP_CUDA(launch_tc_bwd_q128(a, st), "tensor-core backward (all ring steps)");
   } else {
     CP_CUDA(stager().upload(w + L.qitems, ps->fwd_nat.items.data(),
                             ps->fwd_nat.items.size() * sizeof(FwdItem), st),

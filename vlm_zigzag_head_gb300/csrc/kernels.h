@@ -46,6 +46,38 @@ cudaError_t launch_prefix_reduce(const float* slots_k, const float* slots_v, int
                                  const int32_t* cu_dev, int n_seqs, int N, int H, int d,
                                  float* dk, float* dv, cudaStream_t st);
 
+// ---- f16 operand copies (kmem.cu) ---------------------------------------------
+// Statistics and power-of-two factors of the f16 operand copies that the
+// tensor-core kernels use above softmax scale 0.25, computed on the device
+// (workspace) before the attention kernel reads them.
+struct OpScales {
+  uint32_t amax[4];   // bit patterns of max |x| (non-negative floats order as integers):
+                      // forward V; backward Q, K, V, dO.  Zeroed before each call.
+  int32_t e[4];       // copy of tensor t = x * 2^-e[t]
+  float v_mul;        // forward: O = (P V16) * v_mul
+  float qk_mul;       // backward: S = (K16 Q16^T) * qk_mul
+  float ds_inv;       // backward: dS16 = dS * ds_inv (|dS16| < 2^15)
+  float dq_mul;       // backward: dQ = scale * (dS16 K16) * dq_mul
+  float dk_mul;       // backward: dK = scale * (dS16^T Q16) * dk_mul
+  float pad[3];
+};
+static_assert(sizeof(OpScales) == 64, "OpScales layout");
+// max |x| of up to 4 bf16 tensors of n[t] elements (multiples of 8, 16-byte
+// aligned) into sc->amax[t] (atomic max over the bit patterns; NaN counts as
+// the largest, and then gives the factor 1).
+cudaError_t launch_absmax_bf16(const void* const* src, const int64_t* n, int n_tensors,
+                               OpScales* sc, cudaStream_t st);
+// dst[t] = f16(src[t] * 2^-e_t) for up to 2 bf16 tensors of n[t] elements,
+// with e_t chosen from sc->amax[t] so that the largest magnitude lies in
+// [2^14, 2^15) (clamped to |e_t| <= 60: the copies are exact for every value
+// whose scaled magnitude is at least 2^-14).  Also fills sc's factors:
+// backward = false: tensor 0 is V (v_mul); backward = true: tensors 0, 1 are
+// Q and K, sc->amax[2], [3] hold max |V|, max |dO|, and d is the head size
+// (qk_mul, ds_inv, dq_mul, dk_mul; dS is bounded by 2 d max|V| max|dO|).
+cudaError_t launch_to_f16_scaled(const void* const* src, void* const* dst, const int64_t* n,
+                                 int n_tensors, OpScales* sc, bool backward, int d,
+                                 cudaStream_t st);
+
 // ---- fp32 inputs: CUDA-core attention (attn_simt.cu) -------------------------
 struct SimtFwdArgs {
   const void* q_text; const void* k_text; const void* v_text;  // SRC_TEXT tensors

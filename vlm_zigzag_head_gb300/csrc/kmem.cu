@@ -1,6 +1,8 @@
 // HBM-bound kernels of the path: zigzag gather/scatter and index tables,
-// standalone log-sum-exp merge, backward preprocess, prefix-gradient sum.
+// standalone log-sum-exp merge, backward preprocess, prefix-gradient sum, and
+// the power-of-two-scaled f16 operand copies.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include "kernels.h"
 
@@ -221,7 +223,135 @@ int grid_for(long long work, int per_block) {
   return (int)(want < cap ? want : cap);
 }
 
+// ---- f16 operand copies -----------------------------------------------------
+struct Ptrs4 {
+  const uint4* s[4];
+  uint4* d[4];
+  long long nv[4];   // 16-byte vectors (8 elements) per tensor
+};
+// member t of a kernel-parameter array, selected without indexing it
+// dynamically (which would copy the parameters to local memory)
+template <typename T>
+__device__ __forceinline__ T pick4(const T (&x)[4], int t) {
+  return t == 0 ? x[0] : t == 1 ? x[1] : t == 2 ? x[2] : x[3];
+}
+
+// Per block (tensor blockIdx.y): max over |x| of its share, as the bit pattern
+// of a non-negative float (bf16 bits shifted into the high half), then one
+// atomic max per warp.
+__global__ void __launch_bounds__(kThreads) absmax_bf16_kernel(Ptrs4 p, uint32_t* amax) {
+  const int t = blockIdx.y;
+  const uint4* s = pick4(p.s, t);
+  const long long nv = pick4(p.nv, t);
+  uint32_t m = 0;
+  for (long long i = (long long)blockIdx.x * kThreads + threadIdx.x; i < nv;
+       i += (long long)gridDim.x * kThreads) {
+    const uint4 v = ld_stream(s + i);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      m = max(m, (w[k] & 0x7fffu) << 16);
+      m = max(m, w[k] & 0x7fff0000u);
+    }
+  }
+  m = __reduce_max_sync(0xffffffffu, m);
+  if ((threadIdx.x & 31) == 0 && m != 0) atomicMax(&amax[t], m);
+}
+
+// Exponent E of max|x| = f * 2^E with f in [0.5, 1) (normal floats), or
+// `none` for zero, subnormal or non-finite maxima.
+__device__ __forceinline__ int frexp_exp(uint32_t bits, int none) {
+  const int biased = (int)(bits >> 23);
+  if (biased == 0 || biased == 255) return none;
+  return biased - 126;
+}
+__device__ __forceinline__ int clamp_e(int e) { return e < -60 ? -60 : (e > 60 ? 60 : e); }
+// 2^k for |k| <= 126, exactly
+__device__ __forceinline__ float pow2i(int k) { return __int_as_float((k + 127) << 23); }
+// copy exponent of a tensor: its largest magnitude * 2^-e lies in [2^14, 2^15)
+__device__ __forceinline__ int copy_e(uint32_t amax_bits) {
+  return clamp_e(frexp_exp(amax_bits, 15) - 15);
+}
+
+__global__ void __launch_bounds__(kThreads) to_f16_scaled_kernel(Ptrs4 p, OpScales* sc,
+                                                                 int backward, int d_log2) {
+  const int t = blockIdx.y;
+  const int e = copy_e(t == 0 ? sc->amax[0] : sc->amax[1]);
+  const float f = pow2i(-e);
+  if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) {
+    if (!backward) {
+      sc->e[0] = e;
+      sc->v_mul = pow2i(e);
+    } else {
+      const int eq = copy_e(sc->amax[0]), ek = copy_e(sc->amax[1]);
+      // |dS| = |P (dP - D)| <= 2 d max|V| max|dO| < 2^(1 + log2 d + E_V + E_dO)
+      const int es = clamp_e(1 + d_log2 + frexp_exp(sc->amax[2], 0) +
+                             frexp_exp(sc->amax[3], 0) - 15);
+      sc->e[0] = eq;
+      sc->e[1] = ek;
+      sc->qk_mul = pow2i(eq + ek);
+      sc->ds_inv = pow2i(-es);
+      sc->dq_mul = pow2i(es + ek);
+      sc->dk_mul = pow2i(es + eq);
+    }
+  }
+  const uint4* s = pick4(p.s, t);
+  uint4* dst = pick4(p.d, t);
+  const long long nv = pick4(p.nv, t);
+  for (long long i = (long long)blockIdx.x * kThreads + threadIdx.x; i < nv;
+       i += (long long)gridDim.x * kThreads) {
+    const uint4 v = ld_stream(s + i);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float lo = __uint_as_float(w[k] << 16) * f;
+      const float hi = __uint_as_float(w[k] & 0xffff0000u) * f;
+      const __half2 h = __floats2half2_rn(lo, hi);
+      o[k] = *reinterpret_cast<const uint32_t*>(&h);
+    }
+    dst[i] = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_absmax_bf16(const void* const* src, const int64_t* n, int n_tensors,
+                               OpScales* sc, cudaStream_t st) {
+  if (n_tensors < 1 || n_tensors > 4) return cudaErrorInvalidValue;
+  Ptrs4 p{};
+  long long most = 0;
+  for (int t = 0; t < n_tensors; ++t) {
+    if (n[t] % 8 != 0) return cudaErrorInvalidValue;
+    p.s[t] = static_cast<const uint4*>(src[t]);
+    p.nv[t] = n[t] / 8;
+    most = p.nv[t] > most ? p.nv[t] : most;
+  }
+  if (most == 0) return cudaSuccess;
+  absmax_bf16_kernel<<<dim3(grid_for(most, kThreads), n_tensors), kThreads, 0, st>>>(p, sc->amax);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_to_f16_scaled(const void* const* src, void* const* dst, const int64_t* n,
+                                 int n_tensors, OpScales* sc, bool backward, int d,
+                                 cudaStream_t st) {
+  if (n_tensors < 1 || n_tensors > 2) return cudaErrorInvalidValue;
+  int d_log2 = 0;
+  while ((1 << d_log2) < d) ++d_log2;
+  Ptrs4 p{};
+  long long most = 0;
+  for (int t = 0; t < n_tensors; ++t) {
+    if (n[t] % 8 != 0) return cudaErrorInvalidValue;
+    p.s[t] = static_cast<const uint4*>(src[t]);
+    p.d[t] = static_cast<uint4*>(dst[t]);
+    p.nv[t] = n[t] / 8;
+    most = p.nv[t] > most ? p.nv[t] : most;
+  }
+  // one block at least: block (0, 0) writes the factors
+  to_f16_scaled_kernel<<<dim3(grid_for(most, kThreads), n_tensors), kThreads, 0, st>>>(
+      p, sc, backward ? 1 : 0, d_log2);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_gather_rows(const void* const* src, void* const* dst, int n_tensors,
                                size_t row_bytes, const int32_t* idx, int n_rows, bool scatter,

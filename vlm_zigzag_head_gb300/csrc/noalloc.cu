@@ -133,6 +133,12 @@ extern "C" cp_status_t cp_attn_fwd_noalloc(const void* q, const void* k, const v
   if (!bf16) o = up256(o + (size_t)pb.text_rows * H * d * sizeof(float));
   const size_t o_lrun = o;
   if (!bf16) o = up256(o + (size_t)pb.text_rows * H * sizeof(float));
+  // above softmax scale 0.25 the bf16 forward's PV takes an f16 copy of V
+  const bool f16 = bf16 && uses_f16_operands(scale);
+  const size_t o_scales = o;
+  if (f16) o = up256(o + sizeof(OpScales));
+  const size_t o_v16 = o;
+  if (f16) o = up256(o + (size_t)T * H * d * 2);
   if (o > kScratchBytes) {
     char buf[160];
     snprintf(buf, sizeof buf,
@@ -182,7 +188,17 @@ extern "C" cp_status_t cp_attn_fwd_noalloc(const void* q, const void* k, const v
   int32_t* idx = reinterpret_cast<int32_t*>(w + o_idx);
   NA_CUDA(launch_zigzag_index(samples.data(), n_seqs, P, pb.R, idx, nullptr, st),
           "zigzag index kernel");
-  const void* src[3] = {q, k, v};
+  OpScales* sc = reinterpret_cast<OpScales*>(w + o_scales);
+  const void* vsrc = v;
+  if (f16) {
+    const int64_t n = (int64_t)T * H * d;
+    void* v16 = w + o_v16;
+    NA_CUDA(cudaMemsetAsync(sc, 0, sizeof(OpScales), st), "clear operand scales");
+    NA_CUDA(launch_absmax_bf16(&v, &n, 1, sc, st), "max |V|");
+    NA_CUDA(launch_to_f16_scaled(&v, &v16, &n, 1, sc, false, d, st), "f16 copy of V");
+    vsrc = v16;
+  }
+  const void* src[3] = {q, k, vsrc};
   void* dst[3] = {w + o_qkv[0], w + o_qkv[1], w + o_qkv[2]};
   NA_CUDA(launch_gather_rows(src, dst, 3, (size_t)H * d * elem, idx, (int)pb.text_rows, false, st),
           "zigzag gather");
@@ -193,10 +209,10 @@ extern "C" cp_status_t cp_attn_fwd_noalloc(const void* q, const void* k, const v
     const int64_t PR = pb.text_rows;
     const bool ok = make_tmap_thd(&a.tm_q_text, dst[0], PR, H, d, 128, &terr) &&
                     make_tmap_thd(&a.tm_k_text, dst[1], PR, H, d, 128, &terr) &&
-                    make_tmap_thd(&a.tm_v_text, dst[2], PR, H, d, 128, &terr) &&
+                    make_tmap_thd(&a.tm_v_text, dst[2], PR, H, d, 128, &terr, f16) &&
                     make_tmap_thd(&a.tm_q_nat, q, T, H, d, 128, &terr) &&
                     make_tmap_thd(&a.tm_k_nat, k, T, H, d, 128, &terr) &&
-                    make_tmap_thd(&a.tm_v_nat, v, T, H, d, 128, &terr);
+                    make_tmap_thd(&a.tm_v_nat, vsrc, T, H, d, 128, &terr, f16);
     if (!ok) return fail(CP_ERR_CUDA, std::string("tensor map: ") + (terr ? terr : "?"));
     a.H = H; a.Hkv = H; a.d = d; a.pdl = 0;
     a.items = items;
@@ -211,7 +227,8 @@ extern "C" cp_status_t cp_attn_fwd_noalloc(const void* q, const void* k, const v
       a.n_ctas = grid;
     }
     a.scale_log2 = scale * 1.4426950408889634f;
-    a.split_p = scale > kPrecisionSplitScale ? 1 : 0;
+    a.f16_pv = f16 ? 1 : 0;
+    a.op_scales = f16 ? sc : nullptr;
     a.o_run = nullptr; a.lse_run = nullptr; a.run_rows = 0;
     a.text_rows = PR;
     a.out = out; a.lse = lse; a.T = T; a.out_lo = out_lo;

@@ -243,10 +243,31 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int a_mn_major, 
          | ((uint32_t)(M >> 4) << 24);   // M / 16
 }
 
+// Instruction descriptor of kind::f16 with f16 A and B (A and B of one MMA
+// always share a type), fp32 accumulator.
+__host__ __device__ constexpr uint32_t idesc_f16(int M, int N, int a_mn_major, int b_mn_major) {
+  return (1u << 4)                       // accumulator format: f32
+         | ((uint32_t)a_mn_major << 15)  // A format f16 (0); A major-ness
+         | ((uint32_t)b_mn_major << 16)  // B format f16 (0); B major-ness
+         | ((uint32_t)(N >> 3) << 17)    // N / 8
+         | ((uint32_t)(M >> 4) << 24);   // M / 16
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
   return r;
+}
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+// Operand pairs for kind::f16 MMAs: bf16, or f16 when kF16.
+template <bool kF16>
+__device__ __forceinline__ uint32_t pack_op2(float lo, float hi) {
+  if constexpr (kF16) return pack_f16x2(lo, hi);
+  else return pack_bf16x2(lo, hi);
 }
 // Programmatic dependent launch: let the next kernel of the stream start its
 // CTAs once every CTA of this grid has issued this (or exited) ...

@@ -4,24 +4,26 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "kernels.h"
 #include "plan.h"
 
 namespace cpattn {
 
 // Softmax scales above this make dQ = scale * dS K large enough that one bf16
 // rounding of a probability-sized operand (P in the forward's PV product, dS
-// in the backward's dQ product) shows in dQ; both kernels then carry that
-// operand as a bf16 hi + lo pair.
-constexpr float kPrecisionSplitScale = 0.25f;
+// in the backward's dQ and dK products) shows in dQ.  Those products then run
+// on f16 operands (three more mantissa bits): P and dS are rounded to f16, and
+// the other operand is a per-call f16 copy of V (forward) or of Q and K
+// (backward), scaled by a power of two so that its largest magnitude lies in
+// [2^14, 2^15).  The scaling is exact; the factors are undone in fp32.
+constexpr float kF16OperandScale = 0.25f;
+inline bool uses_f16_operands(float scale) { return scale > kF16OperandScale; }
 
-// 3-D tensor map over a bf16 [rows][H][d] tensor, box {64, 1, rows_per_box},
-// 128-byte swizzle.  Returns false (and a message) if encoding fails.
+// 3-D tensor map over a 16-bit [rows][H][d] tensor (bf16, or f16 when f16 is
+// set), box {64, 1, rows_per_box}, 128-byte swizzle.  Returns false (and a
+// message) if encoding fails.
 bool make_tmap_thd(CUtensorMap* map, const void* base, int64_t rows, int H, int d,
-                   int rows_per_box, const char** err);
-// 3-D tensor map over an fp32 [rows][H][d] tensor, box {d, 1, box_rows}, no
-// swizzle (the dQ reduce-add target of the backward).
-bool make_tmap_f32_thd(CUtensorMap* map, void* base, int64_t rows, int H, int d, int box_rows,
-                       const char** err);
+                   int rows_per_box, const char** err, bool f16 = false);
 // 3-D tensor map over an fp32 [rows][H][d] tensor, box {32, 1, box_rows} with
 // the 128-byte swizzle (the dQ reduce-add target of the 128-query backward).
 bool make_tmap_f32_sw128(CUtensorMap* map, void* base, int64_t rows, int H, int d, int box_rows,
@@ -44,9 +46,10 @@ struct TcFwdArgs {
   int n_items, H, d;
   int Hkv;                    // KV heads; query head h reads KV head h / (H / Hkv)
   float scale_log2;           // softmax scale * log2(e)
-  int split_p;                // P enters PV as bf16 hi + lo (softmax scale > kPrecisionSplitScale)
+  int f16_pv;                 // PV on f16 operands: P and the scaled copy of V behind
+                              // tm_v_*; O is multiplied by op_scales->v_mul
+  const OpScales* op_scales;  // device; read when f16_pv
   int pdl;                    // launched as a programmatic dependent of the previous ring step
-                              // (64-query kernel; the 128-query kernel is one launch per call)
   float* o_run; float* lse_run; int64_t run_rows;
   void* out; float* lse; int64_t T;
   void* out_lo;               // nullable: bf16 remainder o - bf16(o)
@@ -57,11 +60,15 @@ struct TcFwdArgs {
 cudaError_t launch_tc_fwd(const TcFwdArgs& a, cudaStream_t st);
 
 struct TcBwdArgs {
-  CUtensorMap tm_q, tm_k, tm_v, tm_do;  // natural order
+  CUtensorMap tm_q, tm_k, tm_v, tm_do;  // natural order (Q, K: the f16 copies when f16)
   CUtensorMap tm_ld;                     // [2][H][pitch] fp32: lse2, D
-  CUtensorMap tm_dq;                     // dq fp32 [T][H][d], box {d, 1, 16}: reduce-add target
+  CUtensorMap tm_dq;                     // dq fp32 [T][H][d], box {32, 1, 32}, 128-byte swizzle:
+                                         // reduce-add target
   const BwdItem* items;
-  const Seg* runs;            // run list of an all-steps plan (128-query kernel); else unused
+  const Seg* runs;            // run list of the all-steps plan: item i's query runs are
+                              // runs[items[i].run0 .. + nseg)
+  int f16;                    // S, dQ and dK on f16 operands (scaled Q, K copies; dS in f16)
+  const OpScales* op_scales;  // device; read when f16
   int n_items, H, d;
   int Hkv;                    // KV heads; one CTA per (key tile, KV head) walks its H / Hkv query heads
   float scale, scale_log2;
@@ -72,22 +79,10 @@ struct TcBwdArgs {
   long long wait_limit;
   int kv_split;               // CTAs sharing one KV head's query heads (divides H / Hkv); > 1:
                               // dK / dV / prefix slots are reduce-added into zeroed memory
-  int pdl;                    // launched as a programmatic dependent of the previous ring step
-                              // (64-query kernel; the 128-query kernel is one launch per call)
   int n_slots;                // prefix-gradient slots (P + 1) behind pre_k / pre_v (index checks)
 };
-cudaError_t launch_tc_bwd(const TcBwdArgs& a, cudaStream_t st);
-
-// The backward walks 128-query tiles (tc_bwd_q128.cu: one launch over the
-// all-steps plan, every item a key tile with the query runs of all ring
-// steps) except at head_dim 128
-// with the dS precision split, whose second dS buffer does not fit in shared
-// memory beside 128-query tiles; that case walks 64-query tiles (tc_bwd.cu).
-// The tensor maps differ: Q / dO boxes of bwd_tile_q(...) rows, an lse2 / D
-// box of bwd_tile_q(...) + 4 rows, and the dQ target as swizzled 32-column
-// boxes of 32 rows (128-query tiles) or unswizzled d-column boxes of 16 rows.
-inline bool bwd_uses_q128(int d, float scale) { return d == 64 || scale <= kPrecisionSplitScale; }
-inline int bwd_tile_q(int d, float scale) { return bwd_uses_q128(d, scale) ? 128 : 64; }
+// The backward (tc_bwd_q128.cu): one launch over the all-steps plan, every
+// item a key tile with the query runs of all ring steps, in 128-query tiles.
 cudaError_t launch_tc_bwd_q128(const TcBwdArgs& a, cudaStream_t st);
 
 }  // namespace cpattn

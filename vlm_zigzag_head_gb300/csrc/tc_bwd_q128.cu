@@ -28,10 +28,11 @@
 // D = 128, dP_{i+1} waits for the drain to have read dQ_i out of the dP^T
 // columns.
 //
-// For softmax scales above kPrecisionSplitScale dS^T also enters dQ as its
-// bf16 remainder (a second product): the dQ values are large enough there
-// that one bf16 rounding of dS would dominate the error.  Only D = 64 is built
-// that way here (the remainder buffer does not fit beside D = 128 tiles).
+// For softmax scales above kF16OperandScale the dQ values are large enough
+// that one bf16 rounding of dS would dominate their error.  S^T, dQ and dK
+// then run on f16 operands: the host-made copies Q * 2^-eQ and K * 2^-eK, and
+// dS^T * 2^-eS rounded to f16 (three more mantissa bits than bf16); the
+// factors are undone in fp32 (OpScales).  dP^T and dV keep bf16 V, dO and P^T.
 //
 // Warp roles (512 threads; TMEM lane quarter of warp w is w % 4):
 //   warp 0       TMA producer: K, V once; Q and the lse2 / D rows per tile
@@ -77,7 +78,7 @@ struct Cols {
   static constexpr bool kAliased = D == 128;
 };
 
-template <int D, bool kSplit>
+template <int D>
 struct Lay {
   static constexpr int kBox = 128 * 128;        // 128 rows x 128 bytes
   static constexpr int kTile = D / 64 * kBox;   // 128 rows x D bf16
@@ -88,9 +89,8 @@ struct Lay {
   static constexpr int kV = kK + kTile;
   static constexpr int kQ = kV + kTile;                     // [stage]
   static constexpr int kDO = kQ + kQStages * kTile;         // [stage]
-  static constexpr int kDS = kDO + kDOStages * kTile;       // bf16 dS^T: 2 boxes [128 keys][64 q]
-  static constexpr int kDSL = kDS + 2 * kBox;               // its bf16 remainder (split only)
-  static constexpr int kStg = kDSL + (kSplit ? 2 * kBox : 0);
+  static constexpr int kDS = kDO + kDOStages * kTile;       // dS^T: 2 boxes [128 keys][64 q]
+  static constexpr int kStg = kDS + 2 * kBox;
   static constexpr int kStgWarp = 32 * 128;                 // [32 rows][32 fp32], 128-byte swizzle
   static constexpr int kLd = kStg + 4 * kStgWarp;           // [stage] {lse2[132], D[132]}
   static constexpr int kLdBytes = 2 * kLdRows * 4;
@@ -103,8 +103,8 @@ struct Lay {
   static_assert(kStg % 1024 == 0, "swizzled staging must be 1024-byte aligned");
   static_assert(kLd % 16 == 0 && (kLdRows * 4) % 16 == 0, "16-byte lse2 / D loads");
 };
-static_assert(Lay<128, false>::kAlloc <= 227 * 1024, "shared memory budget");
-static_assert(Lay<64, true>::kAlloc <= 227 * 1024, "shared memory budget");
+static_assert(Lay<128>::kAlloc <= 227 * 1024, "shared memory budget");
+static_assert(Lay<64>::kAlloc <= 227 * 1024, "shared memory budget");
 
 // What the P / dS warps need of a query tile, written by the Q producer
 // beside the tile (published by the same barrier as the Q load).
@@ -167,10 +167,10 @@ __device__ __forceinline__ void record_timeout(int32_t* status, volatile int* ab
   *abort = 1;
 }
 
-template <int D, bool kSplit, bool kShared>
+template <int D, bool kF16, bool kShared>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_bwd_q128_kernel(const __grid_constant__ TcBwdArgs a) {
-  using L = Lay<D, kSplit>;
+  using L = Lay<D>;
   using C = Cols<D>;
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte aligned base, derived from the shared array itself so that the
@@ -331,11 +331,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == 1) {
       // ---------------------------------------------------------- MMA issuer
       if (lane == 0) {
-        constexpr uint32_t idesc_sdp = idesc_bf16(kBK, kBQ, 0, 0);   // K-major A and B
-        constexpr uint32_t idesc_kv = idesc_bf16(kBK, D, 0, 1);      // B (Q, dO) MN-major
-        constexpr uint32_t idesc_dq = idesc_bf16(kBQ, D, 1, 1);      // A (dS), B (K) MN-major
+        // K-major A and B; B (Q, dO) MN-major; A (dS), B (K) MN-major.  S^T, dQ
+        // and dK take f16 operands when kF16 (K, Q copies and dS^T all f16);
+        // dP^T and dV always bf16 (V, dO, P^T)
+        constexpr uint32_t idesc_s = kF16 ? idesc_f16(kBK, kBQ, 0, 0) : idesc_bf16(kBK, kBQ, 0, 0);
+        constexpr uint32_t idesc_dp = idesc_bf16(kBK, kBQ, 0, 0);
+        constexpr uint32_t idesc_dv = idesc_bf16(kBK, D, 0, 1);
+        constexpr uint32_t idesc_dk = kF16 ? idesc_f16(kBK, D, 0, 1) : idesc_bf16(kBK, D, 0, 1);
+        constexpr uint32_t idesc_dq = kF16 ? idesc_f16(kBQ, D, 1, 1) : idesc_bf16(kBQ, D, 1, 1);
         const uint32_t k_addr = smem_u32(smem + L::kK), v_addr = smem_u32(smem + L::kV);
-        const uint32_t ds_addr = smem_u32(smem + L::kDS), dsl_addr = smem_u32(smem + L::kDSL);
+        const uint32_t ds_addr = smem_u32(smem + L::kDS);
         // S^T (into the S columns) from K and Q stage st
         auto issue_s = [&](int st) {
           const uint32_t q_addr = smem_u32(smem + L::kQ + st * L::kTile);
@@ -343,7 +348,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int kk = 0; kk < D / 16; ++kk) {      // over head dim
             const uint32_t o = (kk / 4) * L::kBox + (kk % 4) * 32;
             mma_bf16(tmem + kColS, sdesc_sw128(k_addr + o, 16, 1024),
-                     sdesc_sw128(q_addr + o, 16, 1024), idesc_sdp, kk > 0 ? 1u : 0u);
+                     sdesc_sw128(q_addr + o, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
           }
           mma_commit(&bars->s_full);
         };
@@ -369,7 +374,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t o = (kk / 4) * L::kBox + (kk % 4) * 32;
             mma_bf16(tmem + kColDP, sdesc_sw128(v_addr + o, 16, 1024),
-                     sdesc_sw128(do_addr + o, 16, 1024), idesc_sdp, kk > 0 ? 1u : 0u);
+                     sdesc_sw128(do_addr + o, 16, 1024), idesc_dp, kk > 0 ? 1u : 0u);
           }
           mma_commit(&bars->dp_full);
           // ---- dV += P^T_i dO_i, P^T from the S columns (query pairs per column)
@@ -379,7 +384,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int kk = 0; kk < kBQ / 16; ++kk) {    // over queries
             const uint32_t pa = tmem + kColS + (kk / 4) * 64 + (kk % 4) * 8;
             mma_bf16_ts(tmem + C::kDV, pa, sdesc_sw128(do_addr + kk * 16 * 128, L::kBox, 1024),
-                        idesc_kv, (i > 0 || kk > 0) ? 1u : 0u);
+                        idesc_dv, (i > 0 || kk > 0) ? 1u : 0u);
           }
           mma_commit(&bars->do_empty[so]);
           // ---- S^T_{i+1} (overwrites P^T_i: issued after dV_i)
@@ -404,9 +409,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t kb = sdesc_sw128(k_addr + kk * 16 * 128, L::kBox, 1024);
             mma_bf16(tmem + C::kDQ, sdesc_sw128(ds_addr + kk * 16 * 128, L::kBox, 1024), kb,
                      idesc_dq, kk > 0 ? 1u : 0u);
-            if constexpr (kSplit)
-              mma_bf16(tmem + C::kDQ, sdesc_sw128(dsl_addr + kk * 16 * 128, L::kBox, 1024), kb,
-                       idesc_dq, 1u);
           }
           mma_commit(&bars->dq_full);
           const uint32_t q_addr = smem_u32(smem + L::kQ + st * L::kTile);
@@ -414,7 +416,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int kk = 0; kk < kBQ / 16; ++kk) {    // over queries
             mma_bf16(tmem + C::kDK,
                      sdesc_sw128(ds_addr + (kk / 4) * L::kBox + (kk % 4) * 32, 16, 1024),
-                     sdesc_sw128(q_addr + kk * 16 * 128, L::kBox, 1024), idesc_kv,
+                     sdesc_sw128(q_addr + kk * 16 * 128, L::kBox, 1024), idesc_dk,
                      (i > 0 || kk > 0) ? 1u : 0u);
           }
           mma_commit(&bars->q_empty[st]);
@@ -441,6 +443,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // the tensor map).
     const int wq = warp & 3;
     const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
+    // dQ = scale * (dS K); with f16 operands also undo the dS and K factors
+    const float dq_mul = kF16 ? a.scale * a.op_scales->dq_mul : a.scale;
     uint8_t* stg = smem + L::kStg + wq * L::kStgWarp;
     uint8_t* my_row = stg + lane * 128;
     const int sw = lane & 7;
@@ -471,10 +475,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
 #pragma unroll
         for (int x = 0; x < 8; ++x) {
-          const float4 v = make_float4(__uint_as_float(r[c][4 * x]) * a.scale,
-                                       __uint_as_float(r[c][4 * x + 1]) * a.scale,
-                                       __uint_as_float(r[c][4 * x + 2]) * a.scale,
-                                       __uint_as_float(r[c][4 * x + 3]) * a.scale);
+          const float4 v = make_float4(__uint_as_float(r[c][4 * x]) * dq_mul,
+                                       __uint_as_float(r[c][4 * x + 1]) * dq_mul,
+                                       __uint_as_float(r[c][4 * x + 2]) * dq_mul,
+                                       __uint_as_float(r[c][4 * x + 3]) * dq_mul);
           *reinterpret_cast<float4*>(my_row + ((x ^ sw) << 4)) = v;
         }
         fence_proxy_async_smem();
@@ -497,7 +501,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int g = (warp - 4) >> 2;
     const int u = (warp & 3) * 32 + lane;        // key row == TMEM lane
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
-    const float sl2 = a.scale_log2;
+    // S^T = (K16 Q16^T) * qk_mul and dS16 = dS * ds_inv with f16 operands
+    const float sl2 = kF16 ? a.scale_log2 * a.op_scales->qk_mul : a.scale_log2;
+    const float ds_inv = kF16 ? a.op_scales->ds_inv : 1.f;
     const bool key_ok = u < it.k_len;
     const int sw = u & 7;
     bool ok = true;
@@ -566,14 +572,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!mbar_wait(&bars->dp_full, i & 1, lim, abort)) { ok = false; break; }
       tc_fence_after();
       uint8_t* srow = smem + L::kDS + g * L::kBox + u * 128;
-      uint8_t* lrow = smem + L::kDSL + g * L::kBox + u * 128;
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         uint32_t rd[32];
         tmem_ld32(tmem + lane_off + kColDP + g * 64 + h * 32, rd);
         tmem_ld_wait();
         reg_fence32(rd);
-        uint32_t hk[16], lk[16];
+        uint32_t hk[16];
 #pragma unroll
         for (int x = 0; x < 32; x += 4) {
           float dd[4];
@@ -589,14 +594,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float d0 = __uint_as_float(rs[h][x + y]) * (__uint_as_float(rd[x + y]) - dd[y]);
             const float d1 =
                 __uint_as_float(rs[h][x + y + 1]) * (__uint_as_float(rd[x + y + 1]) - dd[y + 1]);
-            if constexpr (kSplit) {
-              const float h0 = __bfloat162float(__float2bfloat16_rn(d0));
-              const float h1 = __bfloat162float(__float2bfloat16_rn(d1));
-              hk[(x + y) / 2] = pack_bf16x2(h0, h1);
-              lk[(x + y) / 2] = pack_bf16x2(d0 - h0, d1 - h1);
-            } else {
+            if constexpr (kF16)
+              hk[(x + y) / 2] = pack_f16x2(d0 * ds_inv, d1 * ds_inv);
+            else
               hk[(x + y) / 2] = pack_bf16x2(d0, d1);
-            }
           }
         }
 #pragma unroll
@@ -604,9 +605,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int off = ((h * 4 + c) ^ sw) << 4;
           *reinterpret_cast<uint4*>(srow + off) =
               make_uint4(hk[c * 4], hk[c * 4 + 1], hk[c * 4 + 2], hk[c * 4 + 3]);
-          if constexpr (kSplit)
-            *reinterpret_cast<uint4*>(lrow + off) =
-                make_uint4(lk[c * 4], lk[c * 4 + 1], lk[c * 4 + 2], lk[c * 4 + 3]);
         }
       }
       fence_proxy_async_smem();
@@ -633,7 +631,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         dst = (g == 0 ? a.pre_k : a.pre_v) + (row * a.Hkv + hk) * D;
       }
       const bool first = (it.flags & F_FIRST) != 0;
-      const float mul = g == 0 ? a.scale : 1.f;
+      const float mul = g == 0 ? (kF16 ? a.scale * a.op_scales->dk_mul : a.scale) : 1.f;
       const uint32_t col = g == 0 ? C::kDK : C::kDV;
 #pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {
@@ -673,15 +671,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int D, bool kSplit, bool kShared>
+template <int D, bool kF16, bool kShared>
 cudaError_t launch_q128(const TcBwdArgs& a, cudaStream_t st) {
-  constexpr int smem = Lay<D, kSplit>::kAlloc;
-  cudaError_t e = cudaFuncSetAttribute(tc_bwd_q128_kernel<D, kSplit, kShared>,
+  constexpr int smem = Lay<D>::kAlloc;
+  cudaError_t e = cudaFuncSetAttribute(tc_bwd_q128_kernel<D, kF16, kShared>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const long long blocks = (long long)a.n_items * a.Hkv * a.kv_split;
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  tc_bwd_q128_kernel<D, kSplit, kShared><<<(unsigned)blocks, kThreads, smem, st>>>(a);
+  tc_bwd_q128_kernel<D, kF16, kShared><<<(unsigned)blocks, kThreads, smem, st>>>(a);
   return cudaGetLastError();
 }
 
@@ -691,16 +689,15 @@ cudaError_t launch_tc_bwd_q128(const TcBwdArgs& a, cudaStream_t st) {
   if (a.n_items == 0) return cudaSuccess;
   if (a.runs == nullptr) return cudaErrorInvalidValue;   // all-steps items only
   if (a.kv_split < 1 || (a.H / a.Hkv) % a.kv_split != 0) return cudaErrorInvalidValue;
-  const bool split = a.scale > kPrecisionSplitScale;
+  if (a.f16 && a.op_scales == nullptr) return cudaErrorInvalidValue;
+  const bool sh = a.kv_split > 1;
   if (a.d == 128) {
-    if (split) return cudaErrorNotSupported;   // 64-query tiles (tc_bwd.cu)
-    return a.kv_split > 1 ? launch_q128<128, false, true>(a, st)
-                          : launch_q128<128, false, false>(a, st);
+    if (a.f16) return sh ? launch_q128<128, true, true>(a, st) : launch_q128<128, true, false>(a, st);
+    return sh ? launch_q128<128, false, true>(a, st) : launch_q128<128, false, false>(a, st);
   }
   if (a.d != 64) return cudaErrorNotSupported;
-  if (split)
-    return a.kv_split > 1 ? launch_q128<64, true, true>(a, st) : launch_q128<64, true, false>(a, st);
-  return a.kv_split > 1 ? launch_q128<64, false, true>(a, st) : launch_q128<64, false, false>(a, st);
+  if (a.f16) return sh ? launch_q128<64, true, true>(a, st) : launch_q128<64, true, false>(a, st);
+  return sh ? launch_q128<64, false, true>(a, st) : launch_q128<64, false, false>(a, st);
 }
 
 }  // namespace cpattn

@@ -32,10 +32,11 @@
 // TMEM (512 columns): S_A [0,128), S_B [128,256), O_A [256, 256 + D),
 // O_B [384, 384 + D).  P (bf16 pairs, 64 columns) overwrites the first half of
 // its S buffer and is the A operand of PV, read straight from TMEM.  For
-// softmax scales above kPrecisionSplitScale the bf16 remainder p - bf16(p)
-// fills the second half and enters O through a second PV product: the
-// backward's D = dO . O then carries O to about 16 bits, which keeps large
-// dQ rows (few visible keys, scale 1) inside the bf16 tolerance.  Shared
+// softmax scales above kF16OperandScale P is rounded to f16 instead and V is
+// the host-made f16 copy V * 2^-e (PV on f16 operands, O multiplied by 2^e in
+// the epilogue): the backward's D = dO . O then carries O to about 11 bits,
+// which keeps large dQ rows (few visible keys, scale 1) inside the bf16
+// tolerance.  Shared
 // memory: Q_A, Q_B, two K and two V stages (128 x D each) in the 128-byte
 // swizzled layout TMA writes, 1024-byte aligned.
 #include <cuda_bf16.h>
@@ -133,7 +134,7 @@ __device__ __forceinline__ void record_timeout(int32_t* status, volatile int* ab
   *abort = 1;
 }
 
-template <int D, bool kSplitP>
+template <int D, bool kF16P>
 __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_constant__ TcFwdArgs a) {
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte aligned base, derived from the shared array itself so that the
@@ -269,7 +270,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc_qk = idesc_bf16(kBM, kBN, 0, 0);
-      constexpr uint32_t idesc_pv = idesc_bf16(kBM, D, 0, 1);
+      constexpr uint32_t idesc_pv = kF16P ? idesc_f16(kBM, D, 0, 1) : idesc_bf16(kBM, D, 0, 1);
       const uint32_t q_addr = smem_u32(smem + L::kQ);
       // S_x(j) = Q_x K_j^T into tile x's S buffer
       auto issue_s = [&](int x, int j) {
@@ -298,8 +299,6 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
           const uint64_t bd = sdesc_sw128(v_addr + kk * 16 * 128, L::kBox, 1024);
           mma_bf16_ts(tmem + col_o(x), tmem + col_s(x) + kk * 8, bd, idesc_pv,
                       (!first || kk > 0) ? 1u : 0u);
-          if constexpr (kSplitP)   // the bf16 remainder of P, in S columns [64, 128)
-            mma_bf16_ts(tmem + col_o(x), tmem + col_s(x) + 64 + kk * 8, bd, idesc_pv, 1u);
         }
         mma_commit(&bars->o_done[x]);
         if (x == 1) mma_commit(&bars->v_empty[st]);
@@ -355,6 +354,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     const uint32_t s_col = tmem + lane_off + col_s(x);
     const float sl2 = a.scale_log2;
+    const float vmul = kF16P ? a.op_scales->v_mul : 1.f;   // V = V16 * vmul
     bool ok = true;
     int j = 0;   // KV tile counter across units
     const UnitRange ur = cta_units(a);
@@ -427,58 +427,34 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
             tmem_st_wait();
           }
         }
-        // probabilities, row sum, and P (bf16 pairs) over S columns [0, 64)
+        // probabilities, row sum, and P (bf16 pairs, or f16 pairs for the f16 PV
+        // product) over S columns [0, 64)
         const float mu = m == -INFINITY ? 0.f : m;
         float sp[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) sp[i] = 0.f;
-        if constexpr (kSplitP) {
-          // P (bf16 pairs) over S columns [0, 64) and its bf16 remainder over
-          // [64, 128), written one half row (64 keys) at a time
+        uint32_t pk[2][32];
+        if (whole) {
 #pragma unroll
-          for (int hh = 0; hh < 2; ++hh) {
-            uint32_t pk[32], pl[32];
-#pragma unroll
-            for (int i = hh * 64; i < hh * 64 + 64; i += 2) {
-              float p0 = ex2(fmaf(__uint_as_float(r[i / 32][i % 32]), sl2, -mu));
-              float p1 = ex2(fmaf(__uint_as_float(r[i / 32][i % 32 + 1]), sl2, -mu));
-              if (!whole) {
-                if (i >= vis) p0 = 0.f;
-                if (i + 1 >= vis) p1 = 0.f;
-              }
-              sp[(i >> 1) & 7] += p0 + p1;
-              pk[(i / 2) % 32] = pack_bf16x2(p0, p1);
-              const float h0 = __bfloat162float(__float2bfloat16_rn(p0));
-              const float h1 = __bfloat162float(__float2bfloat16_rn(p1));
-              pl[(i / 2) % 32] = pack_bf16x2(p0 - h0, p1 - h1);
-            }
-            tmem_st32(s_col + hh * 32, pk);
-            tmem_st32(s_col + 64 + hh * 32, pl);
+          for (int i = 0; i < kBN; i += 2) {
+            const float p0 = ex2(fmaf(__uint_as_float(r[i / 32][i % 32]), sl2, -mu));
+            const float p1 = ex2(fmaf(__uint_as_float(r[i / 32][i % 32 + 1]), sl2, -mu));
+            sp[(i >> 1) & 7] += p0 + p1;
+            pk[i / 64][(i / 2) % 32] = pack_op2<kF16P>(p0, p1);
           }
         } else {
-          uint32_t pk[2][32];
-          if (whole) {
 #pragma unroll
-            for (int i = 0; i < kBN; i += 2) {
-              const float p0 = ex2(fmaf(__uint_as_float(r[i / 32][i % 32]), sl2, -mu));
-              const float p1 = ex2(fmaf(__uint_as_float(r[i / 32][i % 32 + 1]), sl2, -mu));
-              sp[(i >> 1) & 7] += p0 + p1;
-              pk[i / 64][(i / 2) % 32] = pack_bf16x2(p0, p1);
-            }
-          } else {
-#pragma unroll
-            for (int i = 0; i < kBN; i += 2) {
-              float p0 = ex2(fmaf(__uint_as_float(r[i / 32][i % 32]), sl2, -mu));
-              float p1 = ex2(fmaf(__uint_as_float(r[i / 32][i % 32 + 1]), sl2, -mu));
-              if (i >= vis) p0 = 0.f;
-              if (i + 1 >= vis) p1 = 0.f;
-              sp[(i >> 1) & 7] += p0 + p1;
-              pk[i / 64][(i / 2) % 32] = pack_bf16x2(p0, p1);
-            }
+          for (int i = 0; i < kBN; i += 2) {
+            float p0 = ex2(fmaf(__uint_as_float(r[i / 32][i % 32]), sl2, -mu));
+            float p1 = ex2(fmaf(__uint_as_float(r[i / 32][i % 32 + 1]), sl2, -mu));
+            if (i >= vis) p0 = 0.f;
+            if (i + 1 >= vis) p1 = 0.f;
+            sp[(i >> 1) & 7] += p0 + p1;
+            pk[i / 64][(i / 2) % 32] = pack_op2<kF16P>(p0, p1);
           }
-          tmem_st32(s_col, pk[0]);
-          tmem_st32(s_col + 32, pk[1]);
         }
+        tmem_st32(s_col, pk[0]);
+        tmem_st32(s_col + 32, pk[1]);
         l += ((sp[0] + sp[1]) + (sp[2] + sp[3])) + ((sp[4] + sp[5]) + (sp[6] + sp[7]));
         tmem_st_wait();
         tc_fence_before();
@@ -507,7 +483,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
           !CP_IN_RANGE(it.run_row0 + tq, 0, a.run_rows, a.status, 108))
         valid = false;
       float lse_s = l > 0.f ? (m + __log2f(l)) * 0.6931471805599453f : -INFINITY;
-      const float inv = l > 0.f ? 1.f / l : 0.f;
+      const float inv = l > 0.f ? vmul / l : 0.f;
       const int flags = it.flags;
       const long long rrow =
           it.run_row0 >= 0 && a.runs == nullptr ? (long long)h * a.run_rows + it.run_row0 + tq : 0;
@@ -602,10 +578,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
   }
 }
 
-template <int D, bool kSplitP>
+template <int D, bool kF16P>
 cudaError_t launch_d(const TcFwdArgs& a, cudaStream_t st) {
   const int smem = Smem<D>::kAlloc;
-  cudaError_t e = cudaFuncSetAttribute(tc_fwd_kernel<D, kSplitP>,
+  cudaError_t e = cudaFuncSetAttribute(tc_fwd_kernel<D, kF16P>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   // persistent: one CTA per SM walks units gridDim.x apart
@@ -629,14 +605,17 @@ cudaError_t launch_d(const TcFwdArgs& a, cudaStream_t st) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = a.pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, tc_fwd_kernel<D, kSplitP>, a);
+  return cudaLaunchKernelEx(&cfg, tc_fwd_kernel<D, kF16P>, a);
 }
 
 }  // namespace
 
 cudaError_t launch_tc_fwd(const TcFwdArgs& a, cudaStream_t st) {
   if (a.n_items == 0) return cudaSuccess;
-  if (a.split_p) return a.d == 64 ? launch_d<64, true>(a, st) : launch_d<128, true>(a, st);
+  if (a.f16_pv) {
+    if (a.op_scales == nullptr) return cudaErrorInvalidValue;
+    return a.d == 64 ? launch_d<64, true>(a, st) : launch_d<128, true>(a, st);
+  }
   return a.d == 64 ? launch_d<64, false>(a, st) : launch_d<128, false>(a, st);
 }
 

@@ -32,7 +32,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 // 64 bf16 = 128 bytes, laid out by the hardware in the 128-byte swizzle that
 // the tensor-core shared-memory descriptors expect.
 bool make_tmap_thd(CUtensorMap* map, const void* base, int64_t rows, int H, int d,
-                   int rows_per_box, const char** err) {
+                   int rows_per_box, const char** err, bool f16) {
   auto fn = encode_fn();
   if (!fn) {
     *err = "cuTensorMapEncodeTiled unavailable";
@@ -43,33 +43,12 @@ bool make_tmap_thd(CUtensorMap* map, const void* base, int64_t rows, int H, int 
   cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)H * d * 2};
   cuuint32_t box[3] = {64, 1, (cuuint32_t)rows_per_box};
   cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
+  CUresult r = fn(map, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+                  const_cast<void*>(base), dims, strides,
                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) {
     *err = "cuTensorMapEncodeTiled failed";
-    return false;
-  }
-  return true;
-}
-
-bool make_tmap_f32_thd(CUtensorMap* map, void* base, int64_t rows, int H, int d, int box_rows,
-                       const char** err) {
-  auto fn = encode_fn();
-  if (!fn) {
-    *err = "cuTensorMapEncodeTiled unavailable";
-    return false;
-  }
-  if (rows < 1) rows = 1;
-  cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)H, (cuuint64_t)rows};
-  cuuint64_t strides[2] = {(cuuint64_t)d * 4, (cuuint64_t)H * d * 4};
-  cuuint32_t box[3] = {(cuuint32_t)d, 1, (cuuint32_t)box_rows};
-  cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, estr,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-                  CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) {
-    *err = "cuTensorMapEncodeTiled failed (fp32 rows)";
     return false;
   }
   return true;
