@@ -125,6 +125,20 @@ cp_status_t cp_zigzag_scatter(const void* src, void* dst, size_t row_bytes, cons
                               int n_rows, void* stream);
 
 /*
+ * cp_copy_rows -- strided row copy between host and device memory (either
+ * direction, or device to device), asynchronous on `stream`: for r < rows,
+ * width bytes from src + r * src_pitch to dst + r * dst_pitch.  Not part of
+ * the method: it moves a range of heads of a [T][H][d] tensor (width =
+ * heads x d x element size, pitch = H x d x element size) so that a host
+ * caller can stream the heads of a large problem through the device in
+ * chunks, copies of one chunk overlapping the kernels of another.  Host
+ * memory must be page-locked for the copy to be asynchronous.
+ * Errors: CP_ERR_INVALID_ARG (null pointer, width > a pitch), CP_ERR_CUDA.
+ */
+cp_status_t cp_copy_rows(void* dst, size_t dst_pitch, const void* src, size_t src_pitch,
+                         size_t width, size_t rows, void* stream);
+
+/*
  * cp_attn_fwd -- context-parallel causal attention forward.
  * CP-VLM page §1.1 (zigzag split), §1 (Ring Attention), §4.1 (replicated
  * prefix), §5.3 (cu_seqlens).

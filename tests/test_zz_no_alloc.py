@@ -84,6 +84,26 @@ def test_noalloc_forward_matches_oracle_and_workspace_forward_twice(P, N, texts,
                          r[2].cpu().double() + r[0].cpu().double(), "bf16")
 
 
+def test_noalloc_forward_scale_one_uses_the_f16_copy_of_v():
+    """Softmax scale 1 on pre-scaled queries: PV on f16 operands, with the f16
+    copy of V and its factors held in the fixed scratch."""
+    import vlm_zigzag_head_gb300 as cp
+    P, N, texts, H, d = 3, 37, [384, 0, 192], 2, 128
+    cu = _cu(N, texts)
+    q, k, v = _inputs(cu, H, d, torch.bfloat16, 23)
+    q = (q.float() * d ** -0.5).to(torch.bfloat16)
+    o_ref, l_ref = oracle.causal_attention_fwd(q, k, v, cu, 1.0)
+    qd, kd, vd = (x.to(DEV) for x in (q, k, v))
+    r = cp.cp_attn_fwd(qd, kd, vd, cu, P, N, 1.0)
+    out, lse = cp.cp_attn_fwd_noalloc(qd, kd, vd, cu, P, N, 1.0)
+    torch.cuda.synchronize()
+    assert cp.cp_workspace_status() == 0
+    assert_close("out vs oracle", out.cpu(), o_ref, "bf16")
+    assert_close("lse vs oracle", lse.cpu(), l_ref, "bf16")
+    assert torch.equal(out.cpu().view(torch.int16), r[0].cpu().view(torch.int16))
+    assert torch.equal(lse.cpu(), r[1].cpu())
+
+
 def test_noalloc_forward_rejects_problems_beyond_its_scratch():
     from vlm_zigzag_head_gb300 import _binding as B
     cu = [0, 65536]

@@ -36,6 +36,8 @@ SIGNATURES = {
                                        c_vp, ctypes.c_int, c_vp]),
     "cp_zigzag_gather": (ctypes.c_int, [c_vp, c_vp, ctypes.c_size_t, c_vp, ctypes.c_int, c_vp]),
     "cp_zigzag_scatter": (ctypes.c_int, [c_vp, c_vp, ctypes.c_size_t, c_vp, ctypes.c_int, c_vp]),
+    "cp_copy_rows": (ctypes.c_int, [c_vp, ctypes.c_size_t, c_vp, ctypes.c_size_t, ctypes.c_size_t,
+                                    ctypes.c_size_t, c_vp]),
     "cp_attn_fwd_workspace_size": (ctypes.c_size_t, [ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                                      ctypes.c_int, c_i32p, ctypes.c_int,
                                                      ctypes.c_int, ctypes.c_int, ctypes.c_float]),

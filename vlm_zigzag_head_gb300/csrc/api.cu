@@ -626,6 +626,17 @@ cp_status_t cp_attn_fwd_gqa(const void* q, const void* k, const void* v, cp_dtyp
   return CP_OK;
 }
 
+cp_status_t cp_copy_rows(void* dst, size_t dst_pitch, const void* src, size_t src_pitch,
+                         size_t width, size_t rows, void* stream) {
+  if (rows == 0 || width == 0) return CP_OK;
+  if (!dst || !src) return fail(CP_ERR_INVALID_ARG, "NULL pointer");
+  if (width > dst_pitch || width > src_pitch) return fail(CP_ERR_INVALID_ARG, "width > pitch");
+  CP_CUDA(cudaMemcpy2DAsync(dst, dst_pitch, src, src_pitch, width, rows, cudaMemcpyDefault,
+                            static_cast<cudaStream_t>(stream)),
+          "strided row copy");
+  return CP_OK;
+}
+
 cp_status_t cp_lse_merge(int n_parts, const float* part_out, const float* part_lse, int rows,
                          int H, int d, void* out, cp_dtype_t out_dt, float* lse, void* stream) {
   if (n_parts < 1 || rows < 0 || H < 1 || d < 1 || d > 128)
