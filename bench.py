@@ -376,6 +376,23 @@ def run_cuda(args, w, rank, world, dist):
             kernels[k]["hbm_frac"] = kernels[k]["achieved_gbs"] / hbm
     gpu_launches = sum(n for _, n in prof.values())
 
+    # the standalone LSE merge (cp_lse_merge; inside the step the merge is the
+    # forward's online softmax): P partial results of one rank's rows, fp32,
+    # merged into bf16 out and fp32 lse, timed on its own
+    R = max(1, T // P)
+    parts_o = torch.randn((P, R, H, d), device=dev)
+    parts_l = torch.randn((P, H, R), device=dev)
+    m_out = torch.empty((R, H, d), dtype=torch.bfloat16, device=dev)
+    m_lse = torch.empty((H, R), dtype=torch.float32, device=dev)
+    merge_ms = timed(lambda: cp.cp_lse_merge(parts_o, parts_l, torch.bfloat16, out=m_out,
+                                             lse=m_lse), 5)
+    merge_bytes = P * R * H * (d + 1) * 4 + R * H * (d * 2 + 4)
+    kernels["lse_merge"] = {"launches": 5, "ms_per_launch": merge_ms, "standalone": True,
+                            "shape": [P, R, H, d], "bytes_per_launch": merge_bytes,
+                            "achieved_gbs": merge_bytes / (merge_ms / 1e3) / 1e9,
+                            "hbm_frac": merge_bytes / (merge_ms / 1e3) / 1e9 / hbm}
+    del parts_o, parts_l
+
     # ---- end to end through the public API with host buffers
     e2e = None
     if not args.no_e2e:

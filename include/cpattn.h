@@ -236,7 +236,9 @@ cp_status_t cp_attn_fwd_noalloc(const void* q, const void* k, const void* v, cp_
  * on in §1 and §4.1 step 5):
  *     lse = log sum_p exp(lse_p),   out = sum_p exp(lse_p - lse) * out_p.
  * A part with lse = -inf contributes nothing; if every part is -inf the row
- * gets lse = -inf and out = 0.  Parts are folded in index order.
+ * gets lse = -inf and out = 0.  The merged lse comes first (the largest
+ * lse_p, then the sum of exp(lse_p - max)); out then sums the parts in index
+ * order, each read once (16-byte loads when d is a multiple of 4).
  *
  *   part_out  [n_parts][rows][H][d] fp32       part_lse [n_parts][H][rows] fp32
  *   out       [rows][H][d], dtype out_dt       lse      [H][rows] fp32

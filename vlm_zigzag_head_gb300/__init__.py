@@ -215,13 +215,16 @@ def cp_attn_fwd_noalloc(q, k, v, cu_seqlens, P: int, prefix_len: int, softmax_sc
     return out, lse
 
 
-def cp_lse_merge(part_out: torch.Tensor, part_lse: torch.Tensor, out_dtype=torch.float32):
+def cp_lse_merge(part_out: torch.Tensor, part_lse: torch.Tensor, out_dtype=torch.float32,
+                 out=None, lse=None):
     """Merge ``part_out [n,rows,H,d]`` / ``part_lse [n,H,rows]`` (fp32) into
-    ``(out [rows,H,d], lse [H,rows])`` by log-sum-exp."""
-    _need_cuda(part_out, part_lse)
+    ``(out [rows,H,d], lse [H,rows])`` by log-sum-exp (outputs may be passed in)."""
+    _need_cuda(part_out, part_lse, out, lse)
     n, rows, H, d = part_out.shape
-    out = torch.empty((rows, H, d), dtype=out_dtype, device=part_out.device)
-    lse = torch.empty((H, rows), dtype=torch.float32, device=part_out.device)
+    if out is None:
+        out = torch.empty((rows, H, d), dtype=out_dtype, device=part_out.device)
+    if lse is None:
+        lse = torch.empty((H, rows), dtype=torch.float32, device=part_out.device)
     _b.check(_b.lib().cp_lse_merge(n, _ptr(part_out), _ptr(part_lse), rows, H, d, _ptr(out),
                                    _dt(out), _ptr(lse), _stream(part_out.device)))
     return out, lse
@@ -370,60 +373,134 @@ def _side_streams(dev):
     return _side[key]
 
 
+def host_chunks(T: int, H: int, H_kv: int, d: int, elem: int) -> int:
+    """Head chunks of :func:`attention_host`: 4 (or 2) when the problem's
+    tensors exceed 256 MB, so that one chunk's copies hide behind another's
+    kernels; 1 for smaller problems, whose launches would shrink too far."""
+    if T * (2 * H + 2 * H_kv) * d * elem < (256 << 20):
+        return 1
+    for n in (4, 2):
+        if H_kv % n == 0:
+            return n
+    return 1
+
+
+def _copy_rows(dst, dst_off, dst_pitch, src, src_off, src_pitch, width, rows, stream):
+    _b.check(_b.lib().cp_copy_rows(ctypes.c_void_p(dst.data_ptr() + dst_off), dst_pitch,
+                                   ctypes.c_void_p(src.data_ptr() + src_off), src_pitch,
+                                   width, rows, ctypes.c_void_p(stream.cuda_stream)))
+
+
 def attention_host(q, k, v, dout, cu_seqlens, P: int, prefix_len: int, softmax_scale: float,
-                   device="cuda", host_out=None):
+                   device="cuda", host_out=None, chunks: int = 0):
     """End-to-end call on host tensors (pinned for asynchronous copies): copy the
     inputs to ``device``, run forward (and backward when ``dout`` is given),
-    copy results back.  Returns host tensors ``(out, lse[, dq, dk, dv])``.
+    copy results back.  Returns host tensors ``(out, lse[, dq, dk, dv])``;
+    ``host_out`` may supply them (pinned).  ``k``, ``v`` may have fewer heads
+    than ``q`` (grouped KV heads).
 
-    The copies overlap the kernels: q, k, v go up first on a copy stream and
-    the forward starts once they have landed; dO goes up on the same stream
-    while the forward runs; out and lse come down on a second copy stream
-    while the backward runs; the gradients come down after it.  Events order
-    every copy against the kernels that write or read its tensor."""
+    Heads are independent, so the call streams them through the device in
+    ``chunks`` groups of KV heads (default :func:`host_chunks`), two groups'
+    buffers in flight: while the kernels of one group run on the current
+    stream, the next group's q, k, v, dO go up on one copy stream and the
+    previous group's results come down on another (strided row copies of the
+    head range, ``cp_copy_rows``).  Within a group, dO goes up while the
+    forward runs and out, lse come down while the backward runs.  Events order
+    every copy against the kernels that write or read its buffers."""
     dev = torch.device(device)
     comp = torch.cuda.current_stream(dev)
     up, down = _side_streams(dev)
-    up.wait_stream(comp)            # device memory freed by earlier work on comp
-    with torch.cuda.stream(up):
-        qd, kd, vd = (x.to(dev, non_blocking=True) for x in (q, k, v))
-        ev_qkv = torch.cuda.Event()
-        ev_qkv.record(up)
-        dod = dout.to(dev, non_blocking=True) if dout is not None else None
-        ev_do = torch.cuda.Event()
-        ev_do.record(up)
-    comp.wait_event(ev_qkv)
-    for t in (qd, kd, vd):
-        t.record_stream(comp)
-    keep = dout is not None and qd.dtype == torch.bfloat16
-    r = cp_attn_fwd(qd, kd, vd, cu_seqlens, P, prefix_len, softmax_scale, residual=keep)
-    out, lse = r[0], r[1]
-    n_res = 5 if dout is not None else 2
+    T, H, d = q.shape
+    Hkv = k.shape[1]
+    dt = q.dtype
+    elem = q.element_size()
+    bwd = dout is not None
+    keep = bwd and dt == torch.bfloat16
+    n = chunks or host_chunks(T, H, Hkv, d, elem)
+    if Hkv % n != 0:
+        raise ValueError("chunks must divide the KV heads")
+    Gc, Hc = Hkv // n, H // n          # KV and query heads per chunk
+    n_res = 5 if bwd else 2
     if host_out is None:
-        shapes = [(out.shape, out.dtype), (lse.shape, lse.dtype)]
-        if dout is not None:
-            shapes += [(qd.shape, torch.float32), (kd.shape, torch.float32),
-                       (kd.shape, torch.float32)]
-        host_out = [torch.empty(sh, dtype=dt, pin_memory=True) for sh, dt in shapes]
-    ev_fwd = torch.cuda.Event()
-    ev_fwd.record(comp)
-    down.wait_event(ev_fwd)
-    with torch.cuda.stream(down):
-        for h, t in zip(host_out[:2], (out, lse)):
-            h.copy_(t, non_blocking=True)
-            t.record_stream(down)
-    if dout is not None:
-        comp.wait_event(ev_do)
-        dod.record_stream(comp)
-        grads = cp_attn_bwd(qd, kd, vd, out, lse, dod, cu_seqlens, P, prefix_len, softmax_scale,
-                            out_lo=r[2] if keep else None)
-        ev_bwd = torch.cuda.Event()
-        ev_bwd.record(comp)
-        down.wait_event(ev_bwd)
-        with torch.cuda.stream(down):
-            for h, t in zip(host_out[2:n_res], grads):
-                h.copy_(t, non_blocking=True)
-                t.record_stream(down)
+        shapes = [((T, H, d), dt), ((H, T), torch.float32)]
+        if bwd:
+            shapes += [((T, H, d), torch.float32), ((T, Hkv, d), torch.float32),
+                       ((T, Hkv, d), torch.float32)]
+        host_out = [torch.empty(sh, dtype=dt_, pin_memory=True) for sh, dt_ in shapes]
+    # device buffers of up to two chunks in flight
+    nb = min(2, n)
+    sets = []
+    for _ in range(nb):
+        st = {"q": torch.empty((T, Hc, d), dtype=dt, device=dev),
+              "k": torch.empty((T, Gc, d), dtype=dt, device=dev),
+              "v": torch.empty((T, Gc, d), dtype=dt, device=dev),
+              "out": torch.empty((T, Hc, d), dtype=dt, device=dev),
+              "lse": torch.empty((Hc, T), dtype=torch.float32, device=dev)}
+        if keep:
+            st["lo"] = torch.empty((T, Hc, d), dtype=dt, device=dev)
+        if bwd:
+            st["do"] = torch.empty((T, Hc, d), dtype=dt, device=dev)
+            st["dq"] = torch.empty((T, Hc, d), dtype=torch.float32, device=dev)
+            st["dk"] = torch.empty((T, Gc, d), dtype=torch.float32, device=dev)
+            st["dv"] = torch.empty((T, Gc, d), dtype=torch.float32, device=dev)
+        sets.append(st)
+    ready = torch.cuda.Event()
+    ready.record(comp)               # buffers allocated (and earlier work) on comp
+    up.wait_event(ready)
+    down.wait_event(ready)
+    freed = [None] * nb              # per set: its last results have come down
+    qrow, krow = H * d, Hkv * d      # elements per host row
+    for c in range(n):
+        S = sets[c % nb]
+        h0, g0 = c * Hc, c * Gc
+        # ---- inputs up
+        if freed[c % nb] is not None:
+            up.wait_event(freed[c % nb])
+        for name, src, row, heads, h in (("q", q, qrow, Hc, h0), ("k", k, krow, Gc, g0),
+                                         ("v", v, krow, Gc, g0)):
+            _copy_rows(S[name], 0, heads * d * elem, src, h * d * elem, row * elem,
+                       heads * d * elem, T, up)
+        ev_in = torch.cuda.Event()
+        ev_in.record(up)
+        if bwd:
+            _copy_rows(S["do"], 0, Hc * d * elem, dout, h0 * d * elem, qrow * elem,
+                       Hc * d * elem, T, up)
+            ev_do = torch.cuda.Event()
+            ev_do.record(up)
+        # ---- kernels
+        comp.wait_event(ev_in)
+        cp_attn_fwd_gqa(S["q"], S["k"], S["v"], cu_seqlens, P, prefix_len, softmax_scale,
+                        out=S["out"], lse=S["lse"], residual=keep,
+                        out_lo=S["lo"] if keep else None)
+        ev_fwd = torch.cuda.Event()
+        ev_fwd.record(comp)
+        if bwd:
+            comp.wait_event(ev_do)
+            cp_attn_bwd_gqa(S["q"], S["k"], S["v"], S["out"], S["lse"], S["do"], cu_seqlens, P,
+                            prefix_len, softmax_scale, grads=(S["dq"], S["dk"], S["dv"]),
+                            out_lo=S["lo"] if keep else None)
+            ev_bwd = torch.cuda.Event()
+            ev_bwd.record(comp)
+        # ---- results down
+        down.wait_event(ev_fwd)
+        _copy_rows(host_out[0], h0 * d * elem, qrow * elem, S["out"], 0, Hc * d * elem,
+                   Hc * d * elem, T, down)
+        _copy_rows(host_out[1], h0 * T * 4, Hc * T * 4, S["lse"], 0, Hc * T * 4,
+                   Hc * T * 4, 1, down)
+        if bwd:
+            down.wait_event(ev_bwd)
+            for i, (name, row, heads, h) in enumerate((("dq", qrow, Hc, h0),
+                                                       ("dk", krow, Gc, g0),
+                                                       ("dv", krow, Gc, g0))):
+                _copy_rows(host_out[2 + i], h * d * 4, row * 4, S[name], 0, heads * d * 4,
+                           heads * d * 4, T, down)
+        ev = torch.cuda.Event()
+        ev.record(down)
+        freed[c % nb] = ev
+        # the next use of this set's outputs by the kernels waits for the
+        # copies down: its inputs go up only after `freed`, and the kernels
+        # wait for the inputs
     down.synchronize()
+    up.synchronize()
     comp.synchronize()
     return tuple(host_out[:n_res])

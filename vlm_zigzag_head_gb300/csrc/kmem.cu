@@ -130,6 +130,81 @@ __global__ void __launch_bounds__(kThreads) lse_merge_kernel(int n_parts,
   }
 }
 
+__device__ __forceinline__ float warp_max(float x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
+  return x;
+}
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+  return x;
+}
+
+// d a multiple of 4: one warp per (row, head), 4 consecutive elements per
+// lane (16-byte loads).  The merged lse comes first (max, then the sum of
+// exp(lse_p - max), both over the parts in lanes), then every part's row is
+// read once with its weight exp(lse_p - lse): the parts' loads do not wait on
+// one another.
+__global__ void __launch_bounds__(kThreads) lse_merge_v4_kernel(int n_parts,
+                                                                const float* __restrict__ po,
+                                                                const float* __restrict__ pl,
+                                                                int rows, int H, int d, void* out,
+                                                                int out_bf16, float* lse) {
+  const int lane = threadIdx.x & 31;
+  const long long pairs = (long long)rows * H;
+  const long long stride_o = (long long)rows * H * d;
+  const long long stride_l = (long long)rows * H;
+  const bool mine = lane * 4 < d;
+  for (long long w = (long long)blockIdx.x * (kThreads / 32) + threadIdx.x / 32; w < pairs;
+       w += (long long)gridDim.x * (kThreads / 32)) {
+    const int h = (int)(w / rows);
+    const long long row = w - (long long)h * rows;
+    const float* lp = pl + (long long)h * rows + row;
+    float m = -INFINITY;
+    for (int p = lane; p < n_parts; p += 32) m = fmaxf(m, lp[p * stride_l]);
+    m = warp_max(m);
+    const long long o = (row * H + h) * (long long)d + lane * 4;
+    if (m == -INFINITY) {   // no part saw a key
+      if (mine) {
+        if (out_bf16) *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(out) + o) =
+            make_uint2(0u, 0u);
+        else *reinterpret_cast<float4*>(reinterpret_cast<float*>(out) + o) =
+            make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+      if (lane == 0) lse[(long long)h * rows + row] = -INFINITY;
+      continue;
+    }
+    float sum = 0.f;
+    for (int p = lane; p < n_parts; p += 32) sum += expf(lp[p * stride_l] - m);
+    const float l_tot = m + logf(warp_sum(sum));
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    const float* src = po + (row * H + h) * (long long)d + lane * 4;
+#pragma unroll 4
+    for (int p = 0; p < n_parts; ++p) {
+      const float wgt = expf(lp[p * stride_l] - l_tot);   // 0 for a part with lse = -inf
+      if (mine) {
+        const float4 x = __ldg(reinterpret_cast<const float4*>(src + p * stride_o));
+        acc.x = fmaf(wgt, x.x, acc.x);
+        acc.y = fmaf(wgt, x.y, acc.y);
+        acc.z = fmaf(wgt, x.z, acc.z);
+        acc.w = fmaf(wgt, x.w, acc.w);
+      }
+    }
+    if (mine) {
+      if (out_bf16) {
+        const __nv_bfloat162 a = __floats2bfloat162_rn(acc.x, acc.y);
+        const __nv_bfloat162 b = __floats2bfloat162_rn(acc.z, acc.w);
+        *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(out) + o) =
+            make_uint2(*reinterpret_cast<const uint32_t*>(&a), *reinterpret_cast<const uint32_t*>(&b));
+      } else {
+        *reinterpret_cast<float4*>(reinterpret_cast<float*>(out) + o) = acc;
+      }
+    }
+    if (lane == 0) lse[(long long)h * rows + row] = l_tot;
+  }
+}
+
 template <typename T>
 __device__ __forceinline__ float to_f(T x);
 template <>
@@ -399,8 +474,12 @@ cudaError_t launch_lse_merge(int n_parts, const float* po, const float* pl, int 
                              int d, void* out, bool out_bf16, float* lse, cudaStream_t st) {
   const long long pairs = (long long)rows * H;
   if (pairs == 0) return cudaSuccess;
-  lse_merge_kernel<<<grid_for(pairs, kThreads / 32), kThreads, 0, st>>>(
-      n_parts, po, pl, rows, H, d, out, out_bf16 ? 1 : 0, lse);
+  if (d % 4 == 0 && d <= 128)
+    lse_merge_v4_kernel<<<grid_for(pairs, kThreads / 32), kThreads, 0, st>>>(
+        n_parts, po, pl, rows, H, d, out, out_bf16 ? 1 : 0, lse);
+  else
+    lse_merge_kernel<<<grid_for(pairs, kThreads / 32), kThreads, 0, st>>>(
+        n_parts, po, pl, rows, H, d, out, out_bf16 ? 1 : 0, lse);
   return cudaGetLastError();
 }
 
