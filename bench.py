@@ -409,9 +409,20 @@ def run_cuda(args, w, rank, world, dist):
         e2e_s = (time.perf_counter() - t0) / n_e2e
         h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hdo))
         d2h = sum(t.numel() * t.element_size() for t in host_out)
+        # this box's pinned copy rates (one 1 GiB copy each way, outside the
+        # timed steps): with every copy hidden behind the kernels the step is
+        # bounded below by the slower direction's bytes at its rate
+        buf_h = torch.empty(1 << 30, dtype=torch.uint8).pin_memory()
+        buf_d = torch.empty(1 << 30, dtype=torch.uint8, device=dev)
+        h2d_ms = timed(lambda: buf_d.copy_(buf_h, non_blocking=True), 2)
+        d2h_ms = timed(lambda: buf_h.copy_(buf_d, non_blocking=True), 2)
+        del buf_h, buf_d
+        rate_h2d, rate_d2h = (1 << 30) / (h2d_ms / 1e3) / 1e9, (1 << 30) / (d2h_ms / 1e3) / 1e9
         e2e = {"value": world * total / e2e_s / 1e12, "unit": "TFLOP/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-               "ms_per_step": e2e_s * 1e3}
+               "ms_per_step": e2e_s * 1e3,
+               "pinned_copy_gbs": {"h2d": rate_h2d, "d2h": rate_d2h},
+               "copy_floor_ms": max(h2d / rate_h2d, d2h / rate_d2h) / 1e6}
 
     # ---- the other bf16 workloads of the method (parity configs, measured the
     # same way at fewer steps): fwd, bwd and fwd+bwd rates, and the oracle's

@@ -373,6 +373,14 @@ def _side_streams(dev):
     return _side[key]
 
 
+_host_bufs = {}
+
+
+def release_host_buffers():
+    """Free the device buffers :func:`attention_host` keeps between calls."""
+    _host_bufs.clear()
+
+
 def host_chunks(T: int, H: int, H_kv: int, d: int, elem: int) -> int:
     """Head chunks of :func:`attention_host`: 4 (or 2) when the problem's
     tensors exceed 256 MB, so that one chunk's copies hide behind another's
@@ -427,23 +435,29 @@ def attention_host(q, k, v, dout, cu_seqlens, P: int, prefix_len: int, softmax_s
             shapes += [((T, H, d), torch.float32), ((T, Hkv, d), torch.float32),
                        ((T, Hkv, d), torch.float32)]
         host_out = [torch.empty(sh, dtype=dt_, pin_memory=True) for sh, dt_ in shapes]
-    # device buffers of up to two chunks in flight
+    # device buffers of up to two chunks in flight, kept for the next call of
+    # the same shape (release_host_buffers() frees them)
     nb = min(2, n)
-    sets = []
-    for _ in range(nb):
-        st = {"q": torch.empty((T, Hc, d), dtype=dt, device=dev),
-              "k": torch.empty((T, Gc, d), dtype=dt, device=dev),
-              "v": torch.empty((T, Gc, d), dtype=dt, device=dev),
-              "out": torch.empty((T, Hc, d), dtype=dt, device=dev),
-              "lse": torch.empty((Hc, T), dtype=torch.float32, device=dev)}
-        if keep:
-            st["lo"] = torch.empty((T, Hc, d), dtype=dt, device=dev)
-        if bwd:
-            st["do"] = torch.empty((T, Hc, d), dtype=dt, device=dev)
-            st["dq"] = torch.empty((T, Hc, d), dtype=torch.float32, device=dev)
-            st["dk"] = torch.empty((T, Gc, d), dtype=torch.float32, device=dev)
-            st["dv"] = torch.empty((T, Gc, d), dtype=torch.float32, device=dev)
-        sets.append(st)
+    key = (str(dev), T, Hc, Gc, d, dt, bwd, keep)
+    sets = _host_bufs.get(key)
+    if sets is None:
+        _host_bufs.clear()
+        sets = []
+        for _ in range(nb):
+            st = {"q": torch.empty((T, Hc, d), dtype=dt, device=dev),
+                  "k": torch.empty((T, Gc, d), dtype=dt, device=dev),
+                  "v": torch.empty((T, Gc, d), dtype=dt, device=dev),
+                  "out": torch.empty((T, Hc, d), dtype=dt, device=dev),
+                  "lse": torch.empty((Hc, T), dtype=torch.float32, device=dev)}
+            if keep:
+                st["lo"] = torch.empty((T, Hc, d), dtype=dt, device=dev)
+            if bwd:
+                st["do"] = torch.empty((T, Hc, d), dtype=dt, device=dev)
+                st["dq"] = torch.empty((T, Hc, d), dtype=torch.float32, device=dev)
+                st["dk"] = torch.empty((T, Gc, d), dtype=torch.float32, device=dev)
+                st["dv"] = torch.empty((T, Gc, d), dtype=torch.float32, device=dev)
+            sets.append(st)
+        _host_bufs[key] = sets
     ready = torch.cuda.Event()
     ready.record(comp)               # buffers allocated (and earlier work) on comp
     up.wait_event(ready)
