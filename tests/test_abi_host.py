@@ -125,6 +125,17 @@ def test_bad_arguments_return_status(cplib):
     assert L.cp_status_string(7) == b"CP_ERR_TIMEOUT"
 
 
+def test_copy_rows_arguments(cplib):
+    """cp_copy_rows checks its arguments before any CUDA call: nothing to copy
+    is CP_OK, a null pointer or a row wider than a pitch is CP_ERR_INVALID_ARG."""
+    L = cplib
+    p = ctypes.c_void_p(1 << 20)
+    assert L.cp_copy_rows(p, 64, p, 64, 64, 0, None) == 0
+    assert L.cp_copy_rows(None, 64, p, 64, 64, 4, None) == 1
+    assert L.cp_copy_rows(p, 32, p, 64, 64, 4, None) == 1
+    assert b"pitch" in L.cp_last_error()
+
+
 def test_grouped_kv_arguments(cplib):
     """The grouped-KV entry points: H must be a positive multiple of H_kv, the
     KV-side workspace shrinks with H_kv, and H_kv == H sizes like the plain
