@@ -416,12 +416,26 @@ def run_cuda(args, w, rank, world, dist):
         buf_d = torch.empty(1 << 30, dtype=torch.uint8, device=dev)
         h2d_ms = timed(lambda: buf_d.copy_(buf_h, non_blocking=True), 2)
         d2h_ms = timed(lambda: buf_h.copy_(buf_d, non_blocking=True), 2)
+        # the strided row copies of the head-chunk pipeline (one chunk of q)
+        n_ch = cp.host_chunks(T, H, Hkv, d, 2)
+        wid, pitch = (H // n_ch) * d * 2, H * d * 2
+        rows = min(T, (1 << 30) // pitch)
+        def rows_copy(up_):
+            dst, src = (buf_d, buf_h) if up_ else (buf_h, buf_d)
+            cp._copy_rows(dst, 0, pitch, src, 0, pitch, wid, rows, stream)
+        h2d_rows_ms = timed(lambda: rows_copy(True), 2)
+        d2h_rows_ms = timed(lambda: rows_copy(False), 2)
         del buf_h, buf_d
-        rate_h2d, rate_d2h = (1 << 30) / (h2d_ms / 1e3) / 1e9, (1 << 30) / (d2h_ms / 1e3) / 1e9
+        rate = lambda nb, ms: nb / (ms / 1e3) / 1e9  # noqa: E731
+        rate_h2d, rate_d2h = rate(1 << 30, h2d_ms), rate(1 << 30, d2h_ms)
         e2e = {"value": world * total / e2e_s / 1e12, "unit": "TFLOP/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "ms_per_step": e2e_s * 1e3,
-               "pinned_copy_gbs": {"h2d": rate_h2d, "d2h": rate_d2h},
+               "pinned_copy_gbs": {"h2d": rate_h2d, "d2h": rate_d2h,
+                                   "h2d_rows": rate(wid * rows, h2d_rows_ms),
+                                   "d2h_rows": rate(wid * rows, d2h_rows_ms),
+                                   "row_bytes": wid, "pitch": pitch},
+               "chunks": n_ch,
                "copy_floor_ms": max(h2d / rate_h2d, d2h / rate_d2h) / 1e6}
 
     # ---- the other bf16 workloads of the method (parity configs, measured the
