@@ -408,11 +408,11 @@ def attention_host(q, k, v, dout, cu_seqlens, P: int, prefix_len: int, softmax_s
     than ``q`` (grouped KV heads).
 
     Heads are independent, so the call streams them through the device in
-    ``chunks`` groups of KV heads (default :func:`host_chunks`), two groups'
-    buffers in flight: while the kernels of one group run on the current
-    stream, the next group's q, k, v, dO go up on one copy stream and the
-    previous group's results come down on another (strided row copies of the
-    head range, ``cp_copy_rows``).  Within a group, dO goes up while the
+    ``chunks`` groups of KV heads (default :func:`host_chunks`), each with its
+    own device buffers: while the kernels of one group run on the current
+    stream, later groups' q, k, v, dO go up on one copy stream and earlier
+    groups' results come down on another (strided row copies of the head
+    range, ``cp_copy_rows``).  Within a group, dO goes up while the
     forward runs and out, lse come down while the backward runs.  Events order
     every copy against the kernels that write or read its buffers."""
     dev = torch.device(device)
@@ -435,9 +435,11 @@ def attention_host(q, k, v, dout, cu_seqlens, P: int, prefix_len: int, softmax_s
             shapes += [((T, H, d), torch.float32), ((T, Hkv, d), torch.float32),
                        ((T, Hkv, d), torch.float32)]
         host_out = [torch.empty(sh, dtype=dt_, pin_memory=True) for sh, dt_ in shapes]
-    # device buffers of up to two chunks in flight, kept for the next call of
-    # the same shape (release_host_buffers() frees them)
-    nb = min(2, n)
+    # device buffers of every chunk (the footprint of the unchunked call), so
+    # that no upload waits for an earlier chunk's download: a copy that stalls
+    # delays only its own chunk.  Kept for the next call of the same shape
+    # (release_host_buffers() frees them).
+    nb = n
     key = (str(dev), T, Hc, Gc, d, dt, bwd, keep)
     sets = _host_bufs.get(key)
     if sets is None:
