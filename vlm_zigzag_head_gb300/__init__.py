@@ -414,7 +414,9 @@ def attention_host(q, k, v, dout, cu_seqlens, P: int, prefix_len: int, softmax_s
     groups' results come down on another (strided row copies of the head
     range, ``cp_copy_rows``).  Within a group, dO goes up while the
     forward runs and out, lse come down while the backward runs.  Events order
-    every copy against the kernels that write or read its buffers."""
+    every copy against the kernels that write or read its buffers.  The
+    device buffers are cached per shape, so concurrent calls from several
+    host threads must be serialised by the caller."""
     dev = torch.device(device)
     comp = torch.cuda.current_stream(dev)
     up, down = _side_streams(dev)
