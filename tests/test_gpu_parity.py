@@ -159,6 +159,7 @@ EDGE = [
     (3, 37, [384, 0, 1152], 2, 128),   # text-less sample, c = 64 / 192 (ragged)
     (8, 0, [2048], 2, 128),            # P = 8
     (2, 300, [0], 2, 128),             # prefix only
+    (2, 4, [8] * 200, 1, 64),          # 200 packed samples (index kernel batches of 192)
 ]
 
 
