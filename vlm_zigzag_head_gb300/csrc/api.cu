@@ -744,9 +744,9 @@ cp_status_t cp_attn_bwd_gqa(const void* q, const void* k, const void* v, const v
   if (tc) {
     CP_CUDA(cudaMemsetAsync(dq, 0, (size_t)T * H * d * sizeof(float), st), "clear dq");
     // With grouped KV heads one CTA walks all G query heads of its KV head.
-    // When that leaves too few CTAs to fill the GPU (under ~4 per SM per
-    // step), the group is shared by kv_split CTAs whose partial dK / dV are
-    // reduce-added into zeroed memory.
+    // When that leaves too few CTAs to fill the GPU (under ~4 per SM), the
+    // group is shared by kv_split CTAs whose partial dK / dV are reduce-added
+    // into zeroed memory.
     const int G = H / Hkv;
     int kv_split = 1;
     {
