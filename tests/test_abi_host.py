@@ -35,6 +35,18 @@ def test_library_exports_every_declared_symbol(cplib):
     assert set(B.SIGNATURES) >= names
 
 
+def test_bounds_checked_library_builds_and_exports_every_symbol():
+    """The debug build (-DCPATTN_BOUNDS_CHECK) compiles from the same sources
+    and exports the same C ABI; its kernels run in the -m gpu tests."""
+    from vlm_zigzag_head_gb300 import build
+    path = build.build(checked=True)
+    lib = ctypes.CDLL(path)
+    for n in _declared_symbols():
+        assert hasattr(lib, n), n
+    lib.cp_status_string.restype = ctypes.c_char_p
+    assert lib.cp_status_string(9) == b"CP_ERR_BOUNDS"
+
+
 def _cu(prefix, texts):
     cu = [0]
     for L in texts:
