@@ -255,9 +255,13 @@ cp_status_t cp_lse_merge(int n_parts, const float* part_out, const float* part_l
  * text dK/dV are accumulated for the rank that owns the KV (on chip over all
  * ring steps, in ring-step order, and written once).  At step 0 each
  * rank produces its own gradient of the replicated prefix K/V; these per-rank
- * gradients and the prefix queries' own term are summed in fixed order
- * (ranks 0..P-1, then the prefix-query term) -- the single-GPU stand-in for
- * the page's AllReduce.
+ * gradients and the prefix queries' own term are summed -- the single-GPU
+ * stand-in for the page's AllReduce.  With prefix_grad_per_rank (and on the
+ * CP_F32 path) each term is kept in its own slot and a separate kernel sums
+ * the slots in fixed order (ranks 0..P-1, then the prefix-query term).
+ * Without it, the CP_BF16 path sums the terms on chip: one work item per
+ * prefix key tile walks every rank's query runs in a fixed order and writes
+ * the sum (no slot memory, no separate pass).
  *
  *   q, k, v, out, dout  [T][H][d], dtype dt;  lse [H][T] fp32 (from cp_attn_fwd)
  *   out_lo              NULL, or the remainder written by cp_attn_fwd: then

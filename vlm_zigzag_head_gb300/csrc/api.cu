@@ -129,6 +129,7 @@ struct PlanSet {
   FwdPlan fwd_nat;   // text rows in natural order (fp32 dQ pass)
   BwdPlan bwd;
   FusedBwdPlan bwd_fused;   // bwd with all ring steps of a key tile in one item (128-query kernel)
+  FusedBwdPlan bwd_fused_merged;   // the same with each prefix key tile's slots in one item
   std::vector<int32_t> samples;  // [n][4]: t0, c, off, ord0 (index kernel)
   std::mutex ul_mu;
   std::vector<std::shared_ptr<const UnitLists>> ul;  // recent unit lists
@@ -182,7 +183,8 @@ cp_status_t get_plans(const int32_t* cu, int n_seqs, int N, int P, int T, int H,
   plan_forward_fused(ps->fwd2, P, &ps->fused);
   plan_forward(pb, false, &ps->fwd_nat);
   plan_backward(pb, &ps->bwd);
-  plan_backward_fused(ps->bwd, P, 128, &ps->bwd_fused);
+  plan_backward_fused(ps->bwd, P, 128, false, &ps->bwd_fused);
+  plan_backward_fused(ps->bwd, P, 128, true, &ps->bwd_fused_merged);
   int64_t ord = 0;
   for (int i = 0; i < n_seqs; ++i) {
     ps->samples.push_back(pb.cu[i] + N);
@@ -255,7 +257,9 @@ BwdWs bwd_layout(const PlanSet& ps, int H, int Hkv, int d, bool simt, bool own_s
   w.items = o;
   o = align_up(o + std::max(ps.bwd.items.size(), ps.bwd_fused.items.size()) * sizeof(BwdItem), 256);
   w.runs = o;
-  if (!simt) o = align_up(o + ps.bwd_fused.runs.size() * sizeof(Seg), 256);
+  if (!simt)
+    o = align_up(o + std::max(ps.bwd_fused.runs.size(), ps.bwd_fused_merged.runs.size()) *
+                         sizeof(Seg), 256);
   w.qitems = o;
   if (simt) o = align_up(o + ps.fwd_nat.items.size() * sizeof(FwdItem), 256);
   w.cu = o; o = align_up(o + pb.cu.size() * sizeof(int32_t), 256);
@@ -660,7 +664,10 @@ size_t cp_attn_bwd_workspace_size_gqa(cp_dtype_t dt, int T, int H, int Hkv, int 
   if (!cu || H < 1 || Hkv < 1 || H % Hkv != 0 || (dt != CP_F32 && dt != CP_BF16)) return 0;
   if (get_plans(cu, n_seqs, N, P, T, H, d, &ps) != CP_OK) return 0;
   const bool simt = dt != CP_BF16;   // fp32: the CUDA-core parity path
-  return bwd_layout(*ps, H, Hkv, d, simt, true, !simt && uses_f16_operands(scale)).total;
+  // per-rank prefix slots in the workspace: only the CUDA-core path needs them
+  // when the caller does not ask for them (the tensor-core path then sums the
+  // ranks' prefix terms on chip)
+  return bwd_layout(*ps, H, Hkv, d, simt, simt, !simt && uses_f16_operands(scale)).total;
 }
 
 size_t cp_attn_bwd_workspace_size(cp_dtype_t dt, int T, int H, int d, const int32_t* cu,
@@ -698,7 +705,7 @@ cp_status_t cp_attn_bwd_gqa(const void* q, const void* k, const void* v, const v
   if (tc && (s = check_device_for_bf16()) != CP_OK) return s;
   // above softmax scale 0.25: S^T, dQ and dK on f16 operands (scaled copies of Q, K)
   const bool f16 = tc && uses_f16_operands(scale);
-  const BwdWs L = bwd_layout(*ps, H, Hkv, d, !tc, pgrad == nullptr, f16);
+  const BwdWs L = bwd_layout(*ps, H, Hkv, d, !tc, !tc && pgrad == nullptr, f16);
   if (!ws || ws_bytes < L.total)
     return fail(CP_ERR_WORKSPACE, "workspace smaller than cp_attn_bwd_workspace_size()");
   if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0)
@@ -713,13 +720,17 @@ cp_status_t cp_attn_bwd_gqa(const void* q, const void* k, const void* v, const v
   float* Dd = reinterpret_cast<float*>(w + L.D);
   float* lse2 = reinterpret_cast<float*>(w + L.lse2);
   CP_CUDA(cudaMemsetAsync(w + L.status, 0, kStatusBytes, st), "clear status");
-  // tensor cores: one launch over the all-steps plan; CUDA cores: per step
-  const std::vector<BwdItem>& bitems = tc ? ps->bwd_fused.items : ps->bwd.items;
+  // tensor cores: one launch over the all-steps plan; CUDA cores: per step.
+  // Without per-rank prefix gradients the tensor-core plan sums each prefix
+  // key tile's rank terms on chip (one item, natural rows): no slots, no
+  // separate sum.
+  const bool slots_used = !tc || pgrad != nullptr;
+  const FusedBwdPlan& fb = pgrad ? ps->bwd_fused : ps->bwd_fused_merged;
+  const std::vector<BwdItem>& bitems = tc ? fb.items : ps->bwd.items;
   CP_CUDA(stager().upload(w + L.items, bitems.data(), bitems.size() * sizeof(BwdItem), st),
           "upload work list");
   if (tc)
-    CP_CUDA(stager().upload(w + L.runs, ps->bwd_fused.runs.data(),
-                            ps->bwd_fused.runs.size() * sizeof(Seg), st),
+    CP_CUDA(stager().upload(w + L.runs, fb.runs.data(), fb.runs.size() * sizeof(Seg), st),
             "upload run list");
   CP_CUDA(stager().upload(w + L.cu, pb.cu.data(), pb.cu.size() * 4, st), "upload cu_seqlens");
   const int64_t pitch = ld_pitch(T);
@@ -759,7 +770,7 @@ cp_status_t cp_attn_bwd_gqa(const void* q, const void* k, const void* v, const v
     if (kv_split > 1) {
       CP_CUDA(cudaMemsetAsync(dk, 0, (size_t)T * Hkv * d * sizeof(float), st), "clear dk");
       CP_CUDA(cudaMemsetAsync(dv, 0, (size_t)T * Hkv * d * sizeof(float), st), "clear dv");
-      if (N > 0)
+      if (N > 0 && slots_used)
         CP_CUDA(cudaMemsetAsync(slots, 0, 2 * (size_t)(P + 1) * pre_rows * Hkv * d * sizeof(float),
                                 st),
                 "clear prefix slots");
@@ -809,7 +820,7 @@ cp_status_t cp_attn_bwd_gqa(const void* q, const void* k, const void* v, const v
       CP_CUDA(launch_simt_bwd_dkdv(a, st), "backward dk/dv step");
     }
   }
-  if (N > 0) {
+  if (N > 0 && slots_used) {
     // the AllReduce of the replicated prefix gradient: fixed-order sum of slots
     ProfScope ps_(5, st);
     CP_CUDA(launch_prefix_reduce(pre_k, pre_v, P + 1, reinterpret_cast<const int32_t*>(w + L.cu),
@@ -886,12 +897,13 @@ cp_status_t cp_plan_pairs(const int32_t* cu, int n_seqs, int N, int P, int64_t* 
   FwdPlan f, f1;
   FusedFwdPlan fu;
   BwdPlan b;
-  FusedBwdPlan bu;
+  FusedBwdPlan bu, bm;
   plan_forward(pb, true, &f, kFwdPairQ);
   plan_forward(pb, true, &f1, kFwdTileQ);
   plan_forward_fused(f, P, &fu);
   plan_backward(pb, &b);
-  plan_backward_fused(b, P, 128, &bu);
+  plan_backward_fused(b, P, 128, false, &bu);
+  plan_backward_fused(b, P, 128, true, &bm);
   auto run_pairs = [](const Seg& sg, int q_len) {
     int64_t n = 0;
     for (int t = 0; t < q_len; ++t)
@@ -915,13 +927,17 @@ cp_status_t cp_plan_pairs(const int32_t* cu, int n_seqs, int N, int P, int64_t* 
       }
     return n;
   };
-  int64_t bwd_fused_pairs = 0, bwd_step_sum = 0;
-  std::map<std::tuple<int32_t, int32_t, int32_t>, int> seen;
-  for (const BwdItem& it : bu.items) {
-    if (it.flags != F_FIRST || it.run0 < 0 || it.run0 + it.nseg > (int64_t)bu.runs.size() ||
-        seen[std::make_tuple(it.dk_mode, it.k_row0, it.slot)]++ > 0)
-      return fail(CP_ERR_UNSUPPORTED, "all-steps backward item with a bad run range");
-    bwd_fused_pairs += key_pairs(it, bu.runs.data() + it.run0);
+  int64_t bwd_fused_pairs = 0, bwd_merged_pairs = 0, bwd_step_sum = 0;
+  for (const FusedBwdPlan* plan : {&bu, &bm}) {
+    std::map<std::tuple<int32_t, int32_t, int32_t>, int> seen;
+    int64_t& sum = plan == &bu ? bwd_fused_pairs : bwd_merged_pairs;
+    for (const BwdItem& it : plan->items) {
+      if (it.flags != F_FIRST || it.run0 < 0 || it.run0 + it.nseg > (int64_t)plan->runs.size() ||
+          seen[std::make_tuple(it.dk_mode, it.k_row0, it.slot)]++ > 0 ||
+          (plan == &bm && it.dk_mode != DK_TEXT))
+        return fail(CP_ERR_UNSUPPORTED, "all-steps backward item with a bad run range");
+      sum += key_pairs(it, plan->runs.data() + it.run0);
+    }
   }
   int64_t fused_pairs = 0, step_sum = 0;
   for (const FwdItem& it : fu.items) {
@@ -945,7 +961,7 @@ cp_status_t cp_plan_pairs(const int32_t* cu, int n_seqs, int N, int P, int64_t* 
   }
   if (fused_pairs != step_sum)
     return fail(CP_ERR_UNSUPPORTED, "all-steps forward items disagree with the ring steps");
-  if (bwd_fused_pairs != bwd_step_sum)
+  if (bwd_fused_pairs != bwd_step_sum || bwd_merged_pairs != bwd_step_sum)
     return fail(CP_ERR_UNSUPPORTED, "all-steps backward items disagree with the ring steps");
   return CP_OK;
 }

@@ -329,9 +329,11 @@ void plan_backward(const Problem& pb, BwdPlan* plan) {
   }
 }
 
-void plan_backward_fused(const BwdPlan& per_step, int P, int tile_q, FusedBwdPlan* out) {
+void plan_backward_fused(const BwdPlan& per_step, int P, int tile_q, bool merge_prefix_slots,
+                         FusedBwdPlan* out) {
   // group the per-step items by destination (text key tile, or prefix key
-  // tile and slot), keeping ring-step order
+  // tile and slot, or prefix key tile alone when the slots merge), keeping
+  // ring-step order
   struct Acc {
     BwdItem head;
     std::vector<Seg> segs;
@@ -340,7 +342,12 @@ void plan_backward_fused(const BwdPlan& per_step, int P, int tile_q, FusedBwdPla
   std::map<std::tuple<int32_t, int32_t, int32_t>, size_t> where;  // (dk_mode, k_row0, slot)
   for (int s = 0; s < P; ++s) {
     for (int x = per_step.step_begin[s]; x < per_step.step_begin[s + 1]; ++x) {
-      const BwdItem& it = per_step.items[x];
+      BwdItem it = per_step.items[x];
+      if (merge_prefix_slots && it.dk_mode == DK_PREFIX_SLOT) {
+        it.dk_mode = DK_TEXT;   // the summed prefix gradient, at its natural rows
+        it.dk_row0 = it.k_row0;
+        it.slot = 0;
+      }
       const auto key = std::make_tuple(it.dk_mode, it.k_row0, it.slot);
       auto f = where.find(key);
       if (f == where.end()) {

@@ -130,10 +130,16 @@ void plan_backward(const Problem& pb, BwdPlan* plan);
 // 0..P-1, so that dK / dV accumulate on chip across the steps and are written
 // once (flags = F_FIRST).  Items: nseg runs from run0 in `runs`; n_tiles =
 // query tiles of tile_q rows (the cost); heaviest first.
+// merge_prefix_slots = false: a prefix key tile has one item per slot (rank
+// 0..P-1, and P for the prefix queries), written to its slot for the
+// fixed-order sum that follows.  true: the slots' runs join one item that
+// writes the summed prefix dK / dV straight to its natural rows (DK_TEXT):
+// the same sum, taken on chip in the item's run order.
 struct FusedBwdPlan {
   std::vector<BwdItem> items;
   std::vector<Seg> runs;
 };
-void plan_backward_fused(const BwdPlan& per_step, int P, int tile_q, FusedBwdPlan* out);
+void plan_backward_fused(const BwdPlan& per_step, int P, int tile_q, bool merge_prefix_slots,
+                         FusedBwdPlan* out);
 
 }  // namespace cpattn
