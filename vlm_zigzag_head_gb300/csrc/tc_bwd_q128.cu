@@ -7,8 +7,9 @@
 // query head that reads this KV head (page "context-parallel-multimodal"
 // §4.2: each rank differentiates its queries against the KV it saw; the KV
 // owner receives dK/dV, here summed on chip over the steps and written once;
-// the replicated prefix gets one gradient per rank, one item per slot).  Per
-// 128-row query tile i, with the final lse:
+// the replicated prefix gets one gradient per rank: one item per slot when
+// the per-rank terms are kept, else one item that walks every rank's queries
+// and writes their sum).  Per 128-row query tile i, with the final lse:
 //
 //   S^T  = K Q^T          dP^T = V dO^T                          (TMEM)
 //   P^T  = exp2(S^T * scale*log2e - lse2),  dS^T = P^T (dP^T - D)  (registers)
